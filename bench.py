@@ -1,0 +1,429 @@
+"""Benchmark of one decode step (attention + output projection) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one decode_attn_fwd call (the split-KV attention kernel, then the
+projection kernel) over one batch of synthetic inputs resident in HBM. The
+default workload is b8_h32x8_l8k (batch 8, 32 query / 8 KV heads, kv_len
+8192, hidden 4096). Consecutive steps read different copies of the inputs
+(rotated sets, more than twice the L2 between reuses), so no step hits data a
+previous step left in L2. Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (a bounded
+sample of the same workload per step); it is the reference arm of this method.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attn+o_proj µs/step and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+DEFAULT_WORKLOAD = "b8_h32x8_l8k"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["attn_decode.cu", "ptx.cuh", "kernels.h"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle baseline leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo")  # timing barrier and max only; no data-path collective
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------- clocks
+_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+            0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting", 0x10: "sync_boost"}
+
+
+class ClockSampler:
+    """Samples the SM clock and the clock-event reasons through NVML (read only),
+    falling back to `nvidia-smi -lms`, while the timed region runs."""
+
+    def __init__(self, uuid: str | None):
+        self.samples = []  # (t, sm_mhz, reasons bitmask or names)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+        self._nvml = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            if uuid and nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0:
+                pass
+            elif nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._nvml, self._h = nv, h
+        except OSError:
+            self._nvml = None
+
+    def _run(self):
+        nv, h = self._nvml, self._h
+        mhz, reasons = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(reasons))
+                self.samples.append((t, float(mhz.value), int(reasons.value) if r == 0 else 0))
+            time.sleep(0.002)
+
+    def start(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        else:
+            try:
+                self._t0 = time.perf_counter()
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-i", "0", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self._proc = None
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+        if self._proc is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate(timeout=10)
+            for line in out.strip().splitlines():
+                try:
+                    sm, mx, rs = [s.strip() for s in line.split(",")]
+                    self.max_mhz = float(mx)
+                    self.samples.append((0.0, float(sm), int(rs, 16)))
+                except ValueError:
+                    continue
+
+    def summary(self, t0=None, t1=None):
+        s = [x for x in self.samples if t0 is None or (t0 <= x[0] <= t1)] or self.samples
+        if not s:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        bits = 0
+        for x in s:
+            bits |= x[2]
+        return {"sm_mhz": statistics.median(x[1] for x in s), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(name for b, name in _REASONS.items() if bits & b), "samples": len(s),
+                "source": "nvml" if self._nvml is not None else "nvidia-smi"}
+
+
+# ------------------------------------------------------------------ helpers
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha1()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "decode_attention_output_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary,
+    valid only while the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "attn_decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def oracle_baseline(x_host: dict, w, rows, budget_s: float):
+    """Times the fp64 oracle on host copies of `rows` batch rows; returns a dict."""
+    import numpy as np
+
+    import oracle
+    from decode_attention_output_gb300 import synth
+
+    orc = oracle.default()
+    lens = x_host["seq_lens"][rows].numpy().astype(np.int32)
+    args = (synth.to_bits(x_host["q"][rows]), synth.to_bits(x_host["k_cache"][rows]),
+            synth.to_bits(x_host["v_cache"][rows]), lens, synth.to_bits(x_host["o_weight"]), x_host["scale"])
+    sub = synth.Workload("sample", B=len(rows), Hq=w.Hq, Hkv=w.Hkv, Lcap=w.Lcap, N=w.N)
+    nbytes = synth.algorithmic_bytes(sub, lens)["total"]
+    orc.decode(*args)  # warm-up
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < 3 or (time.perf_counter() - t_start < budget_s and len(times) < 1000):
+        t0 = time.perf_counter()
+        orc.decode(*args)
+        times.append(time.perf_counter() - t0)
+    sec = statistics.median(times)
+    return {"value": nbytes / sec / 1e9, "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+            "sample": f"batch rows {list(rows)} of {w.name} (attention of all heads + o_proj of those rows), "
+                      f"median of {len(times)} runs, {sec * 1e3:.1f} ms per run",
+            "us_per_sample": sec * 1e6}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import torch
+
+    from decode_attention_output_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    rows = [0]
+    sub = synth.Workload(w.name, B=len(rows), Hq=w.Hq, Hkv=w.Hkv, Lcap=w.Lcap, N=w.N, lens=w.lens,
+                         ragged_lo=w.ragged_lo, ragged_hi=w.ragged_hi, k_mult=w.k_mult)
+    x = synth.make_inputs(sub, seed=args.seed, device="cpu")
+    import numpy as np
+
+    import oracle
+
+    orc = oracle.default()
+    lens = x["seq_lens"].numpy().astype(np.int32)
+    a = (synth.to_bits(x["q"]), synth.to_bits(x["k_cache"]), synth.to_bits(x["v_cache"]), lens,
+         synth.to_bits(x["o_weight"]), x["scale"])
+    for _ in range(args.warmup):
+        orc.decode(*a)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.decode(*a)
+    sec = (time.perf_counter() - t0) / max(1, args.steps)
+    nbytes = synth.algorithmic_bytes(sub, lens)["total"]
+    val = nbytes / sec / 1e9
+    line = {"metric": METRIC, "value": val, "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "us_per_step": sec * 1e6,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "sample_rows": rows, "B": w.B, "Hq": w.Hq,
+                                            "Hkv": w.Hkv, "kv_len": w.Lcap, "hidden": w.N},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+                             "sample": f"batch row 0 of {w.name} per step (all heads + o_proj of that row)"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# -------------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import torch
+
+    import decode_attention_output_gb300 as da
+    from decode_attention_output_gb300 import build, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    da.load()
+    w = synth.WORKLOADS[args.workload]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+
+    base = synth.make_inputs(w, seed=args.seed + 1000 * rank, device=dev)
+    lens = base["seq_lens"]
+    nb = synth.algorithmic_bytes(w, lens.cpu())
+    set_bytes = sum(base[k].numel() * base[k].element_size() for k in ("q", "k_cache", "v_cache", "o_weight"))
+    n_sets = max(2, math.ceil(2.5 * l2 / max(1, nb["total"])))
+    sets = [base] + [synth.make_inputs(w, seed=args.seed + 1000 * rank + i, device=dev) for i in range(1, n_sets)]
+    for s in sets:
+        s["seq_lens"] = lens  # same lengths for every set (ragged draw is per seed)
+    outs = [torch.empty((w.B, w.N), dtype=torch.bfloat16, device=dev) for _ in range(n_sets)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        s = sets[i % n_sets]
+        da.decode_attn_fwd(s["q"], s["k_cache"], s["v_cache"], s["seq_lens"], s["o_weight"], outs[i % n_sets],
+                           s["scale"], stream=stream)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    assert da.decode_attn_device_error(stream) == 0
+
+    uuid = str(getattr(props, "uuid", "")) or None
+    if uuid and not uuid.startswith("GPU-"):
+        uuid = "GPU-" + uuid
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.05)
+
+    # ---- timed region: exactly K steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.perf_counter()
+    barrier(world)
+    step_ms = ev0.elapsed_time(ev1) / args.steps
+    sampler_window = (t_wall0, t_wall1)
+
+    # ---- dominant kernel (split-KV attention) timed alone, per launch, same inputs and plan
+    attn_bufs = [torch.empty((w.B, w.Hq, 128), dtype=torch.bfloat16, device=dev) for _ in range(n_sets)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        s = sets[i % n_sets]
+        evs[i][0].record(stream)
+        da.decode_attn_only(s["q"], s["k_cache"], s["v_cache"], s["seq_lens"], attn_bufs[i % n_sets], s["scale"],
+                            stream=stream)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.stop()
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    assert da.decode_attn_device_error(stream) == 0
+
+    step_ms_max = max_over_ranks(world, step_ms)
+    total_bytes = sum_over_ranks(world, float(nb["total"]))
+    value = total_bytes / (step_ms_max * 1e-3) / 1e9
+    peak, peak_src = measured_hbm_peak()
+    attn_bytes = nb["kv"] + w.B * w.Hq * 128 * 2 * 2  # K+V of valid tokens + q in + attention out
+    achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(w.name)
+
+    # ---- end to end through the C ABI from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: base[k].cpu().pin_memory() for k in ("q", "k_cache", "v_cache", "o_weight", "seq_lens")}
+        dbuf = {k: torch.empty_like(base[k]) for k in host}
+        out_h = torch.empty((w.B, w.N), dtype=torch.bfloat16).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+        n_e2e = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            for k in host:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            da.decode_attn_fwd(dbuf["q"], dbuf["k_cache"], dbuf["v_cache"], dbuf["seq_lens"], dbuf["o_weight"],
+                               outs[0], base["scale"], stream=stream)
+            out_h.copy_(outs[0], non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+
+        e2e_step()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        e2e_s = max_over_ranks(world, (time.perf_counter() - t0) / n_e2e)
+        e2e = {"value": total_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "us_per_step": e2e_s * 1e6, "steps": n_e2e,
+               "note": "all inputs (q, K/V caches, W_o, seq_lens) copied host->device every step"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        x_host = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in base.items()}
+        cpu = oracle_baseline(x_host, w, rows=[0], budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        clocks = sampler.summary(*sampler_window)
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms_max, "us_per_step": step_ms_max * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "kv_len": w.Lcap, "hidden": w.N,
+                       "seq_lens_sum": int(lens.sum().item()), "bytes_per_step": nb,
+                       "l2": f"{n_sets} rotated input sets of {set_bytes / 1e6:.0f} MB (>2x L2 between reuses)",
+                       "step_hbm_frac": value / world / peak, "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "attn_decode_kernel", "achieved": achieved, "peak": peak,
+                         "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": attn_bytes,
+                         "us_per_launch": attn_ms * 1e3},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,162 @@
+"""ctypes binding of libdecode_attn.so (include/decode_attn.h), same names as the C ABI.
+
+Argument marshalling only: each function turns ``torch.Tensor`` arguments into
+``da_tensor_t`` descriptors (data pointer, dtype, shape, strides in elements),
+passes the current CUDA stream, and raises :class:`DecodeAttnError` on a
+nonzero status. Every step of the computation runs in the library's kernels.
+The library must have been built (``decode_attention_output_gb300.build``);
+there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+DA_DTYPE_BF16, DA_DTYPE_F32, DA_DTYPE_I32 = 1, 2, 3
+_DTYPES = {torch.bfloat16: DA_DTYPE_BF16, torch.float32: DA_DTYPE_F32, torch.int32: DA_DTYPE_I32}
+
+# every symbol declared in include/decode_attn.h
+EXPORTS = ("decode_attn_fwd", "decode_attn_only", "decode_attn_scores", "decode_attn_oproj",
+           "decode_attn_set_option", "decode_attn_get_option", "decode_attn_device_error",
+           "decode_attn_release", "decode_attn_status_str")
+
+
+class da_tensor_t(ctypes.Structure):  # noqa: N801 - mirrors the C name
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class DecodeAttnError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} (status {code})")
+        self.code = code
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Loads the library (once). Fails loudly if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = path or _build.lib_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: run decode_attention_output_gb300.build.build() first")
+            lib = ctypes.CDLL(path)
+            P = ctypes.POINTER(da_tensor_t)
+            vp, f32, i64 = ctypes.c_void_p, ctypes.c_float, ctypes.c_int64
+            lib.decode_attn_fwd.argtypes = [P, P, P, P, P, P, f32, vp]
+            lib.decode_attn_only.argtypes = [P, P, P, P, P, f32, vp]
+            lib.decode_attn_scores.argtypes = [P, P, P, P, vp]
+            lib.decode_attn_oproj.argtypes = [P, P, P, vp]
+            lib.decode_attn_set_option.argtypes = [ctypes.c_char_p, i64]
+            lib.decode_attn_get_option.argtypes = [ctypes.c_char_p, ctypes.POINTER(i64)]
+            lib.decode_attn_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+            lib.decode_attn_release.argtypes = []
+            lib.decode_attn_release.restype = None
+            lib.decode_attn_status_str.argtypes = [ctypes.c_int]
+            lib.decode_attn_status_str.restype = ctypes.c_char_p
+            for name in EXPORTS:
+                if name not in ("decode_attn_release", "decode_attn_status_str"):
+                    getattr(lib, name).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def describe(t: torch.Tensor | None) -> da_tensor_t | None:
+    """da_tensor_t view of a tensor (no copy)."""
+    if t is None:
+        return None
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    if t.dim() > 4:
+        raise ValueError("at most 4 dimensions")
+    d = da_tensor_t()
+    d.data = t.data_ptr() if t.numel() else None
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _ref(d):
+    return ctypes.byref(d) if d is not None else None
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(fn: str, code: int) -> None:
+    if code != 0:
+        raise DecodeAttnError(fn, code, status_str(code))
+
+
+def status_str(code: int) -> str:
+    return load().decode_attn_status_str(int(code)).decode()
+
+
+def decode_attn_fwd(q, k_cache, v_cache, seq_lens, o_weight, out, scale: float, stream=None) -> torch.Tensor:
+    """out[B, N] = (softmax(scale * q K^T) V)_flat . o_weight; returns ``out``."""
+    lib = load()
+    ds = [describe(x) for x in (q, k_cache, v_cache, seq_lens, o_weight, out)]
+    _check("decode_attn_fwd", lib.decode_attn_fwd(*[_ref(d) for d in ds], float(scale), _stream(stream)))
+    return out
+
+
+def decode_attn_only(q, k_cache, v_cache, seq_lens, attn_out, scale: float, stream=None) -> torch.Tensor:
+    """attn_out[B, Hq, 128] = softmax(scale * q K^T) V (bf16); returns ``attn_out``."""
+    lib = load()
+    ds = [describe(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
+    _check("decode_attn_only", lib.decode_attn_only(*[_ref(d) for d in ds], float(scale), _stream(stream)))
+    return attn_out
+
+
+def decode_attn_scores(q, k_cache, seq_lens, scores, stream=None) -> torch.Tensor:
+    """scores[B, Hq, Lcap] (fp32) = q K^T for t < seq_lens[b]; returns ``scores``."""
+    lib = load()
+    ds = [describe(x) for x in (q, k_cache, seq_lens, scores)]
+    _check("decode_attn_scores", lib.decode_attn_scores(*[_ref(d) for d in ds], _stream(stream)))
+    return scores
+
+
+def decode_attn_oproj(attn_flat, o_weight, out, stream=None) -> torch.Tensor:
+    """out[B, N] = attn_flat[B, K] . o_weight[K, N] (bf16); returns ``out``."""
+    lib = load()
+    ds = [describe(x) for x in (attn_flat, o_weight, out)]
+    _check("decode_attn_oproj", lib.decode_attn_oproj(*[_ref(d) for d in ds], _stream(stream)))
+    return out
+
+
+def decode_attn_set_option(key: str, value: int) -> None:
+    _check("decode_attn_set_option", load().decode_attn_set_option(key.encode(), int(value)))
+
+
+def decode_attn_get_option(key: str) -> int:
+    v = ctypes.c_int64(0)
+    _check("decode_attn_get_option", load().decode_attn_get_option(key.encode(), ctypes.byref(v)))
+    return int(v.value)
+
+
+def decode_attn_device_error(stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device error word."""
+    code = ctypes.c_int32(0)
+    _check("decode_attn_device_error", load().decode_attn_device_error(_stream(stream), ctypes.byref(code)))
+    return int(code.value)
+
+
+def decode_attn_release() -> None:
+    load().decode_attn_release()

@@ -1,0 +1,475 @@
+// api.cu -- the C ABI declared in include/decode_attn.h: argument validation,
+// the per-device workspace, TMA descriptor encoding, launch planning and dispatch.
+// No arithmetic of the method happens here; every step runs in the kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "decode_attn.h"
+#include "kernels.h"
+
+namespace {
+
+using namespace da;
+
+// ------------------------------------------------------------------ options
+struct Options {
+  int64_t attn_ctas = 0;
+  int64_t oproj_path = 0;  // 0 auto, 1 gemv, 2 tcgen05
+  int64_t oproj_splitk = 0;
+  int64_t gemm_min_batch = 1 << 30;  // auto mode keeps the GEMV until the GEMM path is enabled
+  int64_t pdl = 1;
+};
+std::mutex g_mu;
+Options g_opt;
+
+Options options_snapshot() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_opt;
+}
+
+// ---------------------------------------------------------------- workspace
+// Fixed header (zeroed once when allocated, kept at zero by the kernels):
+//   [0, 256)                      device error word
+//   [256, 256 + 256 KiB)          attention completion counters (B*Hkv <= 65536)
+//   [.., + 256 KiB)               projection completion counters
+// followed by per-call scratch laid out by the caller.
+constexpr size_t kMaxCounters = 65536;
+constexpr size_t kErrOff = 0;
+constexpr size_t kAttnCntOff = 256;
+constexpr size_t kGemvCntOff = kAttnCntOff + kMaxCounters * 4;
+constexpr size_t kHeaderBytes = kGemvCntOff + kMaxCounters * 4;
+constexpr int kMaxDevices = 64;
+
+struct Workspace {
+  char* base = nullptr;
+  size_t bytes = 0;
+};
+Workspace g_ws[kMaxDevices];
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Returns the workspace of the current device with at least `scratch` bytes after
+// the header, growing it if needed (growth synchronises the device).
+int workspace_get(size_t scratch, cudaStream_t stream, char** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace& ws = g_ws[dev];
+  const size_t need = kHeaderBytes + align_up(scratch, 256);
+  if (need > ws.bytes) {
+    if (ws.base) {
+      if (cudaDeviceSynchronize() != cudaSuccess) return DA_ERR_CUDA;
+      cudaFree(ws.base);
+      ws.base = nullptr;
+      ws.bytes = 0;
+    }
+    const size_t bytes = std::max(need, (size_t)32 << 20);
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return DA_ERR_NOMEM;
+    }
+    if (cudaMemsetAsync(p, 0, kHeaderBytes, stream) != cudaSuccess) {
+      cudaFree(p);
+      return DA_ERR_CUDA;
+    }
+    ws.base = static_cast<char*>(p);
+    ws.bytes = bytes;
+  }
+  *out = ws.base;
+  return DA_OK;
+}
+
+// --------------------------------------------------------------- device info
+int sm_count() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// ------------------------------------------------------------ TMA encoding
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 4-D map over a [B][Hkv][Lcap][128] bf16 cache; box = 64 dims x 64 tokens.
+int encode_kv_map(CUtensorMap* map, const da_tensor_t* t) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return DA_ERR_CUDA;
+  const int64_t B = t->shape[0], H = t->shape[1], L = t->shape[2];
+  // a stride of an extent-1 dimension is never used; give it a harmless legal value
+  const int64_t st = L == 1 ? 128 : t->stride[2];
+  const int64_t sh = H == 1 ? st * L : t->stride[1];
+  const int64_t sb = B == 1 ? sh * H : t->stride[0];
+  cuuint64_t dims[4] = {128, (cuuint64_t)L, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)st * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)kTile, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_UNSUPPORTED;
+}
+
+// --------------------------------------------------------------- validation
+enum Use { kInput16, kOutput };  // inputs feed TMA / 16-byte loads, outputs take scalar stores
+
+int elem_size(int dtype) { return dtype == DA_DTYPE_BF16 ? 2 : 4; }
+
+int check_tensor(const da_tensor_t* t, int dtype, int ndim, Use use) {
+  if (!t) return DA_ERR_NULL;
+  if (t->dtype != dtype) return DA_ERR_DTYPE;
+  if (t->ndim != ndim) return DA_ERR_SHAPE;
+  int64_t numel = 1;
+  for (int i = 0; i < ndim; ++i) {
+    if (t->shape[i] < 0) return DA_ERR_SHAPE;
+    numel *= t->shape[i];
+  }
+  if (numel == 0) return DA_OK;  // empty: the caller decides whether that is allowed
+  if (!t->data) return DA_ERR_NULL;
+  if (t->shape[ndim - 1] > 1 && t->stride[ndim - 1] != 1) return DA_ERR_STRIDE;
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(t->data);
+  if (use == kInput16) {
+    if (addr % 16) return DA_ERR_ALIGN;
+    for (int i = 0; i < ndim - 1; ++i)
+      if (t->shape[i] > 1 && (t->stride[i] <= 0 || t->stride[i] % 8)) return DA_ERR_STRIDE;
+  } else {
+    if (addr % elem_size(dtype)) return DA_ERR_ALIGN;
+    for (int i = 0; i < ndim - 1; ++i)
+      if (t->shape[i] > 1 && t->stride[i] <= 0) return DA_ERR_STRIDE;
+  }
+  return DA_OK;
+}
+
+#define DA_TRY(expr)          \
+  do {                        \
+    const int _rc = (expr);   \
+    if (_rc != DA_OK) return _rc; \
+  } while (0)
+
+struct AttnShape {
+  int B, Hq, Hkv, G, Lcap;
+};
+
+int check_attention_inputs(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t* v,
+                           const da_tensor_t* lens, bool need_v, AttnShape* s) {
+  DA_TRY(check_tensor(q, DA_DTYPE_BF16, 3, kInput16));
+  DA_TRY(check_tensor(k, DA_DTYPE_BF16, 4, kInput16));
+  if (need_v) DA_TRY(check_tensor(v, DA_DTYPE_BF16, 4, kInput16));
+  if (!lens) return DA_ERR_NULL;
+  if (lens->dtype != DA_DTYPE_I32) return DA_ERR_DTYPE;
+  if (lens->ndim != 1) return DA_ERR_SHAPE;
+  const int64_t B = q->shape[0], Hq = q->shape[1], Hkv = k->shape[1], Lcap = k->shape[2];
+  if (q->shape[2] != kHeadDim || k->shape[3] != kHeadDim) return DA_ERR_SHAPE;
+  if (k->shape[0] != B || lens->shape[0] != B) return DA_ERR_SHAPE;
+  if (need_v)
+    for (int i = 0; i < 4; ++i)
+      if (v->shape[i] != k->shape[i]) return DA_ERR_SHAPE;
+  if (B > 0) {
+    if (!lens->data) return DA_ERR_NULL;
+    if (B > 1 && lens->stride[0] != 1) return DA_ERR_STRIDE;
+    if (reinterpret_cast<uintptr_t>(lens->data) % 4) return DA_ERR_ALIGN;
+  }
+  if (Hq <= 0 || Hkv <= 0 || Lcap <= 0) return DA_ERR_SHAPE;
+  if (Hq % Hkv) return DA_ERR_SHAPE;
+  if (Hq / Hkv > kMaxGroup) return DA_ERR_UNSUPPORTED;
+  if (B > DA_MAX_BATCH) return DA_ERR_UNSUPPORTED;
+  if (B * Hkv > (int64_t)kMaxCounters) return DA_ERR_UNSUPPORTED;
+  if (Lcap > (int64_t)1 << 30) return DA_ERR_UNSUPPORTED;
+  if (B * Hkv * ((Lcap + kTile - 1) / kTile) >= ((int64_t)1 << 31)) return DA_ERR_UNSUPPORTED;
+  s->B = (int)B;
+  s->Hq = (int)Hq;
+  s->Hkv = (int)Hkv;
+  s->G = (int)(Hq / Hkv);
+  s->Lcap = (int)Lcap;
+  return DA_OK;
+}
+
+// ------------------------------------------------------------------ planning
+struct AttnPlan {
+  int grid, nb, gpad;
+  size_t part_o_off, part_ml_off, bytes;
+};
+
+AttnPlan plan_attention(const AttnShape& s, const Options& o) {
+  AttnPlan pl;
+  const int sms = std::max(1, sm_count());
+  pl.grid = o.attn_ctas > 0 ? (int)o.attn_ctas : sms;
+  pl.nb = s.G <= 8 ? 1 : 2;
+  pl.gpad = 8 * pl.nb;
+  const size_t slots = (size_t)pl.grid + (size_t)s.B * s.Hkv;
+  pl.part_ml_off = 0;
+  pl.part_o_off = align_up(slots * pl.gpad * 2 * 4, 256);
+  pl.bytes = pl.part_o_off + align_up(slots * pl.gpad * kHeadDim * 4, 256);
+  return pl;
+}
+
+struct GemvPlan {
+  int bt, kc, ksplit, ncb, nbz;
+  size_t bytes;
+};
+
+GemvPlan plan_gemv(int B, int K, int N, const Options& o) {
+  GemvPlan pl;
+  pl.bt = B <= 1 ? 1 : (B <= 2 ? 2 : (B <= 4 ? 4 : 8));
+  pl.nbz = (B + pl.bt - 1) / pl.bt;
+  pl.ncb = (N + kGemvCols - 1) / kGemvCols;
+  const int sms = std::max(1, sm_count());
+  int ksplit = (int)o.oproj_splitk;
+  if (ksplit <= 0) {
+    const double target = 2.0 * sms;
+    ksplit = std::max(1, (int)std::lround(target / (double)(pl.ncb * pl.nbz)));
+  }
+  ksplit = std::min(ksplit, std::max(1, K / 8));
+  int kc = (int)align_up((size_t)((K + ksplit - 1) / ksplit), 8);
+  kc = std::min(kc, kGemvMaxKc);
+  pl.kc = kc;
+  pl.ksplit = (K + kc - 1) / kc;
+  pl.bytes = pl.ksplit > 1 ? align_up((size_t)pl.ksplit * B * N * 4, 256) : 0;
+  return pl;
+}
+
+int run_gemv(const __nv_bfloat16* x, long long x_sb, const da_tensor_t* w, const da_tensor_t* out, int B, int K,
+             int N, char* ws, char* scratch, const GemvPlan& pl, bool pdl, cudaStream_t stream) {
+  if (pl.nbz * pl.ncb > (int)kMaxCounters) return DA_ERR_UNSUPPORTED;
+  GemvParams gp;
+  gp.x = x;
+  gp.x_sb = x_sb;
+  gp.w = static_cast<const __nv_bfloat16*>(w->data);
+  gp.w_sk = w->stride[0];
+  gp.y = static_cast<__nv_bfloat16*>(out->data);
+  gp.y_sb = out->stride[0];
+  gp.part = reinterpret_cast<float*>(scratch);
+  gp.counters = reinterpret_cast<int*>(ws + kGemvCntOff);
+  gp.B = B;
+  gp.K = K;
+  gp.N = N;
+  gp.kc = pl.kc;
+  gp.ksplit = pl.ksplit;
+  return launch_gemv(gp, pl.bt, pdl, stream) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t* v, const da_tensor_t* lens,
+                  const AttnShape& s, const AttnPlan& pl, char* ws, char* scratch, __nv_bfloat16* attn,
+                  long long a_sb, long long a_sh, float* scores, long long s_sb, long long s_sh, float scale,
+                  cudaStream_t stream) {
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  DA_TRY(encode_kv_map(&p.tm_k, k));
+  if (v) DA_TRY(encode_kv_map(&p.tm_v, v));
+  else p.tm_v = p.tm_k;
+  p.q = static_cast<const __nv_bfloat16*>(q->data);
+  p.q_sb = q->stride[0];
+  p.q_sh = q->stride[1];
+  p.seq_lens = static_cast<const int*>(lens->data);
+  p.attn = attn;
+  p.a_sb = a_sb;
+  p.a_sh = a_sh;
+  p.scores = scores;
+  p.s_sb = s_sb;
+  p.s_sh = s_sh;
+  p.part_ml = reinterpret_cast<float*>(scratch + pl.part_ml_off);
+  p.part_o = reinterpret_cast<float*>(scratch + pl.part_o_off);
+  p.counters = reinterpret_cast<int*>(ws + kAttnCntOff);
+  p.err = reinterpret_cast<int*>(ws + kErrOff);
+  p.B = s.B;
+  p.Hkv = s.Hkv;
+  p.G = s.G;
+  p.Lcap = s.Lcap;
+  p.gpad = pl.gpad;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return launch_attention(p, pl.grid, pl.nb, scores != nullptr, stream) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+}  // namespace
+
+// ======================================================================= C ABI
+extern "C" {
+
+const char* decode_attn_status_str(int code) {
+  switch (code) {
+    case DA_OK: return "ok";
+    case DA_ERR_NULL: return "null pointer or descriptor";
+    case DA_ERR_DTYPE: return "wrong dtype";
+    case DA_ERR_SHAPE: return "inconsistent or unsupported shape";
+    case DA_ERR_STRIDE: return "bad stride (innermost must be 1, others multiples of 8 elements)";
+    case DA_ERR_ALIGN: return "misaligned base pointer";
+    case DA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case DA_ERR_NOMEM: return "workspace allocation failed";
+    case DA_ERR_CUDA: return "CUDA error";
+    case DA_ERR_OPTION: return "unknown option or bad value";
+    case DA_ERR_DEVICE: return "device-side error recorded";
+    default: return "unknown status";
+  }
+}
+
+int decode_attn_set_option(const char* key, int64_t value) {
+  if (!key) return DA_ERR_OPTION;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!strcmp(key, "attn_ctas") && value >= 0 && value <= 65535) g_opt.attn_ctas = value;
+  else if (!strcmp(key, "oproj_path") && value >= 0 && value <= 2) g_opt.oproj_path = value;
+  else if (!strcmp(key, "oproj_splitk") && value >= 0 && value <= 4096) g_opt.oproj_splitk = value;
+  else if (!strcmp(key, "gemm_min_batch") && value >= 1) g_opt.gemm_min_batch = value;
+  else if (!strcmp(key, "pdl") && (value == 0 || value == 1)) g_opt.pdl = value;
+  else return DA_ERR_OPTION;
+  return DA_OK;
+}
+
+int decode_attn_get_option(const char* key, int64_t* value) {
+  if (!key || !value) return DA_ERR_OPTION;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!strcmp(key, "attn_ctas")) *value = g_opt.attn_ctas;
+  else if (!strcmp(key, "oproj_path")) *value = g_opt.oproj_path;
+  else if (!strcmp(key, "oproj_splitk")) *value = g_opt.oproj_splitk;
+  else if (!strcmp(key, "gemm_min_batch")) *value = g_opt.gemm_min_batch;
+  else if (!strcmp(key, "pdl")) *value = g_opt.pdl;
+  else return DA_ERR_OPTION;
+  return DA_OK;
+}
+
+int decode_attn_only(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
+                     const da_tensor_t* seq_lens, const da_tensor_t* attn_out, float scale, void* stream) {
+  AttnShape s;
+  DA_TRY(check_attention_inputs(q, k_cache, v_cache, seq_lens, true, &s));
+  DA_TRY(check_tensor(attn_out, DA_DTYPE_BF16, 3, kOutput));
+  if (attn_out->shape[0] != s.B || attn_out->shape[1] != s.Hq || attn_out->shape[2] != kHeadDim)
+    return DA_ERR_SHAPE;
+  if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
+  if (s.B == 0) return DA_OK;
+  const Options o = options_snapshot();
+  const AttnPlan pl = plan_attention(s, o);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = nullptr;
+  DA_TRY(workspace_get(pl.bytes, st, &ws));
+  return run_attention(q, k_cache, v_cache, seq_lens, s, pl, ws, ws + kHeaderBytes,
+                       static_cast<__nv_bfloat16*>(attn_out->data), attn_out->stride[0], attn_out->stride[1],
+                       nullptr, 0, 0, scale, st);
+}
+
+int decode_attn_scores(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* seq_lens,
+                       const da_tensor_t* scores, void* stream) {
+  AttnShape s;
+  DA_TRY(check_attention_inputs(q, k_cache, nullptr, seq_lens, false, &s));
+  DA_TRY(check_tensor(scores, DA_DTYPE_F32, 3, kOutput));
+  if (scores->shape[0] != s.B || scores->shape[1] != s.Hq || scores->shape[2] != s.Lcap) return DA_ERR_SHAPE;
+  if (s.B == 0) return DA_OK;
+  const Options o = options_snapshot();
+  const AttnPlan pl = plan_attention(s, o);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = nullptr;
+  DA_TRY(workspace_get(pl.bytes, st, &ws));
+  return run_attention(q, k_cache, nullptr, seq_lens, s, pl, ws, ws + kHeaderBytes, nullptr, 0, 0,
+                       static_cast<float*>(scores->data), scores->stride[0], scores->stride[1], 1.0f, st);
+}
+
+int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight, const da_tensor_t* out,
+                      void* stream) {
+  DA_TRY(check_tensor(attn_flat, DA_DTYPE_BF16, 2, kInput16));
+  DA_TRY(check_tensor(o_weight, DA_DTYPE_BF16, 2, kInput16));
+  DA_TRY(check_tensor(out, DA_DTYPE_BF16, 2, kOutput));
+  const int64_t B = attn_flat->shape[0], K = attn_flat->shape[1], N = o_weight->shape[1];
+  if (o_weight->shape[0] != K || out->shape[0] != B || out->shape[1] != N) return DA_ERR_SHAPE;
+  if (B == 0) return DA_OK;
+  if (K <= 0 || N <= 0 || K % 8 || N % 8) return DA_ERR_SHAPE;
+  if (K > (1 << 30) || N > (1 << 30)) return DA_ERR_UNSUPPORTED;
+  const Options o = options_snapshot();
+  const GemvPlan pl = plan_gemv((int)B, (int)K, (int)N, o);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = nullptr;
+  DA_TRY(workspace_get(pl.bytes, st, &ws));
+  return run_gemv(static_cast<const __nv_bfloat16*>(attn_flat->data), attn_flat->stride[0], o_weight, out, (int)B,
+                  (int)K, (int)N, ws, ws + kHeaderBytes, pl, false, st);
+}
+
+int decode_attn_fwd(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
+                    const da_tensor_t* seq_lens, const da_tensor_t* o_weight, const da_tensor_t* out, float scale,
+                    void* stream) {
+  AttnShape s;
+  DA_TRY(check_attention_inputs(q, k_cache, v_cache, seq_lens, true, &s));
+  DA_TRY(check_tensor(o_weight, DA_DTYPE_BF16, 2, kInput16));
+  DA_TRY(check_tensor(out, DA_DTYPE_BF16, 2, kOutput));
+  const int64_t K = (int64_t)s.Hq * kHeadDim, N = o_weight->shape[1];
+  if (o_weight->shape[0] != K || out->shape[0] != s.B || out->shape[1] != N) return DA_ERR_SHAPE;
+  if (N <= 0 || N % 8) return DA_ERR_SHAPE;
+  if (N > (1 << 30) || K > (1 << 30)) return DA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
+  if (s.B == 0) return DA_OK;
+  const Options o = options_snapshot();
+  const AttnPlan ap = plan_attention(s, o);
+  const GemvPlan gp = plan_gemv(s.B, (int)K, (int)N, o);
+  const size_t attn_bytes = align_up((size_t)s.B * K * 2, 256);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = nullptr;
+  DA_TRY(workspace_get(ap.bytes + attn_bytes + gp.bytes, st, &ws));
+  char* scratch = ws + kHeaderBytes;
+  __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(scratch + ap.bytes);
+  DA_TRY(run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, kHeadDim, nullptr, 0, 0, scale,
+                       st));
+  return run_gemv(attn, K, o_weight, out, s.B, (int)K, (int)N, ws, scratch + ap.bytes + attn_bytes, gp, o.pdl != 0,
+                  st);
+}
+
+int decode_attn_device_error(void* stream, int32_t* host_code) {
+  if (!host_code) return DA_ERR_NULL;
+  *host_code = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return DA_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DA_ERR_CUDA;
+  char* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    base = g_ws[dev].base;
+  }
+  if (!base) return DA_OK;
+  int32_t code = 0;
+  if (cudaMemcpy(&code, base + kErrOff, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) return DA_ERR_CUDA;
+  if (code && cudaMemset(base + kErrOff, 0, sizeof(code)) != cudaSuccess) return DA_ERR_CUDA;
+  *host_code = code;
+  return DA_OK;
+}
+
+void decode_attn_release(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (int d = 0; d < kMaxDevices; ++d) {
+    if (!g_ws[d].base) continue;
+    if (cudaSetDevice(d) == cudaSuccess) {
+      cudaDeviceSynchronize();
+      cudaFree(g_ws[d].base);
+    }
+    g_ws[d].base = nullptr;
+    g_ws[d].bytes = 0;
+  }
+  cudaSetDevice(cur);
+}
+
+}  // extern "C"

@@ -1,0 +1,166 @@
+/*
+ * decode_attn.h -- C ABI of libdecode_attn.so: one decode step of grouped-query
+ * attention over a bf16 KV cache, followed by the output projection, on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The computation is the one of the page "PyPTO 开箱性能调优实战 Decode
+ * Attention 多 Matmul 独立 TileShape 配置 F-16" (eliteato.com/news/26629),
+ * section "代码对比": three contractions with their own result types
+ *
+ *   scores_fp32 = q_grouped . k_cache^T                 (fp32 scores)
+ *   weights     = softmax(scale * scores_fp32)          (the "vector ops")
+ *   attn_output = weights . v_cache                     (bf16)
+ *   result      = attn_output_flat . o_weight           (bf16)
+ *
+ * and the shapes of its table "三个 Matmul 的 Shape 特征分析" (QK^T: M = query
+ * heads per KV head, K = head_dim = 128, N = kv_len; attn.V: M = heads per KV
+ * head, K = kv_len, N = 128; output_proj: M = batch, K = heads * 128,
+ * N = hidden).
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor argument is a da_tensor_t descriptor. Its data pointer is a
+ *    DEVICE pointer owned by the caller; the library never frees or keeps it.
+ *  - Strides are in elements. The innermost dimension must be contiguous
+ *    (stride 1); every other stride must be a multiple of 8 elements and every
+ *    base pointer 16-byte aligned (TMA and 16-byte vector loads need it).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Every call only enqueues work on it and returns; nothing is
+ *    synchronised, nothing is copied back to the host.
+ *  - All arguments are validated on the host before anything is launched; on
+ *    a failure the call returns a negative da_status_t and launches nothing.
+ *    A failed launch returns DA_ERR_CUDA.
+ *  - The library owns one workspace per device (partial results of the split
+ *    KV pass and of the split-K projection, completion counters, the bf16
+ *    attention intermediate). It is grown with cudaMalloc when a call needs
+ *    more, so the first call with the largest shapes should precede any CUDA
+ *    graph capture. Calls that run concurrently on different streams of the
+ *    same device share it and must not overlap.
+ *  - seq_lens lives on the device. Each length is clamped to [0, Lcap] on the
+ *    device; a length of 0 gives an all-zero attention row.
+ *  - Bounded device waits: every wait inside a kernel gives up after about
+ *    two seconds and records a code that decode_attn_device_error() returns.
+ */
+#ifndef DECODE_ATTN_H
+#define DECODE_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types of da_tensor_t.dtype. */
+enum { DA_DTYPE_BF16 = 1, DA_DTYPE_F32 = 2, DA_DTYPE_I32 = 3 };
+
+/* A strided view of caller-owned device memory (DLPack-like). */
+typedef struct da_tensor {
+  void* data;        /* device pointer */
+  int32_t dtype;     /* DA_DTYPE_* */
+  int32_t ndim;      /* number of valid entries in shape/stride, 1..4 */
+  int64_t shape[4];
+  int64_t stride[4]; /* in elements */
+} da_tensor_t;
+
+typedef enum {
+  DA_OK = 0,
+  DA_ERR_NULL = -1,        /* a required pointer or descriptor is NULL */
+  DA_ERR_DTYPE = -2,       /* wrong element type */
+  DA_ERR_SHAPE = -3,       /* inconsistent or unsupported shape */
+  DA_ERR_STRIDE = -4,      /* innermost dim not contiguous, or a stride not a multiple of 8 */
+  DA_ERR_ALIGN = -5,       /* base pointer not 16-byte aligned */
+  DA_ERR_UNSUPPORTED = -6, /* valid request outside what the kernels implement */
+  DA_ERR_NOMEM = -7,       /* the workspace could not be grown */
+  DA_ERR_CUDA = -8,        /* a CUDA runtime call or launch failed */
+  DA_ERR_OPTION = -9,      /* unknown option key or value out of range */
+  DA_ERR_DEVICE = -10      /* a kernel recorded a device-side error (bounded wait ran out) */
+} da_status_t;
+
+/* Limits checked on the host. */
+#define DA_HEAD_DIM 128  /* D: the only head_dim the kernels implement */
+#define DA_MAX_GROUP 16  /* G = Hq / Hkv */
+#define DA_MAX_BATCH 1024
+
+/*
+ * decode_attn_fwd -- the whole step: attention, then the output projection.
+ * Page: "PyPTO 开箱性能调优实战 Decode Attention 多 Matmul 独立 TileShape 配置
+ * F-16", section "代码对比" (the three matmuls) and the shape table.
+ *
+ *   q        [B, Hq, 128]        bf16  the new token's queries
+ *   k_cache  [B, Hkv, Lcap, 128] bf16  keys; token t of sequence b is row t
+ *   v_cache  [B, Hkv, Lcap, 128] bf16  values, same shape as k_cache
+ *   seq_lens [B]                 int32 valid tokens per sequence (device)
+ *   o_weight [Hq*128, N]         bf16  row-major; row k = h*128 + d
+ *   out      [B, N]              bf16  written
+ *   scale    softmax scale applied to the fp32 scores (usually 1/sqrt(128))
+ *
+ * Query head h attends with KV head h / (Hq / Hkv) over tokens t < seq_lens[b].
+ * Requires Hq % Hkv == 0, Hq / Hkv <= 16, B <= 1024, N % 8 == 0.
+ * Returns DA_OK or a negative da_status_t.
+ */
+int decode_attn_fwd(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
+                    const da_tensor_t* seq_lens, const da_tensor_t* o_weight, const da_tensor_t* out,
+                    float scale, void* stream);
+
+/*
+ * decode_attn_only -- the attention half: attn_out[b, h, :] =
+ * softmax(scale * q[b,h] . K[b, h/G]^T) . V[b, h/G] over t < seq_lens[b],
+ * written as bf16 (the page's `attn_output`, DT_BF16).
+ *   attn_out [B, Hq, 128] bf16, caller-allocated, any strides obeying the
+ *   conventions. Other arguments as decode_attn_fwd.
+ */
+int decode_attn_only(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
+                     const da_tensor_t* seq_lens, const da_tensor_t* attn_out, float scale,
+                     void* stream);
+
+/*
+ * decode_attn_scores -- the first contraction alone: the page's `scores_fp32`
+ * (q_grouped . k_cache^T, b_trans=True), unscaled, in fp32.
+ *   scores [B, Hq, Lcap] fp32: scores[b, h, t] is written for t < seq_lens[b]
+ *   only; entries at t >= seq_lens[b] are left as they were.
+ * A checking and tuning hook; it runs the attention kernel's QK^T code.
+ */
+int decode_attn_scores(const da_tensor_t* q, const da_tensor_t* k_cache,
+                       const da_tensor_t* seq_lens, const da_tensor_t* scores, void* stream);
+
+/*
+ * decode_attn_oproj -- the last contraction alone: out = attn_flat . o_weight
+ * (the page's output_proj: M = batch, K = Hq*128, N = hidden), bf16 operands,
+ * fp32 accumulation, bf16 result.
+ *   attn_flat [B, K] bf16;  o_weight [K, N] bf16 row-major;  out [B, N] bf16.
+ * Requires N % 8 == 0 and K % 8 == 0.
+ */
+int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
+                      const da_tensor_t* out, void* stream);
+
+/*
+ * Tuning options (process-wide; 0 = automatic). Keys:
+ *   "attn_ctas"     CTAs of the persistent attention kernel (0: one per SM)
+ *   "oproj_path"    0 auto, 1 CUDA-core GEMV, 2 tcgen05 tensor-core GEMM
+ *   "oproj_splitk"  split-K factor of the projection (0: auto)
+ *   "gemm_min_batch" smallest batch that takes the tensor-core GEMM in auto mode
+ *   "pdl"           1 (default): launch the projection with programmatic
+ *                   dependent launch so it overlaps the attention kernel's tail
+ * Returns DA_OK or DA_ERR_OPTION.
+ */
+int decode_attn_set_option(const char* key, int64_t value);
+int decode_attn_get_option(const char* key, int64_t* value);
+
+/*
+ * decode_attn_device_error -- synchronises `stream`, then reports (in
+ * *host_code) and clears the device error word of the current device's
+ * workspace: 0 when no kernel recorded an error. Returns DA_OK, or
+ * DA_ERR_CUDA when the synchronisation itself failed.
+ */
+int decode_attn_device_error(void* stream, int32_t* host_code);
+
+/* Frees the workspace of every device (synchronises those devices). */
+void decode_attn_release(void);
+
+/* A static, human-readable name for a da_status_t. */
+const char* decode_attn_status_str(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_ATTN_H */

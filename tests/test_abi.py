@@ -1,0 +1,172 @@
+"""The C-ABI library on the host (no GPU needed): it builds, loads, exports every
+symbol include/decode_attn.h declares, and rejects bad arguments on the host
+with the documented status codes before touching the device.
+
+The argument-validation cases use fake device addresses. They are skipped when
+a GPU is visible, so that a validation bug can never turn into a launch on
+made-up pointers.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import decode_attention_output_gb300 as da
+from decode_attention_output_gb300 import binding
+from decode_attention_output_gb300 import build as lib_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "decode_attn.h")
+
+OK, NULL, DTYPE, SHAPE, STRIDE, ALIGN, UNSUP = 0, -1, -2, -3, -4, -5, -6
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return binding.load()
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(decode_attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_what_binding_wraps():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_status_strings(lib):
+    for code in range(-10, 1):
+        assert binding.status_str(code) != binding.status_str(-99)
+    assert binding.status_str(-99) == "unknown status"
+
+
+def test_options_roundtrip(lib):
+    old = da.decode_attn_get_option("attn_ctas")
+    da.decode_attn_set_option("attn_ctas", 7)
+    assert da.decode_attn_get_option("attn_ctas") == 7
+    da.decode_attn_set_option("attn_ctas", old)
+    with pytest.raises(da.DecodeAttnError):
+        da.decode_attn_set_option("no_such_option", 1)
+    with pytest.raises(da.DecodeAttnError):
+        da.decode_attn_set_option("oproj_path", 5)
+
+
+# ---------------------------------------------------------------- validation
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
+
+
+def desc(shape, dtype=binding.DA_DTYPE_BF16, strides=None, addr=FAKE):
+    d = binding.da_tensor_t()
+    d.data = addr
+    d.dtype = dtype
+    d.ndim = len(shape)
+    if strides is None:
+        strides, acc = [], 1
+        for s in reversed(shape):
+            strides.insert(0, acc)
+            acc *= s
+    for i, (s, st) in enumerate(zip(shape, strides)):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+def fwd_args(B=2, Hq=8, Hkv=2, L=64, N=256, **over):
+    a = dict(q=desc([B, Hq, 128]), k=desc([B, Hkv, L, 128]), v=desc([B, Hkv, L, 128]),
+             lens=desc([B], binding.DA_DTYPE_I32), w=desc([Hq * 128, N]), out=desc([B, N]))
+    a.update(over)
+    return a
+
+
+def call_fwd(lib, a, scale=0.1):
+    r = lambda d: ctypes.byref(d) if d is not None else None  # noqa: E731
+    return lib.decode_attn_fwd(r(a["q"]), r(a["k"]), r(a["v"]), r(a["lens"]), r(a["w"]), r(a["out"]),
+                               ctypes.c_float(scale), None)
+
+
+cpu_only = pytest.mark.skipif(torch.cuda.is_available(), reason="fake-pointer cases run only without a GPU")
+
+BAD_FWD = [
+    ("q_dtype", dict(q=desc([2, 8, 128], binding.DA_DTYPE_F32)), DTYPE),
+    ("lens_dtype", dict(lens=desc([2], binding.DA_DTYPE_F32)), DTYPE),
+    ("head_dim_64", dict(q=desc([2, 8, 64])), SHAPE),
+    ("kv_head_dim_64", dict(k=desc([2, 2, 64, 64]), v=desc([2, 2, 64, 64])), SHAPE),
+    ("heads_not_multiple", dict(q=desc([2, 6, 128]), k=desc([2, 4, 64, 128]), v=desc([2, 4, 64, 128]),
+                                w=desc([6 * 128, 256])), SHAPE),
+    ("group_32", dict(q=desc([2, 64, 128]), w=desc([64 * 128, 256])), UNSUP),
+    ("batch_mismatch", dict(k=desc([3, 2, 64, 128]), v=desc([3, 2, 64, 128])), SHAPE),
+    ("v_shape", dict(v=desc([2, 2, 32, 128])), SHAPE),
+    ("w_rows", dict(w=desc([4 * 128, 256])), SHAPE),
+    ("out_cols", dict(out=desc([2, 128])), SHAPE),
+    ("n_not_multiple_of_8", dict(w=desc([8 * 128, 260], strides=[264, 1]), out=desc([2, 260])), SHAPE),
+    ("q_misaligned", dict(q=desc([2, 8, 128], addr=FAKE + 2)), ALIGN),
+    ("k_misaligned", dict(k=desc([2, 2, 64, 128], addr=FAKE + 8)), ALIGN),
+    ("q_inner_stride", dict(q=desc([2, 8, 128], strides=[2048, 256, 2])), STRIDE),
+    ("k_row_stride_odd", dict(k=desc([2, 2, 64, 128], strides=[2 * 64 * 130, 64 * 130, 130, 1])), STRIDE),
+    ("w_row_stride_odd", dict(w=desc([1024, 256], strides=[260, 1])), STRIDE),
+    ("null_q", dict(q=None), NULL),
+    ("null_lens", dict(lens=None), NULL),
+    ("lens_strided", dict(lens=desc([2], binding.DA_DTYPE_I32, strides=[2])), STRIDE),
+    ("batch_too_large", dict(q=desc([2048, 8, 128]), k=desc([2048, 2, 64, 128]), v=desc([2048, 2, 64, 128]),
+                             lens=desc([2048], binding.DA_DTYPE_I32), out=desc([2048, 256])), UNSUP),
+    ("empty_cache", dict(k=desc([2, 2, 0, 128]), v=desc([2, 2, 0, 128])), SHAPE),
+]
+
+
+@cpu_only
+@pytest.mark.parametrize("name,over,code", BAD_FWD, ids=[c[0] for c in BAD_FWD])
+def test_fwd_rejects(lib, name, over, code):
+    assert call_fwd(lib, fwd_args(**over)) == code
+
+
+@cpu_only
+def test_fwd_rejects_nonfinite_scale(lib):
+    assert call_fwd(lib, fwd_args(), scale=float("nan")) == UNSUP
+    assert call_fwd(lib, fwd_args(), scale=float("inf")) == UNSUP
+
+
+@cpu_only
+def test_empty_batch_is_a_noop(lib):
+    a = fwd_args(B=0)
+    for key in ("q", "k", "v", "lens", "out"):  # zero-element tensors carry no storage
+        a[key].data = None
+    assert call_fwd(lib, a) == OK
+
+
+@cpu_only
+def test_only_and_scores_and_oproj_reject(lib):
+    r = ctypes.byref
+    a = fwd_args()
+    bad_attn = desc([2, 8, 64])
+    assert lib.decode_attn_only(r(a["q"]), r(a["k"]), r(a["v"]), r(a["lens"]), r(bad_attn), ctypes.c_float(1.0),
+                                None) == SHAPE
+    bad_scores = desc([2, 8, 63], binding.DA_DTYPE_F32)
+    assert lib.decode_attn_scores(r(a["q"]), r(a["k"]), r(a["lens"]), r(bad_scores), None) == SHAPE
+    scores_bf16 = desc([2, 8, 64])
+    assert lib.decode_attn_scores(r(a["q"]), r(a["k"]), r(a["lens"]), r(scores_bf16), None) == DTYPE
+    x, w, out = desc([2, 1024]), desc([1000, 256]), desc([2, 256])
+    assert lib.decode_attn_oproj(r(x), r(w), r(out), None) == SHAPE
+    x, w, out = desc([2, 1020]), desc([1020, 256]), desc([2, 256])
+    assert lib.decode_attn_oproj(r(x), r(w), r(out), None) == STRIDE  # row stride 1020 is not a multiple of 8
+
+
+@cpu_only
+def test_binding_raises_with_code(lib):
+    q = torch.zeros((2, 8, 128), dtype=torch.float32)  # wrong dtype: rejected before any device access
+    k = torch.zeros((2, 2, 64, 128), dtype=torch.bfloat16)
+    lens = torch.zeros((2,), dtype=torch.int32)
+    attn = torch.zeros((2, 8, 128), dtype=torch.bfloat16)
+    with pytest.raises(da.DecodeAttnError) as ei:
+        da.decode_attn_only(q, k, k, lens, attn, 0.1, stream=0)
+    assert ei.value.code == DTYPE

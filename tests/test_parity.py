@@ -1,0 +1,248 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, element by
+element, on seeded inputs that span several 64-token tiles, ragged tails, every
+GQA group width the kernels specialise on, and the degenerate cases: empty
+sequences, one token, lengths past the cache (clamped), a single persistent CTA
+doing all the work and more CTAs than tiles.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import decode_attention_output_gb300 as da
+from decode_attention_output_gb300 import synth
+from gpu_helpers import RTOL_SCORES, assert_bf16_close, f64, oracle_decode
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    from decode_attention_output_gb300 import build
+
+    build.build()
+    da.load()
+    torch.cuda.set_device(0)
+    yield
+    assert da.decode_attn_device_error() == 0
+
+
+def W(name, B, Hq, Hkv, Lcap, N, lens, k_mult=1.0):
+    return synth.Workload(name, B=B, Hq=Hq, Hkv=Hkv, Lcap=Lcap, N=N, fixed_lens=tuple(lens), k_mult=k_mult)
+
+
+CASES = [
+    W("g4_ragged", 3, 8, 2, 300, 256, (300, 1, 129)),
+    W("g4_tiles", 2, 32, 8, 640, 1024, (640, 511)),
+    W("g8", 2, 16, 2, 200, 512, (200, 77)),
+    W("g16", 2, 32, 2, 150, 256, (150, 64)),
+    W("g1_mha", 2, 4, 4, 100, 128, (100, 16)),
+    W("g3", 2, 6, 2, 257, 264, (257, 130)),
+    W("g5_sharp", 2, 10, 2, 190, 640, (190, 33), k_mult=2.0),
+    W("zero_len", 3, 8, 2, 130, 256, (0, 130, 65)),
+    W("all_zero_len", 2, 8, 2, 70, 256, (0, 0)),
+    W("tiny", 1, 2, 1, 1, 8, (1,)),
+    W("one_tile", 1, 8, 2, 64, 256, (64,)),
+    W("tile_plus_one", 1, 8, 2, 65, 256, (65,)),
+    W("many_batches", 40, 8, 1, 70, 128, tuple(int(x) for x in np.random.default_rng(3).integers(0, 71, 40))),
+    W("b9_gemv_chunks", 9, 8, 2, 96, 256, (96, 1, 2, 3, 64, 65, 95, 33, 17)),
+]
+
+
+def _run(w, seed=0, ctas=0):
+    x = synth.make_inputs(w, seed=seed, device=DEV)
+    old = da.decode_attn_get_option("attn_ctas")
+    da.decode_attn_set_option("attn_ctas", ctas)
+    try:
+        attn = torch.full((w.B, w.Hq, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+        da.decode_attn_only(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], attn, x["scale"])
+        out = torch.full((w.B, w.N), float("nan"), dtype=torch.bfloat16, device=DEV)
+        da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out, x["scale"])
+        torch.cuda.synchronize()
+    finally:
+        da.decode_attn_set_option("attn_ctas", old)
+    assert da.decode_attn_device_error() == 0
+    return x, attn, out
+
+
+@pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
+def test_decode_matches_oracle(orc, w):
+    x, attn, out = _run(w)
+    ref_attn, ref_out = oracle_decode(orc, x)
+    assert_bf16_close(f64(attn), ref_attn, f"{w.name} attention")
+    assert_bf16_close(f64(out), ref_out, f"{w.name} output")
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 7, 300])
+def test_cta_count_does_not_change_the_result(orc, ctas):
+    """Split-KV over any number of persistent CTAs (1 = no split at all, 300 = more
+    CTAs than many sequences have tiles) equals the oracle and the default plan."""
+    w = W("splits", 3, 16, 2, 700, 256, (700, 333, 64))
+    x, attn, out = _run(w, seed=5, ctas=ctas)
+    _, attn0, out0 = _run(w, seed=5, ctas=0)
+    ref_attn, ref_out = oracle_decode(orc, x)
+    assert_bf16_close(f64(attn), ref_attn, f"ctas={ctas} attention")
+    assert_bf16_close(f64(out), ref_out, f"ctas={ctas} output")
+    # fp32 merges in another order: at most one bf16 step apart
+    a, b = f64(attn), f64(attn0)
+    assert np.all(np.abs(a - b) <= 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b)) + 1e-6)
+
+
+def test_lengths_are_clamped_to_the_cache(orc):
+    w = W("clamp", 3, 8, 2, 100, 256, (150, -5, 100))
+    x, attn, out = _run(w)
+    ref_attn, ref_out = oracle_decode(orc, x)  # the helper clamps to [0, Lcap] for the oracle
+    assert_bf16_close(f64(attn), ref_attn, "clamped attention")
+    assert np.all(f64(attn)[1] == 0.0)
+    assert_bf16_close(f64(out), ref_out, "clamped output")
+
+
+def test_garbage_past_seq_len_is_ignored():
+    """Inf and NaN in cache rows t >= seq_len must not reach the output."""
+    w = W("garbage", 2, 8, 2, 200, 256, (70, 129))
+    x = synth.make_inputs(w, seed=1, device=DEV)
+    a0 = torch.empty((2, 8, 128), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_only(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], a0, x["scale"])
+    x["k_cache"][0, :, 70:] = float("inf")
+    x["v_cache"][0, :, 70:] = float("nan")
+    x["k_cache"][1, :, 129:] = float("nan")
+    x["v_cache"][1, :, 129:] = float("inf")
+    a1 = torch.empty_like(a0)
+    da.decode_attn_only(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], a1, x["scale"])
+    torch.cuda.synchronize()
+    assert torch.equal(a0, a1)
+
+
+def test_softmax_rows_sum_to_one():
+    """V = 1: every attention output is exactly 1.0 after the bf16 store."""
+    w = W("ones", 2, 16, 2, 333, 256, (333, 70))
+    x = synth.make_inputs(w, seed=2, device=DEV)
+    x["v_cache"].fill_(1.0)
+    attn = torch.empty((2, 16, 128), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_only(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], attn, x["scale"])
+    assert torch.all(attn.float() == 1.0)
+
+
+def test_identical_keys_give_the_mean_of_v():
+    w = W("same_keys", 1, 8, 2, 250, 256, (250,))
+    x = synth.make_inputs(w, seed=3, device=DEV)
+    x["k_cache"][:] = x["k_cache"][:, :, :1]
+    attn = torch.empty((1, 8, 128), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_only(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], attn, x["scale"])
+    mean = x["v_cache"].double().mean(dim=2)  # [1, Hkv, 128]
+    ref = mean.repeat_interleave(4, dim=1)
+    assert torch.max(torch.abs(attn.double() - ref)).item() <= 2.0 ** -8 * ref.abs().max().item() + 1e-3
+
+
+def test_dominant_key_copies_its_value_row():
+    w = W("dominant", 1, 8, 2, 300, 256, (300,))
+    x = synth.make_inputs(w, seed=4, device=DEV)
+    q = torch.zeros_like(x["q"])
+    q[..., 0] = 8.0
+    x["q"] = q
+    x["k_cache"].clamp_(-2, 2)
+    tstar = 211
+    x["k_cache"][:, :, tstar, 0] = 64.0  # scaled score 45.25 vs <= 1.42 for the others
+    attn = torch.empty((1, 8, 128), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_only(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], attn, x["scale"])
+    ref = x["v_cache"][:, :, tstar].repeat_interleave(4, dim=1)  # [1, 8, 128]
+    assert torch.equal(attn, ref)
+
+
+# ------------------------------------------------------------- fp32 scores
+@pytest.mark.parametrize("G,Hkv", [(4, 2), (8, 1), (16, 1), (3, 2)])
+def test_scores_match_oracle(orc, G, Hkv):
+    B, Lcap = 2, 203
+    w = W("scores", B, G * Hkv, Hkv, Lcap, 8, (203, 90))
+    x = synth.make_inputs(w, seed=9, device=DEV)
+    s = torch.full((B, w.Hq, Lcap), float("nan"), dtype=torch.float32, device=DEV)
+    da.decode_attn_scores(x["q"], x["k_cache"], x["seq_lens"], s)
+    ref = orc.scores(synth.to_bits(x["q"]), synth.to_bits(x["k_cache"]), x["seq_lens"].cpu().numpy())
+    got = s.cpu().numpy().astype(np.float64)
+    for b in range(B):
+        L = int(x["seq_lens"][b])
+        assert np.all(np.isnan(got[b, :, L:])), "scores past seq_len must be left untouched"
+        num = np.linalg.norm(got[b, :, :L] - ref[b, :, :L], axis=1)
+        den = np.linalg.norm(ref[b, :, :L], axis=1)
+        assert np.all(num <= RTOL_SCORES * den), f"b={b}: worst rel {np.max(num / den):.2e}"
+
+
+def test_integer_scores_are_exact(orc):
+    """Integer-valued q and K: every fp32 partial sum is exact, so the scores equal
+    the oracle bit for bit (the msKPP page's all-integer golden pattern)."""
+    B, Hq, Hkv, Lcap = 2, 8, 2, 150
+    g = torch.Generator(device="cpu").manual_seed(21)
+    q = torch.randint(-4, 5, (B, Hq, 128), generator=g).to(torch.bfloat16).to(DEV)
+    k = torch.randint(-4, 5, (B, Hkv, Lcap, 128), generator=g).to(torch.bfloat16).to(DEV)
+    lens = torch.tensor([150, 77], dtype=torch.int32, device=DEV)
+    s = torch.full((B, Hq, Lcap), float("nan"), dtype=torch.float32, device=DEV)
+    da.decode_attn_scores(q, k, lens, s)
+    ref = orc.scores(synth.to_bits(q), synth.to_bits(k), lens.cpu().numpy())
+    got = s.cpu().numpy().astype(np.float64)
+    mask = ~np.isnan(ref)
+    assert np.array_equal(got[mask], ref[mask])
+
+
+# ------------------------------------------------------------ output projection
+@pytest.mark.parametrize("B", [1, 2, 3, 4, 5, 8, 9, 16])
+def test_oproj_integer_exact(B):
+    """Integer attention rows and W in {-1, 0, 1}: fp32 sums are exact, so the result
+    is the round-to-nearest-even bf16 of the exact integer matmul."""
+    K, N = 1032, 264  # ragged k-slices and a partial 256-column block
+    g = torch.Generator(device="cpu").manual_seed(100 + B)
+    xi = torch.randint(-8, 9, (B, K), generator=g)
+    wi = torch.randint(-1, 2, (K, N), generator=g)
+    ref = (xi.long() @ wi.long()).double().to(torch.bfloat16)
+    out = torch.full((B, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_oproj(xi.to(torch.bfloat16).to(DEV), wi.to(torch.bfloat16).to(DEV), out)
+    assert torch.equal(out.cpu(), ref)
+
+
+@pytest.mark.parametrize("B,K,N", [(1, 4096, 4096), (4, 512, 1024), (8, 1024, 768), (32, 256, 512)])
+def test_oproj_matches_oracle(orc, B, K, N):
+    g = torch.Generator(device="cpu").manual_seed(7)
+    x = torch.randn((B, K), generator=g).to(torch.bfloat16)
+    w = (torch.randn((K, N), generator=g) / math.sqrt(K)).to(torch.bfloat16)
+    out = torch.empty((B, N), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_oproj(x.to(DEV), w.to(DEV), out)
+    ref = orc.oproj(synth.to_bits(x), synth.to_bits(w))
+    assert_bf16_close(f64(out), ref, "o_proj")
+
+
+def test_strided_views():
+    """Non-contiguous but legal views (padded rows, a sliced cache) give the same bits."""
+    w = W("strided", 2, 8, 2, 130, 256, (130, 50))
+    x = synth.make_inputs(w, seed=11, device=DEV)
+    ref = torch.empty((2, w.N), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], ref, x["scale"])
+    big_k = torch.zeros((2, 3, 160, 136), dtype=torch.bfloat16, device=DEV)
+    big_v = torch.zeros((2, 3, 160, 136), dtype=torch.bfloat16, device=DEV)
+    big_k[:, 1:3, 5:135, :128] = x["k_cache"]
+    big_v[:, 1:3, 5:135, :128] = x["v_cache"]
+    k_view = big_k[:, 1:3, 5:135, :128]
+    v_view = big_v[:, 1:3, 5:135, :128]
+    q_big = torch.zeros((2, 8, 136), dtype=torch.bfloat16, device=DEV)
+    q_big[..., :128] = x["q"]
+    w_big = torch.zeros((w.Hq * 128, 272), dtype=torch.bfloat16, device=DEV)
+    w_big[:, :256] = x["o_weight"]
+    out_big = torch.zeros((2, 300), dtype=torch.bfloat16, device=DEV)
+    out_view = out_big[:, 8:264]
+    da.decode_attn_fwd(q_big[..., :128], k_view, v_view, x["seq_lens"], w_big[:, :256], out_view, x["scale"])
+    torch.cuda.synchronize()
+    assert torch.equal(out_view, ref)
+    assert torch.all(out_big[:, :8] == 0) and torch.all(out_big[:, 264:] == 0)
+
+
+def test_repeated_calls_are_deterministic():
+    w = W("repeat", 4, 32, 8, 1000, 512, (1000, 999, 500, 3))
+    x = synth.make_inputs(w, seed=12, device=DEV)
+    outs = []
+    for _ in range(3):
+        o = torch.empty((4, 512), dtype=torch.bfloat16, device=DEV)
+        da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], o, x["scale"])
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])

@@ -1,0 +1,55 @@
+"""The five synthetic decode workloads at full size, run exactly as bench.py runs
+them (default plan, one decode_attn_fwd call), checked on sampled batch rows the
+oracle recomputes one by one: every attention head and every output column of
+each sampled row, with the same tolerances as the small cases. Properties that
+hold at any size are checked on the whole output (finite, attention-only and
+fused paths agree).
+"""
+import numpy as np
+import pytest
+import torch
+
+import decode_attention_output_gb300 as da
+from decode_attention_output_gb300 import synth
+from gpu_helpers import assert_bf16_close, f64, oracle_decode
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    from decode_attention_output_gb300 import build
+
+    build.build()
+    da.load()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", synth.ORDER)
+def test_workload_sampled_rows(orc, name):
+    w = synth.WORKLOADS[name]
+    x = synth.make_inputs(w, seed=0, device=DEV)
+    out = torch.full((w.B, w.N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out, x["scale"])
+    attn = torch.full((w.B, w.Hq, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    da.decode_attn_only(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], attn, x["scale"])
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_error() == 0
+    assert torch.isfinite(out.float()).all() and torch.isfinite(attn.float()).all()
+    # the fused step projects the same attention the attention-only entry returns
+    out2 = torch.empty_like(out)
+    da.decode_attn_oproj(attn.view(w.B, w.Hq * 128), x["o_weight"], out2)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+
+    lens = x["seq_lens"].cpu().numpy()
+    rows = sorted({0, w.B - 1, int(np.argmax(lens)), int(np.argmin(lens))})
+    ref_attn, ref_out = oracle_decode(orc, x, rows=rows)
+    assert_bf16_close(f64(attn[rows]), ref_attn, f"{name} attention rows {rows}")
+    assert_bf16_close(f64(out[rows]), ref_out, f"{name} output rows {rows}")
+    del x, out, attn, out2
+    torch.cuda.empty_cache()
