@@ -122,9 +122,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   pdl_launch_dependents();
 
   const long long T = prefix[B];
-  const int P = gridDim.x, cta = blockIdx.x;
-  const long long start = T > 0 ? (long long)cta * T / P : 0;
-  const long long end = T > 0 ? (long long)(cta + 1) * T / P : 0;
+  const int cta = blockIdx.x;
+  // P workers share the T tiles; with P <= T every range is non-empty, so the CTAs
+  // cta_of(first tile) .. cta_of(last tile) of a sequence all hold a part of it.
+  const int P = T > 0 ? (int)min((long long)gridDim.x, T) : 1;
+  const long long start = (T > 0 && cta < P) ? (long long)cta * T / P : 0;
+  const long long end = (T > 0 && cta < P) ? (long long)(cta + 1) * T / P : 0;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -164,7 +167,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   } else {
     // ------------------------------------------------------------ consumers
     if (!SCORES) {  // empty sequences produce zero rows
-      for (int s = cta; s < B * Hkv; s += P) {
+      for (int s = cta; s < B * Hkv; s += gridDim.x) {
         const int b = s / Hkv;
         if (prefix[b + 1] != prefix[b]) continue;
         const int kvh = s - b * Hkv;

@@ -86,9 +86,14 @@ def test_cta_count_does_not_change_the_result(orc, ctas):
     ref_attn, ref_out = oracle_decode(orc, x)
     assert_bf16_close(f64(attn), ref_attn, f"ctas={ctas} attention")
     assert_bf16_close(f64(out), ref_out, f"ctas={ctas} output")
-    # fp32 merges in another order: at most one bf16 step apart
+    # Each split rounds its weights P to bf16 against its own running maximum
+    # (relative error <= 2^-9 per weight), and the outputs are rounded to bf16
+    # (<= 2^-9 relative). So |split - unsplit| <= 2 * 2^-9 * (sum_t p_t |v_t| + |o|),
+    # bounded here by 2^-8 * (max|v| + |o|) elementwise.
     a, b = f64(attn), f64(attn0)
-    assert np.all(np.abs(a - b) <= 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b)) + 1e-6)
+    vmax = float(x["v_cache"].abs().max())
+    assert np.all(np.abs(a - b) <= 2.0 ** -8 * (vmax + np.maximum(np.abs(a), np.abs(b))))
+    assert np.sqrt(np.sum((a - b) ** 2) / np.sum(b * b)) <= 2e-3
 
 
 def test_lengths_are_clamped_to_the_cache(orc):
