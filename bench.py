@@ -302,10 +302,10 @@ def run_ours(args, world, rank, local):
     outs = [torch.empty((w.B, w.N), dtype=torch.bfloat16, device=dev) for _ in range(n_sets)]
     stream = torch.cuda.current_stream(dev)
 
-    def step(i):
+    def step(i, st=None):
         s = sets[i % n_sets]
         da.decode_attn_fwd(s["q"], s["k_cache"], s["v_cache"], s["seq_lens"], s["o_weight"], outs[i % n_sets],
-                           s["scale"], stream=stream)
+                           s["scale"], stream=st if st is not None else stream)
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -347,6 +347,38 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     sampler.stop()
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    assert da.decode_attn_device_error(stream) == 0
+
+    # ---- host cost of one eager call (enqueue only) and CUDA-graph replay of the same steps
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    n_host = min(args.steps, 50)
+    for i in range(n_host):
+        step(i)
+    host_us = (time.perf_counter() - t0) / n_host * 1e6
+    torch.cuda.synchronize(dev)
+    graph_us = None
+    try:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(n_sets):
+                step(i, cap)
+        torch.cuda.synchronize(dev)
+        reps = max(1, args.steps // n_sets)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        g0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        graph_us = g0.elapsed_time(g1) * 1e3 / (reps * n_sets)
+        del graph
+    except RuntimeError as e:  # capture unsupported on this setup: report why
+        graph_us = f"unavailable: {e}"[:200]
     assert da.decode_attn_device_error(stream) == 0
 
     step_ms_max = max_over_ranks(world, step_ms)
@@ -400,7 +432,8 @@ def run_ours(args, world, rank, local):
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "kv_len": w.Lcap, "hidden": w.N,
                        "seq_lens_sum": int(lens.sum().item()), "bytes_per_step": nb,
                        "l2": f"{n_sets} rotated input sets of {set_bytes / 1e6:.0f} MB (>2x L2 between reuses)",
-                       "step_hbm_frac": value / world / peak, "parallelism": f"replicas x{world}"},
+                       "step_hbm_frac": value / world / peak, "parallelism": f"replicas x{world}",
+                       "graph_us_per_step": graph_us, "host_us_per_call": host_us},
             "roofline": {"bound": "hbm", "kernel": "attn_decode_kernel", "achieved": achieved, "peak": peak,
                          "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic, "algorithmic_bytes_per_launch": attn_bytes,

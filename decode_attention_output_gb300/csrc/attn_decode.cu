@@ -17,14 +17,16 @@
 //    rule and writes bf16.
 //  * One producer warp streams K and V tiles with 4-D TMA (128-byte swizzle,
 //    two 64-dim boxes per tile) into a 4-stage shared-memory ring guarded by
-//    mbarriers; q rows arrive by 1-D bulk copy with the first tile of a sequence.
-//  * Each of 4 consumer warps owns 16 tokens of a stage and all G query heads of
-//    the group (every K/V byte is read once). S^T = K . Q^T runs on mma.sync
-//    m16n8k16 with tokens as M and heads as N (G <= 8 fills one 8-wide N block),
-//    the online softmax runs in registers (running max / sum, shuffle
-//    reductions, exp2 with scale*log2e folded), P is rounded to bf16 and moved
-//    into the B-operand layout with movmatrix, and O^T = V^T . P^T accumulates in
-//    fp32 registers.
+//    mbarriers; q rows arrive by 1-D bulk copy with a sequence's first tiles.
+//  * Two consumer groups of four warps take alternate stages, so two tiles are
+//    in compute at once per SM. Each warp owns 16 tokens of a stage and all G
+//    query heads of the group (every K/V byte is read once). S^T = K . Q^T runs
+//    on mma.sync m16n8k16 with tokens as M and heads as N (G <= 8 fills one
+//    8-wide N block); the online softmax runs in registers (running max / sum,
+//    shuffle reductions, exp2 with scale*log2e folded); P is rounded to bf16 and
+//    moved into the B-operand layout with movmatrix; O^T = V^T . P^T accumulates
+//    in fp32 registers. At the end of a sequence segment the eight warps' states
+//    are merged (pairwise in registers, then across four warps in shared memory).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -33,25 +35,38 @@ namespace {
 
 constexpr float kNegInf = -__builtin_huge_valf();
 
-struct TileInfo {
+// Position of the current tile in the flattened tile order.
+struct Cursor {
   int b, kvh, j, nt;  // batch row, KV head, tile index in the sequence, tiles in the sequence
 };
 
 // prefix[b] = KV heads x tiles of all batch rows before b; prefix[B] = total tiles.
-__device__ __forceinline__ TileInfo decode_tile(long long x, const int* prefix, int B, int Hkv) {
+__device__ __forceinline__ Cursor cursor_at(long long x, const int* prefix, int B, int Hkv) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (prefix[mid] <= x) lo = mid;
     else hi = mid - 1;
   }
-  TileInfo ti;
-  ti.b = lo;
-  ti.nt = (prefix[lo + 1] - prefix[lo]) / Hkv;
+  Cursor c;
+  c.b = lo;
+  c.nt = (prefix[lo + 1] - prefix[lo]) / Hkv;
   const int r = (int)(x - prefix[lo]);
-  ti.kvh = r / ti.nt;
-  ti.j = r - ti.kvh * ti.nt;
-  return ti;
+  c.kvh = r / c.nt;
+  c.j = r - c.kvh * c.nt;
+  return c;
+}
+
+// Advances to the next tile (only called while one exists).
+__device__ __forceinline__ void cursor_next(Cursor& c, const int* prefix, int B, int Hkv) {
+  if (++c.j < c.nt) return;
+  c.j = 0;
+  if (++c.kvh < Hkv) return;
+  c.kvh = 0;
+  do {
+    ++c.b;
+  } while (c.b < B - 1 && prefix[c.b + 1] == prefix[c.b]);
+  c.nt = (prefix[c.b + 1] - prefix[c.b]) / Hkv;
 }
 
 // CTA whose range [i*T/P, (i+1)*T/P) holds tile x.
@@ -71,41 +86,49 @@ __device__ __forceinline__ uint32_t mask_tokens(uint32_t v, int tok, int valid) 
 
 template <int NB, bool SCORES>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int HP = 8 * NB;  // heads per group, padded to the MMA width
+  const int B = p.B, Hkv = p.Hkv, G = p.G, Lcap = p.Lcap;
+  constexpr AttnSmem kFixed(NB, 0);  // offsets that do not depend on the batch size
+  const AttnSmem lay(NB, B);
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
 
-  uint8_t* q_slots = smem + kStages * kStageBytes;
-  float* merge_o = reinterpret_cast<float*>(q_slots + kStages * kQSlotBytes);
-  float* merge_ml = merge_o + kConsumerWarps * kMaxGroup * kMergeRow;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(merge_ml + kConsumerWarps * kMaxGroup * 2);
-  int* flags = reinterpret_cast<int*>(bars + 2 * kStages);  // [0] abort, [1] last-CTA
-  int* prefix = flags + 4;
+  uint8_t* q_slots = smem + kFixed.off_q();
+  float* merge_o = reinterpret_cast<float*>(smem + kFixed.off_merge_o());    // [4][HP][kMergeRow]
+  float* merge_ml = reinterpret_cast<float*>(smem + kFixed.off_merge_ml());  // [4][HP][2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFixed.off_bars());
+  int* flags = reinterpret_cast<int*>(smem + kFixed.off_flags());            // [0] abort, [1] last CTA
+  int* prefix = reinterpret_cast<int*>(smem + lay.off_prefix());             // [B + 1]
+  int* lens = reinterpret_cast<int*>(smem + lay.off_lens());                 // [B], clamped
   const uint32_t ring = smem_u32(smem);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + kStages + s); };
 
-  const int B = p.B, Hkv = p.Hkv, G = p.G, Lcap = p.Lcap;
-
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kConsumerWarps);
+      mbar_init(empty_bar(s), kGroupWarps);
     }
     flags[0] = 0;
     flags[1] = 0;
     fence_barrier_init();
   }
   // Padded head rows of the q slots stay zero for the whole kernel.
-  for (int i = tid; i < kStages * kQSlotBytes / 16; i += kAttnThreads)
+  for (int i = tid; i < (int)(kStages * kFixed.q_slot() / 16); i += kAttnThreads)
     reinterpret_cast<uint4*>(q_slots)[i] = make_uint4(0, 0, 0, 0);
-  if (warp == 1) {  // tiles per batch row, scanned
+  if (warp == 1) {  // clamped lengths, and tiles per batch row scanned into prefix
     int carry = 0;
     for (int base = 0; base < B; base += 32) {
       const int b = base + lane;
       int v = 0;
-      if (b < B) v = ((clamp_len(__ldg(p.seq_lens + b), Lcap) + kTile - 1) / kTile) * Hkv;
+      if (b < B) {
+        const int L = clamp_len(__ldg(p.seq_lens + b), Lcap);
+        lens[b] = L;
+        v = ((L + kTile - 1) / kTile) * Hkv;
+      }
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int n = __shfl_up_sync(0xffffffffu, v, off);
@@ -129,33 +152,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   const long long start = (T > 0 && cta < P) ? (long long)cta * T / P : 0;
   const long long end = (T > 0 && cta < P) ? (long long)(cta + 1) * T / P : 0;
 
-  if (warp == kConsumerWarps) {
+  if (warp == kGroups * kGroupWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && start < end) {
       prefetch_tensormap(&p.tm_k);
       if (!SCORES) prefetch_tensormap(&p.tm_v);
+      Cursor c = cursor_at(start, prefix, B, Hkv);
+      long long seg0 = start;
       int it = 0;
       for (long long x = start; x < end; ++x, ++it) {
-        const TileInfo ti = decode_tile(x, prefix, B, Hkv);
-        const bool first = (x == start) || (ti.j == 0);
+        if (x != start) {
+          cursor_next(c, prefix, B, Hkv);
+          if (c.j == 0) seg0 = x;
+        }
+        const bool with_q = x - seg0 < kGroups;  // each group's first tile of the segment
         const int stage = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
         mbar_wait_bounded(empty_bar(stage), ph ^ 1, p.err, kErrWaitEmpty, flags);
         const uint32_t fb = full_bar(stage);
         uint32_t bytes = SCORES ? kKTileBytes : kStageBytes;
-        if (first) bytes += G * 256;
+        if (with_q) bytes += G * 256;
         mbar_arrive_expect_tx(fb, bytes);
         const uint32_t kdst = ring + stage * kStageBytes;
-        const int t0 = ti.j * kTile;
-        tma_load_4d(kdst, &p.tm_k, fb, 0, t0, ti.kvh, ti.b);
-        tma_load_4d(kdst + kHalfBytes, &p.tm_k, fb, 64, t0, ti.kvh, ti.b);
+        const int t0 = c.j * kTile;
+        tma_load_4d(kdst, &p.tm_k, fb, 0, t0, c.kvh, c.b);
+        tma_load_4d(kdst + kHalfBytes, &p.tm_k, fb, 64, t0, c.kvh, c.b);
         if (!SCORES) {
-          tma_load_4d(kdst + kKTileBytes, &p.tm_v, fb, 0, t0, ti.kvh, ti.b);
-          tma_load_4d(kdst + kKTileBytes + kHalfBytes, &p.tm_v, fb, 64, t0, ti.kvh, ti.b);
+          tma_load_4d(kdst + kKTileBytes, &p.tm_v, fb, 0, t0, c.kvh, c.b);
+          tma_load_4d(kdst + kKTileBytes + kHalfBytes, &p.tm_v, fb, 64, t0, c.kvh, c.b);
         }
-        if (first) {
-          const uint32_t qdst = smem_u32(q_slots + stage * kQSlotBytes);
-          const __nv_bfloat16* qsrc = p.q + (long long)ti.b * p.q_sb + (long long)(ti.kvh * G) * p.q_sh;
+        if (with_q) {
+          const uint32_t qdst = smem_u32(q_slots + stage * kFixed.q_slot());
+          const __nv_bfloat16* qsrc = p.q + (long long)c.b * p.q_sb + (long long)(c.kvh * G) * p.q_sh;
           for (int h = 0; h < G; ++h) bulk_load(qdst + h * kQRowBytes, qsrc + (long long)h * p.q_sh, 256, fb);
         }
       }
@@ -166,192 +194,244 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
     }
   } else {
     // ------------------------------------------------------------ consumers
+    const int grp = warp / kGroupWarps;  // consumer group: takes iterations it % kGroups == grp
+    const int wg = warp % kGroupWarps;   // warp in group: tokens 16*wg .. 16*wg+15 of a stage
     if (!SCORES) {  // empty sequences produce zero rows
       for (int s = cta; s < B * Hkv; s += gridDim.x) {
         const int b = s / Hkv;
-        if (prefix[b + 1] != prefix[b]) continue;
+        if (lens[b] != 0) continue;
         const int kvh = s - b * Hkv;
-        for (int h = 0; h < G; ++h)
-          p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + tid] = __float2bfloat16_rn(0.f);
+        for (int h = tid >> 7; h < G; h += 2)
+          p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + (tid & 127)] = __float2bfloat16_rn(0.f);
       }
     }
     uint32_t qf[NB][8][2];
     float o[8][NB][4];
     float m_run[NB][2], l_run[NB][2];
-    const int tb = warp * 16;  // this warp's first token inside a stage
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      m_run[nb][0] = m_run[nb][1] = kNegInf;
+      l_run[nb][0] = l_run[nb][1] = 0.f;
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb) o[mb][nb][0] = o[mb][nb][1] = o[mb][nb][2] = o[mb][nb][3] = 0.f;
+    }
+    const int tb = wg * 16;  // this warp's first token inside a stage
     const float sl2 = p.scale_log2;
+    Cursor c;
+    if (start < end) c = cursor_at(start, prefix, B, Hkv);
+    long long seg0 = start;
     int it = 0;
     for (long long x = start; x < end; ++x, ++it) {
-      const TileInfo ti = decode_tile(x, prefix, B, Hkv);
-      const bool first = (x == start) || (ti.j == 0);
-      const bool last = (x == end - 1) || (ti.j == ti.nt - 1);
-      const int L = clamp_len(__ldg(p.seq_lens + ti.b), Lcap);
-      const int t0 = ti.j * kTile;
-      const int vw = min(kTile, L - t0) - tb;  // valid tokens of this warp's 16
-      const int stage = it % kStages;
-      const uint32_t ph = (it / kStages) & 1;
-      mbar_wait_bounded(full_bar(stage), ph, p.err, kErrWaitFull, flags);
-      if (first) {
-        const uint8_t* qs = q_slots + stage * kQSlotBytes;
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint8_t* row = qs + (nb * 8 + g) * kQRowBytes + (ks * 16 + 2 * t) * 2;
-            qf[nb][ks][0] = *reinterpret_cast<const uint32_t*>(row);
-            qf[nb][ks][1] = *reinterpret_cast<const uint32_t*>(row + 16);
-          }
-        }
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          m_run[nb][0] = m_run[nb][1] = kNegInf;
-          l_run[nb][0] = l_run[nb][1] = 0.f;
-#pragma unroll
-          for (int mb = 0; mb < 8; ++mb) o[mb][nb][0] = o[mb][nb][1] = o[mb][nb][2] = o[mb][nb][3] = 0.f;
-        }
+      if (x != start) {
+        cursor_next(c, prefix, B, Hkv);
+        if (c.j == 0) seg0 = x;
       }
-      if (vw > 0) {
-        const uint32_t kbase = ring + stage * kStageBytes;
-        // ---- S^T[16 tokens][8*NB heads] = K_tile . Q^T  (fp32, unscaled)
-        float se[NB][4], so[NB][4];
+      const bool last = (x == end - 1) || (c.j == c.nt - 1);
+      if (it % kGroups == grp) {
+        const int t0 = c.j * kTile;
+        const int vw = min(kTile, lens[c.b] - t0) - tb;  // valid tokens of this warp's 16
+        const int stage = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        mbar_wait_bounded(full_bar(stage), ph, p.err, kErrWaitFull, flags);
+        if (x - seg0 < kGroups) {  // this group's first tile of the segment carries q
+          const uint8_t* qs = q_slots + stage * kFixed.q_slot();
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
+          for (int nb = 0; nb < NB; ++nb) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) se[nb][i] = so[nb][i] = 0.f;
-        {
-          const int row = tb + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const int chunk = 2 * (ks & 3) + (lane >> 4);
-            const uint32_t addr = kbase + (ks >> 2) * kHalfBytes + row * 128 + ((chunk ^ (lane & 7)) << 4);
-            uint32_t a[4];
-            ldsm_x4(addr, a[0], a[1], a[2], a[3]);
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-              if (ks & 1) mma_bf16_16816(so[nb], a, qf[nb][ks][0], qf[nb][ks][1]);
-              else mma_bf16_16816(se[nb], a, qf[nb][ks][0], qf[nb][ks][1]);
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint8_t* row = qs + (nb * 8 + g) * kQRowBytes + (ks * 16 + 2 * t) * 2;
+              qf[nb][ks][0] = *reinterpret_cast<const uint32_t*>(row);
+              qf[nb][ks][1] = *reinterpret_cast<const uint32_t*>(row + 16);
             }
           }
         }
-        float s[NB][4];
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) s[nb][i] = se[nb][i] + so[nb][i];
-        // fragment element i: token g + 8*(i>>1), head 8*nb + 2t + (i&1)
-        if (SCORES) {
+        if (vw > 0) {
+          const uint32_t kbase = ring + stage * kStageBytes;
+          // ---- S^T[16 tokens][8*NB heads] = K_tile . Q^T  (fp32, unscaled)
+          float se[NB][4], so[NB][4];
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int head = nb * 8 + 2 * t + (i & 1);
-              const int tok = g + 8 * (i >> 1);
-              if (head < G && tok < vw)
-                p.scores[(long long)ti.b * p.s_sb + (long long)(ti.kvh * G + head) * p.s_sh + t0 + tb + tok] =
-                    s[nb][i];
-            }
-        } else {
-          const bool v0 = g < vw, v1 = g + 8 < vw;
-          uint32_t pb[NB][2];
+            for (int i = 0; i < 4; ++i) se[nb][i] = so[nb][i] = 0.f;
+          {
+            const int row = tb + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-            const float x0 = v0 ? s[nb][0] * sl2 : kNegInf;
-            const float x1 = v0 ? s[nb][1] * sl2 : kNegInf;
-            const float x2 = v1 ? s[nb][2] * sl2 : kNegInf;
-            const float x3 = v1 ? s[nb][3] * sl2 : kNegInf;
-            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+            for (int ks = 0; ks < 8; ++ks) {
+              const int chunk = 2 * (ks & 3) + (lane >> 4);
+              const uint32_t addr = kbase + (ks >> 2) * kHalfBytes + row * 128 + ((chunk ^ (lane & 7)) << 4);
+              uint32_t a[4];
+              ldsm_x4(addr, a[0], a[1], a[2], a[3]);
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-              mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-              mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+              for (int nb = 0; nb < NB; ++nb) {
+                if (ks & 1) mma_bf16_16816(so[nb], a, qf[nb][ks][0], qf[nb][ks][1]);
+                else mma_bf16_16816(se[nb], a, qf[nb][ks][0], qf[nb][ks][1]);
+              }
             }
-            const float mn0 = fmaxf(m_run[nb][0], mx0), mn1 = fmaxf(m_run[nb][1], mx1);
-            const float al0 = fast_exp2(m_run[nb][0] - mn0), al1 = fast_exp2(m_run[nb][1] - mn1);
-            m_run[nb][0] = mn0;
-            m_run[nb][1] = mn1;
-            const uint32_t r0 = pack_bf16x2(fast_exp2(x0 - mn0), fast_exp2(x1 - mn1));  // token g
-            const uint32_t r1 = pack_bf16x2(fast_exp2(x2 - mn0), fast_exp2(x3 - mn1));  // token g+8
-            // the sum uses the bf16-rounded weights that enter P.V
-            l_run[nb][0] = l_run[nb][0] * al0 + (bf16lo_to_f32(r0) + bf16lo_to_f32(r1));
-            l_run[nb][1] = l_run[nb][1] * al1 + (bf16hi_to_f32(r0) + bf16hi_to_f32(r1));
+          }
+          float s[NB][4];
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s[nb][i] = se[nb][i] + so[nb][i];
+          // fragment element i: token g + 8*(i>>1), head 8*nb + 2t + (i&1)
+          if (SCORES) {
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int head = nb * 8 + 2 * t + (i & 1);
+                const int tok = g + 8 * (i >> 1);
+                if (head < G && tok < vw)
+                  p.scores[(long long)c.b * p.s_sb + (long long)(c.kvh * G + head) * p.s_sh + t0 + tb + tok] =
+                      s[nb][i];
+              }
+          } else {
+            const bool v0 = g < vw, v1 = g + 8 < vw;
+            uint32_t pb[NB][2];
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              const float x0 = v0 ? s[nb][0] * sl2 : kNegInf;
+              const float x1 = v0 ? s[nb][1] * sl2 : kNegInf;
+              const float x2 = v1 ? s[nb][2] * sl2 : kNegInf;
+              const float x3 = v1 ? s[nb][3] * sl2 : kNegInf;
+              float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+              for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+              }
+              const float mn0 = fmaxf(m_run[nb][0], mx0), mn1 = fmaxf(m_run[nb][1], mx1);
+              const float al0 = fast_exp2(m_run[nb][0] - mn0), al1 = fast_exp2(m_run[nb][1] - mn1);
+              m_run[nb][0] = mn0;
+              m_run[nb][1] = mn1;
+              const uint32_t r0 = pack_bf16x2(fast_exp2(x0 - mn0), fast_exp2(x1 - mn1));  // token g
+              const uint32_t r1 = pack_bf16x2(fast_exp2(x2 - mn0), fast_exp2(x3 - mn1));  // token g+8
+              // the sum uses the bf16-rounded weights that enter P.V
+              l_run[nb][0] = l_run[nb][0] * al0 + (bf16lo_to_f32(r0) + bf16lo_to_f32(r1));
+              l_run[nb][1] = l_run[nb][1] * al1 + (bf16hi_to_f32(r0) + bf16hi_to_f32(r1));
+#pragma unroll
+              for (int mb = 0; mb < 8; ++mb) {
+                o[mb][nb][0] *= al0;
+                o[mb][nb][1] *= al1;
+                o[mb][nb][2] *= al0;
+                o[mb][nb][3] *= al1;
+              }
+              pb[nb][0] = movmatrix_trans(r0);  // P[head g][tokens 2t, 2t+1]
+              pb[nb][1] = movmatrix_trans(r1);  // P[head g][tokens 2t+8, 2t+9]
+            }
+            // ---- O^T[128 dims][8*NB heads] += V_tile^T . P^T
+            const uint32_t vbase = kbase + kKTileBytes;
+            const int jm = lane >> 3;
+            const int row = tb + (lane & 7) + (jm >> 1) * 8;
 #pragma unroll
             for (int mb = 0; mb < 8; ++mb) {
-              o[mb][nb][0] *= al0;
-              o[mb][nb][1] *= al1;
-              o[mb][nb][2] *= al0;
-              o[mb][nb][3] *= al1;
-            }
-            pb[nb][0] = movmatrix_trans(r0);  // P[head g][tokens 2t, 2t+1]
-            pb[nb][1] = movmatrix_trans(r1);  // P[head g][tokens 2t+8, 2t+9]
-          }
-          // ---- O^T[128 dims][8*NB heads] += V_tile^T . P^T
-          const uint32_t vbase = kbase + kKTileBytes;
-          const int jm = lane >> 3;
-          const int row = tb + (lane & 7) + (jm >> 1) * 8;
+              const int chunk = 2 * (mb & 3) + (jm & 1);
+              const uint32_t addr = vbase + (mb >> 2) * kHalfBytes + row * 128 + ((chunk ^ (lane & 7)) << 4);
+              uint32_t a[4];
+              ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
+              if (vw < 16) {  // rows past the sequence may hold anything; P is 0 there
+                a[0] = mask_tokens(a[0], 2 * t, vw);
+                a[1] = mask_tokens(a[1], 2 * t, vw);
+                a[2] = mask_tokens(a[2], 2 * t + 8, vw);
+                a[3] = mask_tokens(a[3], 2 * t + 8, vw);
+              }
 #pragma unroll
-          for (int mb = 0; mb < 8; ++mb) {
-            const int chunk = 2 * (mb & 3) + (jm & 1);
-            const uint32_t addr = vbase + (mb >> 2) * kHalfBytes + row * 128 + ((chunk ^ (lane & 7)) << 4);
-            uint32_t a[4];
-            ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
-            if (vw < 16) {  // rows past the sequence may hold anything; P is 0 there
-              a[0] = mask_tokens(a[0], 2 * t, vw);
-              a[1] = mask_tokens(a[1], 2 * t, vw);
-              a[2] = mask_tokens(a[2], 2 * t + 8, vw);
-              a[3] = mask_tokens(a[3], 2 * t + 8, vw);
+              for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(o[mb][nb], a, pb[nb][0], pb[nb][1]);
             }
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(o[mb][nb], a, pb[nb][0], pb[nb][1]);
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(stage));
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(stage));
 
       if (!SCORES && last) {
         // ---------------------------------------- finish this sequence segment
-        const int b = ti.b, kvh = ti.kvh, seq = b * Hkv + kvh;
+        const int b = c.b, kvh = c.kvh, seq = b * Hkv + kvh;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+          for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) l_run[nb][c] += __shfl_xor_sync(0xffffffffu, l_run[nb][c], off);
-        float* mo = merge_o + warp * kMaxGroup * kMergeRow;
+            for (int off = 4; off < 32; off <<= 1) l_run[nb][cc] += __shfl_xor_sync(0xffffffffu, l_run[nb][cc], off);
+        float* mo = merge_o + wg * HP * kMergeRow;
+        float* ml = merge_ml + wg * HP * 2;
+        // (1) group 1 hands its state to the partner warp of group 0
+        if (grp == 1) {
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          const int h0 = nb * 8 + 2 * t;
+          for (int nb = 0; nb < NB; ++nb) {
+            const int h0 = nb * 8 + 2 * t;
 #pragma unroll
-          for (int mb = 0; mb < 8; ++mb) {
-            mo[h0 * kMergeRow + mb * 16 + g] = o[mb][nb][0];
-            mo[(h0 + 1) * kMergeRow + mb * 16 + g] = o[mb][nb][1];
-            mo[h0 * kMergeRow + mb * 16 + g + 8] = o[mb][nb][2];
-            mo[(h0 + 1) * kMergeRow + mb * 16 + g + 8] = o[mb][nb][3];
-          }
-          if (g == 0) {
-            float* ml = merge_ml + (warp * kMaxGroup + h0) * 2;
-            ml[0] = m_run[nb][0];
-            ml[1] = l_run[nb][0];
-            ml[2] = m_run[nb][1];
-            ml[3] = l_run[nb][1];
+            for (int mb = 0; mb < 8; ++mb) {
+              mo[h0 * kMergeRow + mb * 16 + g] = o[mb][nb][0];
+              mo[(h0 + 1) * kMergeRow + mb * 16 + g] = o[mb][nb][1];
+              mo[h0 * kMergeRow + mb * 16 + g + 8] = o[mb][nb][2];
+              mo[(h0 + 1) * kMergeRow + mb * 16 + g + 8] = o[mb][nb][3];
+            }
+            if (g == 0) {
+              ml[h0 * 2] = m_run[nb][0];
+              ml[h0 * 2 + 1] = l_run[nb][0];
+              ml[h0 * 2 + 2] = m_run[nb][1];
+              ml[h0 * 2 + 3] = l_run[nb][1];
+            }
           }
         }
-        named_bar_sync(1, kConsumerWarps * 32);
+        named_bar_sync(1, kConsumerThreads);
+        // (2) group 0 merges it into registers and publishes the pair's state
+        if (grp == 0) {
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int h = nb * 8 + 2 * t + cc;
+              const float mp = ml[h * 2], lp = ml[h * 2 + 1];
+              const float mn = fmaxf(m_run[nb][cc], mp);
+              const float mref = mn == kNegInf ? 0.f : mn;  // both empty: stay empty
+              const float a_self = fast_exp2(m_run[nb][cc] - mref), a_part = fast_exp2(mp - mref);
+              l_run[nb][cc] = l_run[nb][cc] * a_self + lp * a_part;
+              m_run[nb][cc] = mn;
+#pragma unroll
+              for (int mb = 0; mb < 8; ++mb) {
+                o[mb][nb][cc] = o[mb][nb][cc] * a_self + mo[h * kMergeRow + mb * 16 + g] * a_part;
+                o[mb][nb][cc + 2] = o[mb][nb][cc + 2] * a_self + mo[h * kMergeRow + mb * 16 + g + 8] * a_part;
+              }
+            }
+          }
+          __syncwarp();
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            const int h0 = nb * 8 + 2 * t;
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb) {
+              mo[h0 * kMergeRow + mb * 16 + g] = o[mb][nb][0];
+              mo[(h0 + 1) * kMergeRow + mb * 16 + g] = o[mb][nb][1];
+              mo[h0 * kMergeRow + mb * 16 + g + 8] = o[mb][nb][2];
+              mo[(h0 + 1) * kMergeRow + mb * 16 + g + 8] = o[mb][nb][3];
+            }
+            if (g == 0) {
+              ml[h0 * 2] = m_run[nb][0];
+              ml[h0 * 2 + 1] = l_run[nb][0];
+              ml[h0 * 2 + 2] = m_run[nb][1];
+              ml[h0 * 2 + 3] = l_run[nb][1];
+            }
+          }
+        }
+        named_bar_sync(1, kConsumerThreads);
 
-        const long long F = prefix[b] + (long long)kvh * ti.nt;  // first tile of this sequence
-        const int first_cta = cta_of(F, T, P), last_cta = cta_of(F + ti.nt - 1, T, P);
+        // (3) merge the four pair states: thread -> (head parity, dim)
+        const long long F = prefix[b] + (long long)kvh * c.nt;  // first tile of this sequence
+        const int first_cta = cta_of(F, T, P), last_cta = cta_of(F + c.nt - 1, T, P);
         const int n_parts = last_cta - first_cta + 1;
-        const int d = tid;  // 128 consumer threads <-> 128 head dims
-        for (int h = 0; h < G; ++h) {
+        const int d = tid & 127;
+        for (int h = tid >> 7; h < G; h += 2) {
           float M = kNegInf;
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge_ml[(w * kMaxGroup + h) * 2]);
+          for (int w = 0; w < kGroupWarps; ++w) M = fmaxf(M, merge_ml[(w * HP + h) * 2]);
           float lsum = 0.f, acc = 0.f;
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float f = fast_exp2(merge_ml[(w * kMaxGroup + h) * 2] - M);  // 0 for a warp with no tokens
-            lsum += f * merge_ml[(w * kMaxGroup + h) * 2 + 1];
-            acc += f * merge_o[(w * kMaxGroup + h) * kMergeRow + d];
+          for (int w = 0; w < kGroupWarps; ++w) {
+            const float f = fast_exp2(merge_ml[(w * HP + h) * 2] - M);  // 0 for a pair with no tokens
+            lsum += f * merge_ml[(w * HP + h) * 2 + 1];
+            acc += f * merge_o[(w * HP + h) * kMergeRow + d];
           }
           if (n_parts == 1) {
             p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
@@ -366,12 +446,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
         }
         if (n_parts > 1) {
           __threadfence();
-          named_bar_sync(1, kConsumerWarps * 32);
+          named_bar_sync(1, kConsumerThreads);
           if (tid == 0) flags[1] = (atomicAdd(p.counters + seq, 1) == n_parts - 1);
-          named_bar_sync(1, kConsumerWarps * 32);
+          named_bar_sync(1, kConsumerThreads);
           if (flags[1]) {  // every other part has landed: merge them all
             __threadfence();
-            for (int h = 0; h < G; ++h) {
+            for (int h = tid >> 7; h < G; h += 2) {
               float M = kNegInf;
               for (int pc = first_cta; pc <= last_cta; ++pc)
                 M = fmaxf(M, __ldcg(p.part_ml + (((long long)pc + seq) * p.gpad + h) * 2));
@@ -388,7 +468,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
             if (tid == 0) p.counters[seq] = 0;  // ready for the next call
           }
         }
-        named_bar_sync(1, kConsumerWarps * 32);  // merge scratch and flags free again
+        named_bar_sync(1, kConsumerThreads);  // merge scratch and flags free again
+        // the next segment starts from an empty state
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          m_run[nb][0] = m_run[nb][1] = kNegInf;
+          l_run[nb][0] = l_run[nb][1] = 0.f;
+#pragma unroll
+          for (int mb = 0; mb < 8; ++mb) o[mb][nb][0] = o[mb][nb][1] = o[mb][nb][2] = o[mb][nb][3] = 0.f;
+        }
       }
     }
   }
@@ -407,11 +495,11 @@ cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
     e = cudaFuncSetAttribute(attn_decode_kernel<NB, SCORES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)attn_smem_bytes(kMaxBatch));
+                             (int)attn_smem_bytes(kMaxBatch, NB));
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  attn_decode_kernel<NB, SCORES><<<grid, kAttnThreads, attn_smem_bytes(p.B), stream>>>(p);
+  attn_decode_kernel<NB, SCORES><<<grid, kAttnThreads, attn_smem_bytes(p.B, NB), stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -12,29 +12,41 @@ namespace da {
 
 // ----------------------------------------------------------- split-KV attention
 constexpr int kHeadDim = 128;
-constexpr int kTile = 64;                       // tokens per pipeline stage
-constexpr int kConsumerWarps = 4;               // each owns 16 tokens of a stage
-constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;  // + one TMA producer warp
-constexpr int kStages = 4;
-constexpr int kHalfBytes = kTile * 128;         // 64 tokens x 64 dims x bf16 (one 128B-swizzled box)
-constexpr int kKTileBytes = 2 * kHalfBytes;     // 64 tokens x 128 dims
-constexpr int kStageBytes = 2 * kKTileBytes;    // K tile + V tile
-constexpr int kQRowBytes = 272;                 // 256 B of q + 16 B pad (conflict-free fragment loads)
+constexpr int kTile = 64;                      // tokens per pipeline stage
+constexpr int kGroupWarps = 4;                 // consumer warps per group; each owns 16 tokens of a stage
+constexpr int kGroups = 2;                     // consumer groups take alternate stages
+constexpr int kConsumerThreads = kGroups * kGroupWarps * 32;
+constexpr int kAttnThreads = kConsumerThreads + 32;  // + one TMA producer warp
+constexpr int kStages = 4;                     // even: stage s always belongs to group s % 2
+constexpr int kHalfBytes = kTile * 128;        // 64 tokens x 64 dims x bf16 (one 128B-swizzled box)
+constexpr int kKTileBytes = 2 * kHalfBytes;    // 64 tokens x 128 dims
+constexpr int kStageBytes = 2 * kKTileBytes;   // K tile + V tile
+constexpr int kQRowBytes = 272;                // 256 B of q + 16 B pad (conflict-free fragment loads)
 constexpr int kMaxGroup = 16;
 constexpr int kMaxBatch = 1024;
-constexpr int kQSlotBytes = kMaxGroup * kQRowBytes;
-constexpr int kMergeRow = 132;                  // floats per head row of the merge scratch (128 + pad)
+constexpr int kMergeRow = 132;                 // floats per head row of the merge scratch (128 + pad)
+static_assert(kStages % kGroups == 0, "a stage must always be consumed by the same group");
 
-constexpr size_t attn_smem_bytes(int batch) {
-  return 1024                                                  // alignment slack
-         + (size_t)kStages * kStageBytes                       // K/V ring
-         + (size_t)kStages * kQSlotBytes                       // q rows per stage
-         + (size_t)kConsumerWarps * kMaxGroup * kMergeRow * 4  // per-warp O
-         + (size_t)kConsumerWarps * kMaxGroup * 2 * 4          // per-warp (m, l)
-         + (size_t)2 * kStages * 8                             // full/empty barriers
-         + 16                                                  // flags
-         + (size_t)(batch + 1) * 4;                            // tile prefix over the batch
-}
+// Shared-memory carve-up of the attention kernel; nb = 8-head blocks (1 or 2).
+struct AttnSmem {
+  int nb, batch;
+  __host__ __device__ constexpr AttnSmem(int nb_, int batch_) : nb(nb_), batch(batch_) {}
+  __host__ __device__ constexpr int heads() const { return 8 * nb; }
+  __host__ __device__ constexpr size_t q_slot() const { return (size_t)heads() * kQRowBytes; }
+  __host__ __device__ constexpr size_t off_q() const { return (size_t)kStages * kStageBytes; }
+  __host__ __device__ constexpr size_t off_merge_o() const { return off_q() + kStages * q_slot(); }
+  __host__ __device__ constexpr size_t off_merge_ml() const {
+    return off_merge_o() + (size_t)kGroupWarps * heads() * kMergeRow * 4;
+  }
+  __host__ __device__ constexpr size_t off_bars() const { return off_merge_ml() + (size_t)kGroupWarps * heads() * 2 * 4; }
+  __host__ __device__ constexpr size_t off_flags() const { return off_bars() + 2 * kStages * 8; }
+  __host__ __device__ constexpr size_t off_prefix() const { return off_flags() + 16; }
+  __host__ __device__ constexpr size_t off_lens() const { return off_prefix() + (size_t)(batch + 1) * 4; }
+  __host__ __device__ constexpr size_t total() const { return 1024 + off_lens() + (size_t)batch * 4; }
+};
+
+constexpr size_t attn_smem_bytes(int batch, int nb) { return AttnSmem(nb, batch).total(); }
+static_assert(AttnSmem(2, kMaxBatch).total() <= 232448, "attention kernel exceeds 227 KB of shared memory");
 
 struct AttnParams {
   CUtensorMap tm_k;  // [B][Hkv][Lcap][128] bf16, box 64 dims x 64 tokens, 128B swizzle
