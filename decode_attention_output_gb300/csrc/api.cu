@@ -23,8 +23,9 @@ struct Options {
   int64_t attn_ctas = 0;
   int64_t oproj_path = 0;  // 0 auto, 1 gemv, 2 tcgen05
   int64_t oproj_splitk = 0;
-  int64_t gemm_min_batch = 1 << 30;  // auto mode keeps the GEMV until the GEMM path is enabled
+  int64_t gemm_min_batch = 4;  // measured crossover: GEMV ahead at B <= 2, even at 4, GEMM ahead from 8
   int64_t pdl = 1;
+  int64_t l2_prefetch = 0;  // fused step: the attention kernel pulls W_o into L2 (measured slower: off)
 };
 std::mutex g_mu;
 Options g_opt;
@@ -133,6 +134,21 @@ int encode_kv_map(CUtensorMap* map, const da_tensor_t* t) {
   cuuint32_t box[4] = {64, (cuuint32_t)kTile, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_UNSUPPORTED;
+}
+
+// 2-D map over a row-major bf16 matrix [rows][cols] with row stride `ld` elements;
+// box = 64 columns x box_rows rows, 128-byte swizzle.
+int encode_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return DA_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(rows == 1 ? cols : ld) * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_UNSUPPORTED;
@@ -276,10 +292,78 @@ int run_gemv(const __nv_bfloat16* x, long long x_sb, const da_tensor_t* w, const
   return launch_gemv(gp, pl.bt, pdl, stream) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
+struct UmmaPlan {
+  int npad, ksplit;
+  size_t bytes;
+};
+
+UmmaPlan plan_umma(int B, int K, int N, const Options& o) {
+  UmmaPlan pl;
+  pl.npad = B <= 16 ? 16 : (B <= 32 ? 32 : (B <= 64 ? 64 : 128));
+  const int bchunks = (B + pl.npad - 1) / pl.npad;
+  const int mtiles = (N + kUmmaBM - 1) / kUmmaBM;
+  const int nkb = (K + kUmmaBK - 1) / kUmmaBK;
+  const int sms = std::max(1, sm_count());
+  int ks = (int)o.oproj_splitk;
+  if (ks <= 0) ks = std::max(1, 2 * sms / std::max(1, mtiles * bchunks));  // two CTAs per SM
+  pl.ksplit = std::max(1, std::min(ks, nkb));
+  pl.bytes = pl.ksplit > 1 ? align_up((size_t)pl.ksplit * B * N * 4, 256) : 0;
+  return pl;
+}
+
+int run_umma(const void* x, long long x_sb, const da_tensor_t* w, const da_tensor_t* out, int B, int K, int N,
+             char* ws, char* scratch, const UmmaPlan& pl, bool pdl, cudaStream_t stream) {
+  const int bchunks = (B + pl.npad - 1) / pl.npad;
+  const int mtiles = (N + kUmmaBM - 1) / kUmmaBM;
+  if ((int64_t)bchunks * mtiles > (int64_t)kMaxCounters) return DA_ERR_UNSUPPORTED;
+  UmmaParams up;
+  memset(&up, 0, sizeof(up));
+  DA_TRY(encode_2d_map(&up.tm_w, w->data, K, N, w->stride[0], kUmmaBK));
+  DA_TRY(encode_2d_map(&up.tm_x, x, B, K, x_sb, pl.npad));
+  up.y = static_cast<__nv_bfloat16*>(out->data);
+  up.y_sb = out->stride[0];
+  up.part = reinterpret_cast<float*>(scratch);
+  up.counters = reinterpret_cast<int*>(ws + kGemvCntOff);
+  up.err = reinterpret_cast<int*>(ws + kErrOff);
+  up.B = B;
+  up.K = K;
+  up.N = N;
+  up.ksplit = pl.ksplit;
+  return launch_umma(up, pl.npad, pdl, stream) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+// The projection step: picks the CUDA-core GEMV or the tcgen05 GEMM by batch size
+// (or the "oproj_path" option) and says how much scratch it needs.
+struct ProjPlan {
+  bool gemm;
+  GemvPlan gv;
+  UmmaPlan um;
+  size_t bytes;
+};
+
+ProjPlan plan_projection(int B, int K, int N, const Options& o) {
+  ProjPlan pl;
+  pl.gemm = o.oproj_path == 2 || (o.oproj_path == 0 && B >= o.gemm_min_batch);
+  if (pl.gemm) {
+    pl.um = plan_umma(B, K, N, o);
+    pl.bytes = pl.um.bytes;
+  } else {
+    pl.gv = plan_gemv(B, K, N, o);
+    pl.bytes = pl.gv.bytes;
+  }
+  return pl;
+}
+
+int run_projection(const __nv_bfloat16* x, long long x_sb, const da_tensor_t* w, const da_tensor_t* out, int B,
+                   int K, int N, char* ws, char* scratch, const ProjPlan& pl, bool pdl, cudaStream_t stream) {
+  if (pl.gemm) return run_umma(x, x_sb, w, out, B, K, N, ws, scratch, pl.um, pdl, stream);
+  return run_gemv(x, x_sb, w, out, B, K, N, ws, scratch, pl.gv, pdl, stream);
+}
+
 int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t* v, const da_tensor_t* lens,
                   const AttnShape& s, const AttnPlan& pl, char* ws, char* scratch, __nv_bfloat16* attn,
                   long long a_sb, long long a_sh, float* scores, long long s_sb, long long s_sh, float scale,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, const void* prefetch = nullptr, long long prefetch_bytes = 0) {
   AttnParams p;
   memset(&p, 0, sizeof(p));
   DA_TRY(encode_kv_map(&p.tm_k, k));
@@ -305,6 +389,8 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
   p.Lcap = s.Lcap;
   p.gpad = pl.gpad;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.prefetch = static_cast<const char*>(prefetch);
+  p.prefetch_bytes = prefetch ? (prefetch_bytes & ~15ll) : 0;
   return launch_attention(p, pl.grid, pl.nb, scores != nullptr, stream) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
@@ -338,6 +424,7 @@ int decode_attn_set_option(const char* key, int64_t value) {
   else if (!strcmp(key, "oproj_splitk") && value >= 0 && value <= 4096) g_opt.oproj_splitk = value;
   else if (!strcmp(key, "gemm_min_batch") && value >= 1) g_opt.gemm_min_batch = value;
   else if (!strcmp(key, "pdl") && (value == 0 || value == 1)) g_opt.pdl = value;
+  else if (!strcmp(key, "l2_prefetch") && (value == 0 || value == 1)) g_opt.l2_prefetch = value;
   else return DA_ERR_OPTION;
   return DA_OK;
 }
@@ -350,6 +437,7 @@ int decode_attn_get_option(const char* key, int64_t* value) {
   else if (!strcmp(key, "oproj_splitk")) *value = g_opt.oproj_splitk;
   else if (!strcmp(key, "gemm_min_batch")) *value = g_opt.gemm_min_batch;
   else if (!strcmp(key, "pdl")) *value = g_opt.pdl;
+  else if (!strcmp(key, "l2_prefetch")) *value = g_opt.l2_prefetch;
   else return DA_ERR_OPTION;
   return DA_OK;
 }
@@ -400,12 +488,12 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
   if (K <= 0 || N <= 0 || K % 8 || N % 8) return DA_ERR_SHAPE;
   if (K > (1 << 30) || N > (1 << 30)) return DA_ERR_UNSUPPORTED;
   const Options o = options_snapshot();
-  const GemvPlan pl = plan_gemv((int)B, (int)K, (int)N, o);
+  const ProjPlan pl = plan_projection((int)B, (int)K, (int)N, o);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = nullptr;
   DA_TRY(workspace_get(pl.bytes, st, &ws));
-  return run_gemv(static_cast<const __nv_bfloat16*>(attn_flat->data), attn_flat->stride[0], o_weight, out, (int)B,
-                  (int)K, (int)N, ws, ws + kHeaderBytes, pl, false, st);
+  return run_projection(static_cast<const __nv_bfloat16*>(attn_flat->data), B > 1 ? attn_flat->stride[0] : K,
+                        o_weight, out, (int)B, (int)K, (int)N, ws, ws + kHeaderBytes, pl, false, st);
 }
 
 int decode_attn_fwd(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
@@ -423,17 +511,19 @@ int decode_attn_fwd(const da_tensor_t* q, const da_tensor_t* k_cache, const da_t
   if (s.B == 0) return DA_OK;
   const Options o = options_snapshot();
   const AttnPlan ap = plan_attention(s, o);
-  const GemvPlan gp = plan_gemv(s.B, (int)K, (int)N, o);
+  const ProjPlan gp = plan_projection(s.B, (int)K, (int)N, o);
   const size_t attn_bytes = align_up((size_t)s.B * K * 2, 256);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = nullptr;
   DA_TRY(workspace_get(ap.bytes + attn_bytes + gp.bytes, st, &ws));
   char* scratch = ws + kHeaderBytes;
   __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(scratch + ap.bytes);
+  // W_o span: rows 0..K-1 of stride w_sk, the last row N wide
+  const long long w_span = ((long long)(K - 1) * o_weight->stride[0] + N) * 2;
   DA_TRY(run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, kHeadDim, nullptr, 0, 0, scale,
-                       st));
-  return run_gemv(attn, K, o_weight, out, s.B, (int)K, (int)N, ws, scratch + ap.bytes + attn_bytes, gp, o.pdl != 0,
-                  st);
+                       st, o.l2_prefetch ? o_weight->data : nullptr, w_span));
+  return run_projection(attn, K, o_weight, out, s.B, (int)K, (int)N, ws, scratch + ap.bytes + attn_bytes, gp,
+                        o.pdl != 0, st);
 }
 
 int decode_attn_device_error(void* stream, int32_t* host_code) {

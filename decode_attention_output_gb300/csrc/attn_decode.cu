@@ -157,6 +157,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
     if (lane == 0 && start < end) {
       prefetch_tensormap(&p.tm_k);
       if (!SCORES) prefetch_tensormap(&p.tm_v);
+      const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read exactly once
+      // This CTA's share of the prefetch region, in 4 KB-aligned pieces, one per tile.
+      const uint64_t pf_policy = l2_policy_evict_last();
+      const long long pf_per_cta = ((p.prefetch_bytes + P - 1) / P + 4095) & ~4095ll;
+      const long long pf_begin = min((long long)cta * pf_per_cta, p.prefetch_bytes);
+      const long long pf_end = min(pf_begin + pf_per_cta, p.prefetch_bytes);
+      const long long pf_piece = ((pf_end - pf_begin + (end - start) - 1) / (end - start) + 4095) & ~4095ll;
+      long long pf_next = pf_begin;
       Cursor c = cursor_at(start, prefix, B, Hkv);
       long long seg0 = start;
       int it = 0;
@@ -175,11 +183,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
         mbar_arrive_expect_tx(fb, bytes);
         const uint32_t kdst = ring + stage * kStageBytes;
         const int t0 = c.j * kTile;
-        tma_load_4d(kdst, &p.tm_k, fb, 0, t0, c.kvh, c.b);
-        tma_load_4d(kdst + kHalfBytes, &p.tm_k, fb, 64, t0, c.kvh, c.b);
+        tma_load_4d_hint(kdst, &p.tm_k, fb, 0, t0, c.kvh, c.b, kv_policy);
+        tma_load_4d_hint(kdst + kHalfBytes, &p.tm_k, fb, 64, t0, c.kvh, c.b, kv_policy);
         if (!SCORES) {
-          tma_load_4d(kdst + kKTileBytes, &p.tm_v, fb, 0, t0, c.kvh, c.b);
-          tma_load_4d(kdst + kKTileBytes + kHalfBytes, &p.tm_v, fb, 64, t0, c.kvh, c.b);
+          tma_load_4d_hint(kdst + kKTileBytes, &p.tm_v, fb, 0, t0, c.kvh, c.b, kv_policy);
+          tma_load_4d_hint(kdst + kKTileBytes + kHalfBytes, &p.tm_v, fb, 64, t0, c.kvh, c.b, kv_policy);
+        }
+        for (long long todo = min(pf_piece, pf_end - pf_next); todo > 0;) {
+          const long long n = min(todo, 32768ll);
+          bulk_prefetch_l2(p.prefetch + pf_next, (uint32_t)n, pf_policy);
+          pf_next += n;
+          todo -= n;
         }
         if (with_q) {
           const uint32_t qdst = smem_u32(q_slots + stage * kFixed.q_slot());

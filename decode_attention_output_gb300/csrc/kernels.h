@@ -65,6 +65,10 @@ struct AttnParams {
   int B, Hkv, G, Lcap;
   int gpad;              // 8 or 16 (heads per group rounded up to the MMA width)
   float scale_log2;      // scale * log2(e)
+  // Optional region the next kernel reads (the projection weights): pulled into L2
+  // in pieces while the K/V stream runs. prefetch_bytes = 0 disables it.
+  const char* prefetch;
+  long long prefetch_bytes;
 };
 
 // grid = number of persistent CTAs; nb = 1 for G <= 8, 2 for G <= 16.
@@ -90,5 +94,26 @@ struct GemvParams {
 // bt = batch rows per CTA (1, 2, 4 or 8); grid = (col blocks, ksplit, batch chunks).
 cudaError_t launch_gemv(const GemvParams& p, int bt, bool pdl, cudaStream_t stream);
 size_t gemv_smem_bytes(int bt, int kc);
+
+
+// ------------------------------------------- projection: tcgen05 tensor-core path
+constexpr int kUmmaThreads = 128;  // warp 0: TMA producer, warp 1: MMA issuer, all four: epilogue
+constexpr int kUmmaBM = 128;       // hidden columns per tile (the MMA's M, swap-AB)
+constexpr int kUmmaBK = 64;        // k rows per pipeline stage
+
+struct UmmaParams {
+  CUtensorMap tm_w;  // W [K][N] bf16 row-major: box 64 columns x 64 rows, 128B swizzle
+  CUtensorMap tm_x;  // X [B][K] bf16: box 64 k x npad batch rows, 128B swizzle
+  __nv_bfloat16* y;  // [B][N]
+  long long y_sb;
+  float* part;       // [ksplit][B][N] fp32 split-K partials
+  int* counters;     // [batch chunks][column tiles]
+  int* err;
+  int B, K, N, ksplit;
+};
+
+size_t umma_smem_bytes(int npad);
+// grid = (ceil(N / 128), ksplit, ceil(B / npad)); npad in {16, 32, 64, 128}.
+cudaError_t launch_umma(const UmmaParams& p, int npad, bool pdl, cudaStream_t stream);
 
 }  // namespace da

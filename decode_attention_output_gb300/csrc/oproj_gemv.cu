@@ -115,12 +115,23 @@ __global__ void __launch_bounds__(kGemvThreads, 2) oproj_gemv_kernel(const __gri
   if (*flag) {  // last k-slice of this column block: sum all slices in order
     __threadfence();
     const int c = col0 + tid;
-    for (int b = 0; b < BT; ++b) {
-      if (b0 + b >= p.B || c >= p.N) continue;
-      float sum = 0.f;
-      for (int s = 0; s < p.ksplit; ++s) sum += __ldcg(p.part + ((long long)s * p.B + b0 + b) * p.N + c);
-      p.y[(long long)(b0 + b) * p.y_sb + c] = __float2bfloat16_rn(sum);
+    const bool c_ok = c < p.N;
+    float sum[BT];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) sum[b] = 0.f;
+    // slice s is added after slice s-1 (a fixed order); eight slices' loads go out together
+    for (int s0 = 0; s0 < p.ksplit; s0 += 8) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int s = s0 + u;
+#pragma unroll
+        for (int b = 0; b < BT; ++b)
+          if (c_ok && s < p.ksplit && b0 + b < p.B) sum[b] += __ldcg(p.part + ((long long)s * p.B + b0 + b) * p.N + c);
+      }
     }
+#pragma unroll
+    for (int b = 0; b < BT; ++b)
+      if (c_ok && b0 + b < p.B) p.y[(long long)(b0 + b) * p.y_sb + c] = __float2bfloat16_rn(sum[b]);
     if (tid == 0) *counter = 0;
   }
 }

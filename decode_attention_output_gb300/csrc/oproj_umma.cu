@@ -1,0 +1,233 @@
+// oproj_umma.cu -- output projection on the 5th-generation tensor cores (tcgen05,
+// accumulator in TMEM) for batches where it is a real dense contraction:
+//   y[b][n] = sum_k x[b][k] * W[k][n]   (bf16 operands, fp32 accumulation, bf16 out)
+// the page's `result = matmul(attn_output_flat, o_weight, DT_BF16)` (page "PyPTO
+// 开箱性能调优实战 Decode Attention 多 Matmul 独立 TileShape 配置 F-16", section
+// "代码对比"; output_proj row of its shape table: M = batch, K = N = hidden).
+//
+// Swap-AB: the MMA computes y^T[n][b] = W^T[n][k] . x^T[k][b], so the MMA's M is
+// 128 hidden columns and its N is the batch (padded to 16/32/64/128 rows with
+// TMA zero fill). W is [K][N] row-major, i.e. the A operand is MN-major: two TMA
+// boxes of 64 columns x 64 k-rows (128-byte swizzle) per stage form its canonical
+// layout (leading byte offset = distance between the two 64-column atoms, stride
+// byte offset = 1024 between groups of eight k-rows). x is K-major (canonical
+// 128-byte swizzled rows). One thread issues tcgen05.mma, tcgen05.commit frees
+// each stage, and the four warps read the fp32 accumulator out of TMEM.
+// Split-K partials are summed in a fixed order by the CTA that completes a
+// column tile last (atomic counter, no waiting).
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace da {
+namespace {
+
+// Two CTAs per SM: each keeps about 100 KB of W in flight (more stages for narrow batches).
+template <int NPAD>
+struct UmmaCfg {
+  static constexpr int kABytes = kUmmaBM * kUmmaBK * 2;  // 16 KB: two 64-column boxes
+  static constexpr int kBBytes = NPAD * kUmmaBK * 2;
+  static constexpr int kStage = kABytes + ((kBBytes + 1023) / 1024) * 1024;
+  static constexpr int kStages = NPAD <= 16 ? 6 : (NPAD <= 32 ? 5 : (NPAD <= 64 ? 4 : 3));
+  static constexpr int kTmemCols = NPAD < 32 ? 32 : NPAD;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + (2 * kStages + 1) * 8 + 16;
+  static_assert(kSmem <= 113 * 1024, "two CTAs per SM");
+};
+
+template <int NPAD>
+__global__ void __launch_bounds__(kUmmaThreads, 2) oproj_umma_kernel(const __grid_constant__ UmmaParams p) {
+  using C = UmmaCfg<NPAD>;
+  constexpr uint32_t kIdesc = umma_idesc_bf16(kUmmaBM, NPAD, /*A MN-major*/ true, /*B K-major*/ false);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);  // full[S], empty[S], accum
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 1);
+  int* flag = reinterpret_cast<int*>(tmem_slot + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + C::kStages + s); };
+  const uint32_t accum_bar = smem_u32(bars + 2 * C::kStages);
+
+  const int mt = blockIdx.x, ks = blockIdx.y, bz = blockIdx.z;
+  const int n0 = mt * kUmmaBM, b0 = bz * NPAD;
+  const int nkb = (p.K + kUmmaBK - 1) / kUmmaBK;
+  const int kb0 = (int)((long long)ks * nkb / p.ksplit);
+  const int nk = (int)((long long)(ks + 1) * nkb / p.ksplit) - kb0;  // >= 1: the host keeps ksplit <= nkb
+
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(accum_bar, 1);
+    *flag = 0;
+    fence_barrier_init();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&p.tm_w);
+      prefetch_tensormap(&p.tm_x);
+      const uint32_t ring = smem_u32(smem);
+      const int pre = nk < C::kStages ? nk : C::kStages;
+      // W does not depend on the attention kernel: fill the first stages with it
+      // before waiting for that grid (programmatic dependent launch).
+      for (int it = 0; it < pre; ++it) {
+        const uint32_t a = ring + it * C::kStage;
+        const int k0 = (kb0 + it) * kUmmaBK;
+        mbar_arrive_expect_tx(full_bar(it), C::kABytes + C::kBBytes);
+        tma_load_2d(a, &p.tm_w, full_bar(it), n0, k0);
+        tma_load_2d(a + kUmmaBK * 128, &p.tm_w, full_bar(it), n0 + 64, k0);
+      }
+      pdl_wait_primary();
+      for (int it = 0; it < pre; ++it)
+        tma_load_2d(ring + it * C::kStage + C::kABytes, &p.tm_x, full_bar(it), (kb0 + it) * kUmmaBK, b0);
+      for (int it = pre; it < nk; ++it) {
+        const int s = it % C::kStages;
+        const uint32_t ph = (it / C::kStages) & 1;
+        mbar_wait_bounded(empty_bar(s), ph ^ 1, p.err, kErrWaitEmpty, nullptr);
+        const uint32_t a = ring + s * C::kStage;
+        const int k0 = (kb0 + it) * kUmmaBK;
+        mbar_arrive_expect_tx(full_bar(s), C::kABytes + C::kBBytes);
+        tma_load_2d(a, &p.tm_w, full_bar(s), n0, k0);
+        tma_load_2d(a + kUmmaBK * 128, &p.tm_w, full_bar(s), n0 + 64, k0);
+        tma_load_2d(a + C::kABytes, &p.tm_x, full_bar(s), k0, b0);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t ring = smem_u32(smem);
+      for (int it = 0; it < nk; ++it) {
+        const int s = it % C::kStages;
+        const uint32_t ph = (it / C::kStages) & 1;
+        mbar_wait_bounded(full_bar(s), ph, p.err, kErrWaitFull, nullptr);
+        tc_fence_after_sync();
+        const uint32_t a = ring + s * C::kStage;
+        const uint32_t bsm = a + C::kABytes;
+#pragma unroll
+        for (int kk = 0; kk < kUmmaBK / 16; ++kk) {
+          // A: 16 k-rows per MMA = two 8-row groups (1024 B apart); the second 64-column
+          // atom sits 64 rows x 128 B further. B: 16 k = 32 bytes along each 128-byte row.
+          const uint64_t adesc = umma_smem_desc(a + kk * 16 * 128, kUmmaBK * 128, 1024);
+          const uint64_t bdesc = umma_smem_desc(bsm + kk * 32, 16, 1024);
+          umma_bf16(tmem, adesc, bdesc, kIdesc, (it | kk) != 0);
+        }
+        umma_commit(empty_bar(s));  // the stage is free once these MMAs have read it
+      }
+      umma_commit(accum_bar);
+    }
+  }
+  __syncwarp();
+
+  // ------------------------------------------------------------- epilogue
+  mbar_wait_bounded(accum_bar, 0, p.err, kErrWaitMma, nullptr);
+  tc_fence_after_sync();
+  const int n = n0 + warp * 32 + lane;  // TMEM lane = hidden column within the tile
+  float acc[NPAD];
+#pragma unroll
+  for (int c = 0; c < NPAD / 16; ++c) {
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(tmem + ((uint32_t)(warp * 32) << 16) + c * 16, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[c * 16 + i] = __uint_as_float(r[i]);
+  }
+  const bool n_ok = n < p.N;
+  if (p.ksplit == 1) {
+#pragma unroll
+    for (int b = 0; b < NPAD; ++b)
+      if (n_ok && b0 + b < p.B) p.y[(long long)(b0 + b) * p.y_sb + n] = __float2bfloat16_rn(acc[b]);
+  } else {
+#pragma unroll
+    for (int b = 0; b < NPAD; ++b)
+      if (n_ok && b0 + b < p.B) p.part[((long long)ks * p.B + b0 + b) * p.N + n] = acc[b];
+    __threadfence();
+    __syncthreads();
+    int* counter = p.counters + blockIdx.z * gridDim.x + mt;
+    if (tid == 0) *flag = (atomicAdd(counter, 1) == p.ksplit - 1);
+    __syncthreads();
+    if (*flag) {  // last k-slice of this column tile: sum all slices in order
+      __threadfence();
+      const int nb_valid = p.B - b0 < NPAD ? p.B - b0 : NPAD;
+#pragma unroll
+      for (int b = 0; b < NPAD; ++b) acc[b] = 0.f;
+      // slice s is added after slice s-1 for every output (a fixed order); the loads of
+      // a batch of slices are independent and go out together
+      constexpr int kSlices = NPAD >= 64 ? 1 : 64 / NPAD;  // about 64 loads in flight per thread
+      for (int s0 = 0; s0 < p.ksplit; s0 += kSlices) {
+#pragma unroll
+        for (int u = 0; u < kSlices; ++u) {
+          const int s = s0 + u;
+#pragma unroll
+          for (int b = 0; b < NPAD; ++b)
+            if (n_ok && s < p.ksplit && b < nb_valid)
+              acc[b] += __ldcg(p.part + ((long long)s * p.B + b0 + b) * p.N + n);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < NPAD; ++b)
+        if (n_ok && b < nb_valid) p.y[(long long)(b0 + b) * p.y_sb + n] = __float2bfloat16_rn(acc[b]);
+      if (tid == 0) *counter = 0;
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int NPAD>
+cudaError_t launch_npad(const UmmaParams& p, bool pdl, cudaStream_t stream) {
+  using C = UmmaCfg<NPAD>;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(oproj_umma_kernel<NPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.N + kUmmaBM - 1) / kUmmaBM, p.ksplit, (p.B + NPAD - 1) / NPAD);
+  cfg.blockDim = dim3(kUmmaThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, oproj_umma_kernel<NPAD>, p);
+}
+
+}  // namespace
+
+size_t umma_smem_bytes(int npad) {
+  switch (npad) {
+    case 16: return UmmaCfg<16>::kSmem;
+    case 32: return UmmaCfg<32>::kSmem;
+    case 64: return UmmaCfg<64>::kSmem;
+    default: return UmmaCfg<128>::kSmem;
+  }
+}
+
+cudaError_t launch_umma(const UmmaParams& p, int npad, bool pdl, cudaStream_t stream) {
+  switch (npad) {
+    case 16: return launch_npad<16>(p, pdl, stream);
+    case 32: return launch_npad<32>(p, pdl, stream);
+    case 64: return launch_npad<64>(p, pdl, stream);
+    default: return launch_npad<128>(p, pdl, stream);
+  }
+}
+
+}  // namespace da

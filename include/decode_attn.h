@@ -138,8 +138,13 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *   "oproj_path"    0 auto, 1 CUDA-core GEMV, 2 tcgen05 tensor-core GEMM
  *   "oproj_splitk"  split-K factor of the projection (0: auto)
  *   "gemm_min_batch" smallest batch that takes the tensor-core GEMM in auto mode
+ *                   (default 4)
  *   "pdl"           1 (default): launch the projection with programmatic
  *                   dependent launch so it overlaps the attention kernel's tail
+ *   "l2_prefetch"   0 (default) or 1: in decode_attn_fwd the attention kernel
+ *                   pulls o_weight into L2 while it streams K/V, so that the
+ *                   projection reads o_weight from L2 (measured slower on GB300:
+ *                   the prefetch competes with the K/V stream)
  * Returns DA_OK or DA_ERR_OPTION.
  */
 int decode_attn_set_option(const char* key, int64_t value);

@@ -251,3 +251,56 @@ def test_repeated_calls_are_deterministic():
         outs.append(o)
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+# ------------------------------------------------- tensor-core projection path
+class _Path:
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        self.old = da.decode_attn_get_option("oproj_path")
+        da.decode_attn_set_option("oproj_path", self.path)
+
+    def __exit__(self, *exc):
+        da.decode_attn_set_option("oproj_path", self.old)
+
+
+@pytest.mark.parametrize("B", [1, 8, 9, 16, 17, 32, 33, 64, 65, 128, 130])
+@pytest.mark.parametrize("K,N", [(1088, 384), (256, 264)])
+def test_oproj_gemm_integer_exact(B, K, N):
+    """tcgen05 path: integer operands make every fp32 sum exact, so the result is the
+    bf16 rounding of the exact integer matmul (batch padding 16/32/64/128, batch
+    chunks, ragged split-K and a partial 128-column tile)."""
+    g = torch.Generator(device="cpu").manual_seed(300 + B + K)
+    xi = torch.randint(-8, 9, (B, K), generator=g)
+    wi = torch.randint(-1, 2, (K, N), generator=g)
+    ref = (xi.long() @ wi.long()).double().to(torch.bfloat16)
+    out = torch.full((B, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    with _Path(2):
+        da.decode_attn_oproj(xi.to(torch.bfloat16).to(DEV), wi.to(torch.bfloat16).to(DEV), out)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_error() == 0
+    assert torch.equal(out.cpu(), ref)
+
+
+@pytest.mark.parametrize("B,K,N", [(8, 4096, 4096), (32, 4096, 4096), (64, 1024, 2048), (5, 512, 640)])
+def test_oproj_gemm_matches_oracle(orc, B, K, N):
+    g = torch.Generator(device="cpu").manual_seed(8)
+    x = torch.randn((B, K), generator=g).to(torch.bfloat16)
+    w = (torch.randn((K, N), generator=g) / math.sqrt(K)).to(torch.bfloat16)
+    out = torch.empty((B, N), dtype=torch.bfloat16, device=DEV)
+    with _Path(2):
+        da.decode_attn_oproj(x.to(DEV), w.to(DEV), out)
+    ref = orc.oproj(synth.to_bits(x), synth.to_bits(w))
+    assert_bf16_close(f64(out), ref, "o_proj tcgen05")
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_fused_step_on_each_projection_path(orc, path):
+    w = W("paths", 12, 16, 4, 300, 512, (300, 1, 64, 65, 299, 128, 0, 7, 200, 100, 50, 3))
+    with _Path(path):
+        x, attn, out = _run(w, seed=13)
+    ref_attn, ref_out = oracle_decode(orc, x)
+    assert_bf16_close(f64(attn), ref_attn, f"path {path} attention")
+    assert_bf16_close(f64(out), ref_out, f"path {path} output")
