@@ -179,8 +179,8 @@ def pin_oproj_integer_exact(orc):
 
 
 def pin_oproj_all_ones(orc):
-    """All-ones operands give y = K everywhere (the all-ones golden pattern of the msKPP
-    matmul example on the CANN page "基于msKPP的Kernel性能调优", compared there with np.matmul)."""
+    """All-ones operands give y = K everywhere (the golden check of the basic_matmul
+    example on the CANN page "自动调优流程": all-ones operands compared with np.matmul)."""
     B, K, N = 2, 384, 16
     y = orc.oproj(np.ones((B, K)), to_bf16_bits(np.ones((K, N), np.float32)))
     assert np.array_equal(y, np.full((B, N), float(K))), "all-ones o_proj"

@@ -177,7 +177,7 @@ def test_scores_match_oracle(orc, G, Hkv):
 
 def test_integer_scores_are_exact(orc):
     """Integer-valued q and K: every fp32 partial sum is exact, so the scores equal
-    the oracle bit for bit (the msKPP page's all-integer golden pattern)."""
+    the oracle bit for bit (the integer-valued golden check of the CANN page "自动调优流程")."""
     B, Hq, Hkv, Lcap = 2, 8, 2, 150
     g = torch.Generator(device="cpu").manual_seed(21)
     q = torch.randint(-4, 5, (B, Hq, 128), generator=g).to(torch.bfloat16).to(DEV)
