@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     decode_attn_fwd,
     decode_attn_get_option,
     decode_attn_only,
+    decode_attn_only_noalloc,
     decode_attn_oproj,
     decode_attn_release,
     decode_attn_scores,

@@ -21,7 +21,7 @@ DA_DTYPE_BF16, DA_DTYPE_F32, DA_DTYPE_I32 = 1, 2, 3
 _DTYPES = {torch.bfloat16: DA_DTYPE_BF16, torch.float32: DA_DTYPE_F32, torch.int32: DA_DTYPE_I32}
 
 # every symbol declared in include/decode_attn.h
-EXPORTS = ("decode_attn_fwd", "decode_attn_only", "decode_attn_scores", "decode_attn_oproj",
+EXPORTS = ("decode_attn_fwd", "decode_attn_only", "decode_attn_only_noalloc", "decode_attn_scores", "decode_attn_oproj",
            "decode_attn_set_option", "decode_attn_get_option", "decode_attn_device_error",
            "decode_attn_release", "decode_attn_status_str")
 
@@ -54,6 +54,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             vp, f32, i64 = ctypes.c_void_p, ctypes.c_float, ctypes.c_int64
             lib.decode_attn_fwd.argtypes = [P, P, P, P, P, P, f32, vp]
             lib.decode_attn_only.argtypes = [P, P, P, P, P, f32, vp]
+            lib.decode_attn_only_noalloc.argtypes = [P, P, P, P, P, f32, vp]
             lib.decode_attn_scores.argtypes = [P, P, P, P, vp]
             lib.decode_attn_oproj.argtypes = [P, P, P, vp]
             lib.decode_attn_set_option.argtypes = [ctypes.c_char_p, i64]
@@ -122,6 +123,19 @@ def decode_attn_only(q, k_cache, v_cache, seq_lens, attn_out, scale: float, stre
     lib = load()
     ds = [describe(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
     _check("decode_attn_only", lib.decode_attn_only(*[_ref(d) for d in ds], float(scale), _stream(stream)))
+    return attn_out
+
+
+def decode_attn_only_noalloc(q, k_cache, v_cache, seq_lens, attn_out, scale: float, stream=None) -> torch.Tensor:
+    """decode_attn_only without any device allocation by the library: for callers that
+    must not allocate GPU memory at run time (memory reserved up front by their own
+    pool, or no device-wide synchronisation allowed on the request path). Uses a
+    fixed 8 MiB scratch array inside the library; calls that overlap on the GPU race
+    on it. Raises DecodeAttnError (DA_ERR_SCRATCH) when a call needs more scratch."""
+    lib = load()
+    ds = [describe(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
+    _check("decode_attn_only_noalloc",
+           lib.decode_attn_only_noalloc(*[_ref(d) for d in ds], float(scale), _stream(stream)))
     return attn_out
 
 

@@ -412,6 +412,7 @@ const char* decode_attn_status_str(int code) {
     case DA_ERR_CUDA: return "CUDA error";
     case DA_ERR_OPTION: return "unknown option or bad value";
     case DA_ERR_DEVICE: return "device-side error recorded";
+    case DA_ERR_SCRATCH: return "request needs more than the fixed scratch of the no-allocation entry point";
     default: return "unknown status";
   }
 }
@@ -457,6 +458,66 @@ int decode_attn_only(const da_tensor_t* q, const da_tensor_t* k_cache, const da_
   char* ws = nullptr;
   DA_TRY(workspace_get(pl.bytes, st, &ws));
   return run_attention(q, k_cache, v_cache, seq_lens, s, pl, ws, ws + kHeaderBytes,
+                       static_cast<__nv_bfloat16*>(attn_out->data), attn_out->stride[0], attn_out->stride[1],
+                       nullptr, 0, 0, scale, st);
+}
+
+}  // extern "C"
+
+// ----------------------------------------------- attention without allocation
+// Scratch of decode_attn_only_noalloc: a fixed device array that every GPU loading
+// this library holds until the process exits. Its layout copies the workspace's:
+// the error word and completion counters first (the fixed header), then the
+// split-KV partials of one call.
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
+static_assert(kHeaderBytes < kNoAllocScratchBytes, "header must fit the fixed scratch");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {nullptr};
+
+// Device address of g_noalloc_scratch on the current device. In host code the
+// array's name only stands in for it; the runtime gives the real address, looked up
+// once per device (the first call on a device does this lookup).
+int noalloc_scratch(char** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return DA_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = static_cast<char*>(g_noalloc_addr[dev]);
+  return DA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int decode_attn_only_noalloc(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
+                             const da_tensor_t* seq_lens, const da_tensor_t* attn_out, float scale, void* stream) {
+  AttnShape s;
+  DA_TRY(check_attention_inputs(q, k_cache, v_cache, seq_lens, true, &s));
+  DA_TRY(check_tensor(attn_out, DA_DTYPE_BF16, 3, kOutput));
+  if (attn_out->shape[0] != s.B || attn_out->shape[1] != s.Hq || attn_out->shape[2] != kHeadDim)
+    return DA_ERR_SHAPE;
+  if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
+  if (s.B == 0) return DA_OK;
+  const Options o = options_snapshot();
+  const AttnPlan pl = plan_attention(s, o);
+  if (kHeaderBytes + pl.bytes > kNoAllocScratchBytes) return DA_ERR_SCRATCH;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* base = nullptr;
+  DA_TRY(noalloc_scratch(&base));
+  // The array keeps whatever the previous call left: the error word and this call's
+  // completion counters must start at zero (a memset allocates nothing).
+  if (cudaMemsetAsync(base, 0, kAttnCntOff + (size_t)s.B * s.Hkv * 4, st) != cudaSuccess) return DA_ERR_CUDA;
+  return run_attention(q, k_cache, v_cache, seq_lens, s, pl, base, base + kHeaderBytes,
                        static_cast<__nv_bfloat16*>(attn_out->data), attn_out->stride[0], attn_out->stride[1],
                        nullptr, 0, 0, scale, st);
 }

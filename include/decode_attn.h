@@ -72,7 +72,8 @@ typedef enum {
   DA_ERR_NOMEM = -7,       /* the workspace could not be grown */
   DA_ERR_CUDA = -8,        /* a CUDA runtime call or launch failed */
   DA_ERR_OPTION = -9,      /* unknown option key or value out of range */
-  DA_ERR_DEVICE = -10      /* a kernel recorded a device-side error (bounded wait ran out) */
+  DA_ERR_DEVICE = -10,     /* a kernel recorded a device-side error (bounded wait ran out) */
+  DA_ERR_SCRATCH = -11     /* decode_attn_only_noalloc: the call needs more than its fixed scratch */
 } da_status_t;
 
 /* Limits checked on the host. */
@@ -111,6 +112,36 @@ int decode_attn_fwd(const da_tensor_t* q, const da_tensor_t* k_cache, const da_t
 int decode_attn_only(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
                      const da_tensor_t* seq_lens, const da_tensor_t* attn_out, float scale,
                      void* stream);
+
+/*
+ * decode_attn_only_noalloc -- decode_attn_only for callers that must not allocate
+ * device memory at run time: for example a serving process whose GPU memory is
+ * reserved up front by its own allocator or memory pool, or a request path that
+ * may not take the device-wide synchronisation that growing (freeing and
+ * re-allocating) the library workspace implies. The pages have no counterpart;
+ * this is a deployment convenience, with the same arguments and the same result
+ * as decode_attn_only.
+ *
+ * Scratch: a fixed 8 MiB device array inside the library, held by every GPU that
+ * loads it until the process exits. It is never allocated or freed and no
+ * allocating routine is called. The split-KV partials need one slot per
+ * (sequence, KV head) pair plus one per persistent CTA: on a 152-SM GB300 with
+ * the default grid that allows B*Hkv up to 1738 when Hq/Hkv <= 8 and up to 793
+ * when Hq/Hkv <= 16. A larger call returns DA_ERR_SCRATCH and launches nothing.
+ *
+ * - The first call on a device looks up the array's device address (no
+ *   allocation); make that first call before any stream capture.
+ * - Every call clears the error word and its completion counters with
+ *   cudaMemsetAsync on `stream` before the kernel, because the array keeps the
+ *   previous call's contents.
+ * - All calls share the one array: calls whose work overlaps on the GPU (other
+ *   streams, other host threads) race on it and must be serialised by the caller.
+ * - Device-side wait timeouts are recorded in the array's own error word;
+ *   decode_attn_device_error() does not report them.
+ */
+int decode_attn_only_noalloc(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
+                             const da_tensor_t* seq_lens, const da_tensor_t* attn_out, float scale,
+                             void* stream);
 
 /*
  * decode_attn_scores -- the first contraction alone: the page's `scores_fp32`
