@@ -26,6 +26,7 @@ struct Options {
   int64_t gemm_min_batch = 4;  // measured crossover: GEMV ahead at B <= 2, even at 4, GEMM ahead from 8
   int64_t pdl = 1;
   int64_t l2_prefetch = 0;  // fused step: the attention kernel pulls W_o into L2 (measured slower: off)
+  int64_t attn_stages = 4;  // attention pipeline depth, 4 or 6 (6 measured slower)
 };
 std::mutex g_mu;
 Options g_opt;
@@ -237,7 +238,9 @@ struct AttnPlan {
 AttnPlan plan_attention(const AttnShape& s, const Options& o) {
   AttnPlan pl;
   const int sms = std::max(1, sm_count());
-  pl.grid = o.attn_ctas > 0 ? (int)o.attn_ctas : sms;
+  // at most kMaxAttnCtas workers: a sequence then has at most that many parts, whose merge
+  // weights fit the kernel's merge scratch
+  pl.grid = std::min(o.attn_ctas > 0 ? (int)o.attn_ctas : sms, kMaxAttnCtas);
   pl.nb = s.G <= 8 ? 1 : 2;
   pl.gpad = 8 * pl.nb;
   const size_t slots = (size_t)pl.grid + (size_t)s.B * s.Hkv;
@@ -305,7 +308,8 @@ UmmaPlan plan_umma(int B, int K, int N, const Options& o) {
   const int nkb = (K + kUmmaBK - 1) / kUmmaBK;
   const int sms = std::max(1, sm_count());
   int ks = (int)o.oproj_splitk;
-  if (ks <= 0) ks = std::max(1, 2 * sms / std::max(1, mtiles * bchunks));  // two CTAs per SM
+  // one CTA per SM measured best (two fit, but more slices cost more than they hide)
+  if (ks <= 0) ks = std::max(1, sms / std::max(1, mtiles * bchunks));
   pl.ksplit = std::max(1, std::min(ks, nkb));
   pl.bytes = pl.ksplit > 1 ? align_up((size_t)pl.ksplit * B * N * 4, 256) : 0;
   return pl;
@@ -389,6 +393,7 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
   p.Lcap = s.Lcap;
   p.gpad = pl.gpad;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.stages = (int)options_snapshot().attn_stages;
   p.prefetch = static_cast<const char*>(prefetch);
   p.prefetch_bytes = prefetch ? (prefetch_bytes & ~15ll) : 0;
   return launch_attention(p, pl.grid, pl.nb, scores != nullptr, stream) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
@@ -420,12 +425,13 @@ const char* decode_attn_status_str(int code) {
 int decode_attn_set_option(const char* key, int64_t value) {
   if (!key) return DA_ERR_OPTION;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!strcmp(key, "attn_ctas") && value >= 0 && value <= 65535) g_opt.attn_ctas = value;
+  if (!strcmp(key, "attn_ctas") && value >= 0 && value <= kMaxAttnCtas) g_opt.attn_ctas = value;
   else if (!strcmp(key, "oproj_path") && value >= 0 && value <= 2) g_opt.oproj_path = value;
   else if (!strcmp(key, "oproj_splitk") && value >= 0 && value <= 4096) g_opt.oproj_splitk = value;
   else if (!strcmp(key, "gemm_min_batch") && value >= 1) g_opt.gemm_min_batch = value;
   else if (!strcmp(key, "pdl") && (value == 0 || value == 1)) g_opt.pdl = value;
   else if (!strcmp(key, "l2_prefetch") && (value == 0 || value == 1)) g_opt.l2_prefetch = value;
+  else if (!strcmp(key, "attn_stages") && (value == 4 || value == 6)) g_opt.attn_stages = value;
   else return DA_ERR_OPTION;
   return DA_OK;
 }
@@ -439,6 +445,7 @@ int decode_attn_get_option(const char* key, int64_t* value) {
   else if (!strcmp(key, "gemm_min_batch")) *value = g_opt.gemm_min_batch;
   else if (!strcmp(key, "pdl")) *value = g_opt.pdl;
   else if (!strcmp(key, "l2_prefetch")) *value = g_opt.l2_prefetch;
+  else if (!strcmp(key, "attn_stages")) *value = g_opt.attn_stages;
   else return DA_ERR_OPTION;
   return DA_OK;
 }

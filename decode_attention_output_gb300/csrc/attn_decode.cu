@@ -16,7 +16,7 @@
 //    completion counter, no waiting) merges the partials with the log-sum-exp
 //    rule and writes bf16.
 //  * One producer warp streams K and V tiles with 4-D TMA (128-byte swizzle,
-//    two 64-dim boxes per tile) into a 4-stage shared-memory ring guarded by
+//    two 64-dim boxes per tile) into a 4- or 6-stage shared-memory ring guarded by
 //    mbarriers; q rows arrive by 1-D bulk copy with a sequence's first tiles.
 //  * Two consumer groups of four warps take alternate stages, so two tiles are
 //    in compute at once per SM. Each warp owns 16 tokens of a stage and all G
@@ -84,12 +84,13 @@ __device__ __forceinline__ uint32_t mask_tokens(uint32_t v, int tok, int valid) 
   return v & (lo | hi);
 }
 
-template <int NB, bool SCORES>
+template <int NB, bool SCORES, int S>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __grid_constant__ AttnParams p) {
   constexpr int HP = 8 * NB;  // heads per group, padded to the MMA width
   const int B = p.B, Hkv = p.Hkv, G = p.G, Lcap = p.Lcap;
-  constexpr AttnSmem kFixed(NB, 0);  // offsets that do not depend on the batch size
-  const AttnSmem lay(NB, B);
+  static_assert(S % kGroups == 0, "a stage must always be consumed by the same group");
+  constexpr AttnSmem kFixed(NB, 0, S);  // offsets that do not depend on the batch size
+  const AttnSmem lay(NB, B, S);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -105,10 +106,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   int* lens = reinterpret_cast<int*>(smem + lay.off_lens());                 // [B], clamped
   const uint32_t ring = smem_u32(smem);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
-  auto empty_bar = [&](int s) { return smem_u32(bars + kStages + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), kGroupWarps);
     }
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
     fence_barrier_init();
   }
   // Padded head rows of the q slots stay zero for the whole kernel.
-  for (int i = tid; i < (int)(kStages * kFixed.q_slot() / 16); i += kAttnThreads)
+  for (int i = tid; i < (int)(S * kFixed.q_slot() / 16); i += kAttnThreads)
     reinterpret_cast<uint4*>(q_slots)[i] = make_uint4(0, 0, 0, 0);
   if (warp == 1) {  // clamped lengths, and tiles per batch row scanned into prefix
     int carry = 0;
@@ -174,8 +175,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
           if (c.j == 0) seg0 = x;
         }
         const bool with_q = x - seg0 < kGroups;  // each group's first tile of the segment
-        const int stage = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
+        const int stage = it % S;
+        const uint32_t ph = (it / S) & 1;
         mbar_wait_bounded(empty_bar(stage), ph ^ 1, p.err, kErrWaitEmpty, flags);
         const uint32_t fb = full_bar(stage);
         uint32_t bytes = SCORES ? kKTileBytes : kStageBytes;
@@ -202,8 +203,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
         }
       }
       // Do not leave with copies in flight (only matters if the consumers gave up).
-      for (int k = it > kStages ? it - kStages : 0; k < it; ++k)
-        mbar_wait_bounded(full_bar(k % kStages), (k / kStages) & 1, p.err, kErrWaitDrain, nullptr,
+      for (int k = it > S ? it - S : 0; k < it; ++k)
+        mbar_wait_bounded(full_bar(k % S), (k / S) & 1, p.err, kErrWaitDrain, nullptr,
                           kWaitLimitNs / 10);
     }
   } else {
@@ -244,8 +245,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
       if (it % kGroups == grp) {
         const int t0 = c.j * kTile;
         const int vw = min(kTile, lens[c.b] - t0) - tb;  // valid tokens of this warp's 16
-        const int stage = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
+        const int stage = it % S;
+        const uint32_t ph = (it / S) & 1;
         mbar_wait_bounded(full_bar(stage), ph, p.err, kErrWaitFull, flags);
         if (x - seg0 < kGroups) {  // this group's first tile of the segment carries q
           const uint8_t* qs = q_slots + stage * kFixed.q_slot();
@@ -465,19 +466,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
           named_bar_sync(1, kConsumerThreads);
           if (flags[1]) {  // every other part has landed: merge them all
             __threadfence();
-            for (int h = tid >> 7; h < G; h += 2) {
+            // (a) one warp per head: the parts' (m, l) come in together (a lane per part),
+            //     and the normalised weights exp2(m_p - M) / sum go to shared memory
+            float* wpart = merge_o;  // free again: [G][n_parts]
+            for (int h = warp; h < G; h += kGroups * kGroupWarps) {
               float M = kNegInf;
-              for (int pc = first_cta; pc <= last_cta; ++pc)
-                M = fmaxf(M, __ldcg(p.part_ml + (((long long)pc + seq) * p.gpad + h) * 2));
-              float lsum = 0.f, acc = 0.f;
-              for (int pc = first_cta; pc <= last_cta; ++pc) {
-                const long long slot = (long long)pc + seq;
-                const float f = fast_exp2(__ldcg(p.part_ml + (slot * p.gpad + h) * 2) - M);
-                lsum += f * __ldcg(p.part_ml + (slot * p.gpad + h) * 2 + 1);
-                acc += f * __ldcg(p.part_o + (slot * p.gpad + h) * kHeadDim + d);
+              for (int pc = lane; pc < n_parts; pc += 32)
+                M = fmaxf(M, __ldcg(p.part_ml + (((long long)first_cta + pc + seq) * p.gpad + h) * 2));
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+              float lsum = 0.f;
+              for (int pc = lane; pc < n_parts; pc += 32) {
+                const float* ml2 = p.part_ml + (((long long)first_cta + pc + seq) * p.gpad + h) * 2;
+                const float f = fast_exp2(__ldcg(ml2) - M);
+                wpart[h * n_parts + pc] = f;
+                lsum += f * __ldcg(ml2 + 1);
               }
-              p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] =
-                  __float2bfloat16_rn(acc / lsum);
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+              __syncwarp();
+              for (int pc = lane; pc < n_parts; pc += 32) wpart[h * n_parts + pc] /= lsum;
+            }
+            named_bar_sync(1, kConsumerThreads);
+            // (b) O[h][d] = sum_p w_p O_p[h][d]: the loads of eight parts go out together
+            for (int h = tid >> 7; h < G; h += 2) {
+              float acc = 0.f;
+              for (int p0 = 0; p0 < n_parts; p0 += 8) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  const int pc = p0 + u;
+                  if (pc < n_parts)
+                    acc += wpart[h * n_parts + pc] *
+                           __ldcg(p.part_o + (((long long)first_cta + pc + seq) * p.gpad + h) * kHeadDim + d);
+                }
+              }
+              p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc);
             }
             if (tid == 0) p.counters[seq] = 0;  // ready for the next call
           }
@@ -498,30 +521,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   __syncthreads();
 }
 
-template <int NB, bool SCORES>
+template <int NB, bool SCORES, int S>
 cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   // The shared-memory opt-in is a per-device function attribute: set it once per
-  // device, sized for the largest batch the library accepts.
+  // device, sized for the largest batch this instance serves.
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attn_decode_kernel<NB, SCORES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)attn_smem_bytes(kMaxBatch, NB));
+    e = cudaFuncSetAttribute(attn_decode_kernel<NB, SCORES, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kMaxDynSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  attn_decode_kernel<NB, SCORES><<<grid, kAttnThreads, attn_smem_bytes(p.B, NB), stream>>>(p);
+  attn_decode_kernel<NB, SCORES, S><<<grid, kAttnThreads, attn_smem_bytes(p.B, NB, S), stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int NB, bool SCORES>
+cudaError_t launch_nb(const AttnParams& p, int grid, cudaStream_t stream) {
+  if (attn_stages_for(p.B, NB, p.stages) == kMaxStages) return launch_one<NB, SCORES, kMaxStages>(p, grid, stream);
+  return launch_one<NB, SCORES, 4>(p, grid, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_attention(const AttnParams& p, int grid, int nb, bool scores_only, cudaStream_t stream) {
-  if (nb == 1) return scores_only ? launch_one<1, true>(p, grid, stream) : launch_one<1, false>(p, grid, stream);
-  return scores_only ? launch_one<2, true>(p, grid, stream) : launch_one<2, false>(p, grid, stream);
+  if (nb == 1) return scores_only ? launch_nb<1, true>(p, grid, stream) : launch_nb<1, false>(p, grid, stream);
+  return scores_only ? launch_nb<2, true>(p, grid, stream) : launch_nb<2, false>(p, grid, stream);
 }
 
 }  // namespace da

@@ -17,7 +17,7 @@ constexpr int kGroupWarps = 4;                 // consumer warps per group; each
 constexpr int kGroups = 2;                     // consumer groups take alternate stages
 constexpr int kConsumerThreads = kGroups * kGroupWarps * 32;
 constexpr int kAttnThreads = kConsumerThreads + 32;  // + one TMA producer warp
-constexpr int kStages = 4;                     // even: stage s always belongs to group s % 2
+constexpr int kMaxStages = 6;                  // even stage counts: stage s always belongs to group s % 2
 constexpr int kHalfBytes = kTile * 128;        // 64 tokens x 64 dims x bf16 (one 128B-swizzled box)
 constexpr int kKTileBytes = 2 * kHalfBytes;    // 64 tokens x 128 dims
 constexpr int kStageBytes = 2 * kKTileBytes;   // K tile + V tile
@@ -25,28 +25,36 @@ constexpr int kQRowBytes = 272;                // 256 B of q + 16 B pad (conflic
 constexpr int kMaxGroup = 16;
 constexpr int kMaxBatch = 1024;
 constexpr int kMergeRow = 132;                 // floats per head row of the merge scratch (128 + pad)
-static_assert(kStages % kGroups == 0, "a stage must always be consumed by the same group");
-
-// Shared-memory carve-up of the attention kernel; nb = 8-head blocks (1 or 2).
+constexpr int kMaxAttnCtas = 512;              // parts per sequence stay <= this: the cross-CTA merge
+                                               // keeps G x parts weights in the 4*8*nb*kMergeRow scratch
+static_assert(kMaxAttnCtas <= kGroupWarps * kMergeRow, "merge weights must fit the merge scratch");
+// Shared-memory carve-up of the attention kernel; nb = 8-head blocks (1 or 2),
+// stages = pipeline depth (even, so that a stage always belongs to one consumer group).
 struct AttnSmem {
-  int nb, batch;
-  __host__ __device__ constexpr AttnSmem(int nb_, int batch_) : nb(nb_), batch(batch_) {}
+  int nb, batch, stages;
+  __host__ __device__ constexpr AttnSmem(int nb_, int batch_, int stages_) : nb(nb_), batch(batch_), stages(stages_) {}
   __host__ __device__ constexpr int heads() const { return 8 * nb; }
   __host__ __device__ constexpr size_t q_slot() const { return (size_t)heads() * kQRowBytes; }
-  __host__ __device__ constexpr size_t off_q() const { return (size_t)kStages * kStageBytes; }
-  __host__ __device__ constexpr size_t off_merge_o() const { return off_q() + kStages * q_slot(); }
+  __host__ __device__ constexpr size_t off_q() const { return (size_t)stages * kStageBytes; }
+  __host__ __device__ constexpr size_t off_merge_o() const { return off_q() + stages * q_slot(); }
   __host__ __device__ constexpr size_t off_merge_ml() const {
     return off_merge_o() + (size_t)kGroupWarps * heads() * kMergeRow * 4;
   }
   __host__ __device__ constexpr size_t off_bars() const { return off_merge_ml() + (size_t)kGroupWarps * heads() * 2 * 4; }
-  __host__ __device__ constexpr size_t off_flags() const { return off_bars() + 2 * kStages * 8; }
+  __host__ __device__ constexpr size_t off_flags() const { return off_bars() + 2 * stages * 8; }
   __host__ __device__ constexpr size_t off_prefix() const { return off_flags() + 16; }
   __host__ __device__ constexpr size_t off_lens() const { return off_prefix() + (size_t)(batch + 1) * 4; }
   __host__ __device__ constexpr size_t total() const { return 1024 + off_lens() + (size_t)batch * 4; }
 };
 
-constexpr size_t attn_smem_bytes(int batch, int nb) { return AttnSmem(nb, batch).total(); }
-static_assert(AttnSmem(2, kMaxBatch).total() <= 232448, "attention kernel exceeds 227 KB of shared memory");
+constexpr size_t kMaxDynSmem = 232448;  // 227 KB per CTA on sm_100-class GPUs
+constexpr size_t attn_smem_bytes(int batch, int nb, int stages) { return AttnSmem(nb, batch, stages).total(); }
+static_assert(AttnSmem(2, kMaxBatch, 4).total() <= kMaxDynSmem, "attention kernel exceeds 227 KB of shared memory");
+// 4 stages by default (measured faster than 6 on the GB300: deeper rings slowed the
+// stream); 6 on request when it fits this batch and group width.
+constexpr int attn_stages_for(int batch, int nb, int requested) {
+  return requested == kMaxStages && attn_smem_bytes(batch, nb, kMaxStages) <= kMaxDynSmem ? kMaxStages : 4;
+}
 
 struct AttnParams {
   CUtensorMap tm_k;  // [B][Hkv][Lcap][128] bf16, box 64 dims x 64 tokens, 128B swizzle
@@ -69,6 +77,7 @@ struct AttnParams {
   // in pieces while the K/V stream runs. prefetch_bytes = 0 disables it.
   const char* prefetch;
   long long prefetch_bytes;
+  int stages;            // requested pipeline depth (4 or 6)
 };
 
 // grid = number of persistent CTAs; nb = 1 for G <= 8, 2 for G <= 16.

@@ -165,7 +165,7 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
 
 /*
  * Tuning options (process-wide; 0 = automatic). Keys:
- *   "attn_ctas"     CTAs of the persistent attention kernel (0: one per SM)
+ *   "attn_ctas"     CTAs of the persistent attention kernel (0: one per SM; at most 512)
  *   "oproj_path"    0 auto, 1 CUDA-core GEMV, 2 tcgen05 tensor-core GEMM
  *   "oproj_splitk"  split-K factor of the projection (0: auto)
  *   "gemm_min_batch" smallest batch that takes the tensor-core GEMM in auto mode
@@ -176,6 +176,8 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *                   pulls o_weight into L2 while it streams K/V, so that the
  *                   projection reads o_weight from L2 (measured slower on GB300:
  *                   the prefetch competes with the K/V stream)
+ *   "attn_stages"   4 (default) or 6: depth of the attention kernel's K/V ring
+ *                   (6 only when it fits in shared memory for the batch)
  * Returns DA_OK or DA_ERR_OPTION.
  */
 int decode_attn_set_option(const char* key, int64_t value);
