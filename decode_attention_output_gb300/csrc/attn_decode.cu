@@ -460,12 +460,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
           }
         }
         if (n_parts > 1) {
-          __threadfence();
-          named_bar_sync(1, kConsumerThreads);
-          if (tid == 0) flags[1] = (atomicAdd(p.counters + seq, 1) == n_parts - 1);
-          named_bar_sync(1, kConsumerThreads);
+          named_bar_sync(1, kConsumerThreads);  // every thread's partial stores precede the release
+          if (tid == 0) flags[1] = (atomic_add_acq_rel_gpu(p.counters + seq, 1) == n_parts - 1);
+          named_bar_sync(1, kConsumerThreads);  // ... and the acquire precedes every thread's loads
           if (flags[1]) {  // every other part has landed: merge them all
-            __threadfence();
             // (a) one warp per head: the parts' (m, l) come in together (a lane per part),
             //     and the normalised weights exp2(m_p - M) / sum go to shared memory
             float* wpart = merge_o;  // free again: [G][n_parts]

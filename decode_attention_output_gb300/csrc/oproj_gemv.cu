@@ -107,13 +107,11 @@ __global__ void __launch_bounds__(kGemvThreads, 2) oproj_gemv_kernel(const __gri
   }
   if (p.ksplit == 1) return;
 
-  __threadfence();
-  __syncthreads();
+  __syncthreads();  // every thread's partial stores precede the release below
   int* counter = p.counters + blockIdx.z * gridDim.x + cb;
-  if (tid == 0) *flag = (atomicAdd(counter, 1) == p.ksplit - 1);
+  if (tid == 0) *flag = (atomic_add_acq_rel_gpu(counter, 1) == p.ksplit - 1);
   __syncthreads();
   if (*flag) {  // last k-slice of this column block: sum all slices in order
-    __threadfence();
     const int c = col0 + tid;
     const bool c_ok = c < p.N;
     float sum[BT];

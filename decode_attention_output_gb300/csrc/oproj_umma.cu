@@ -150,13 +150,11 @@ __global__ void __launch_bounds__(kUmmaThreads, 2) oproj_umma_kernel(const __gri
 #pragma unroll
     for (int b = 0; b < NPAD; ++b)
       if (n_ok && b0 + b < p.B) p.part[((long long)ks * p.B + b0 + b) * p.N + n] = acc[b];
-    __threadfence();
-    __syncthreads();
+    __syncthreads();  // every thread's partial stores precede the release below
     int* counter = p.counters + blockIdx.z * gridDim.x + mt;
-    if (tid == 0) *flag = (atomicAdd(counter, 1) == p.ksplit - 1);
+    if (tid == 0) *flag = (atomic_add_acq_rel_gpu(counter, 1) == p.ksplit - 1);
     __syncthreads();
     if (*flag) {  // last k-slice of this column tile: sum all slices in order
-      __threadfence();
       const int nb_valid = p.B - b0 < NPAD ? p.B - b0 : NPAD;
 #pragma unroll
       for (int b = 0; b < NPAD; ++b) acc[b] = 0.f;

@@ -211,6 +211,16 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
 
 // Named barrier over `nthreads` threads; the non-.aligned form, so threads of a
 // warp may arrive after divergent code.
+// GPU-scope acquire-release add. After a CTA barrier, one thread's release covers the
+// stores every thread of the CTA made before the barrier (release is cumulative), and
+// its acquire, followed by a barrier, makes other CTAs' released stores visible to the
+// whole CTA. Used by the "last CTA merges" completion counters.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* addr, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
