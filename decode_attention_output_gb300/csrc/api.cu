@@ -27,6 +27,7 @@ struct Options {
   int64_t pdl = 1;
   int64_t l2_prefetch = 0;  // fused step: the attention kernel pulls W_o into L2 (measured slower: off)
   int64_t attn_stages = 4;  // attention pipeline depth, 4 or 6 (6 measured slower)
+  int64_t fused = 0;        // decode_attn_fwd as one persistent launch (measured slower so far: off)
 };
 std::mutex g_mu;
 Options g_opt;
@@ -44,6 +45,7 @@ Options options_snapshot() {
 // followed by per-call scratch laid out by the caller.
 constexpr size_t kMaxCounters = 65536;
 constexpr size_t kErrOff = 0;
+constexpr size_t kGridSyncOff = 64;  // two ints of the fused step's grid barrier
 constexpr size_t kAttnCntOff = 256;
 constexpr size_t kGemvCntOff = kAttnCntOff + kMaxCounters * 4;
 constexpr size_t kHeaderBytes = kGemvCntOff + kMaxCounters * 4;
@@ -364,12 +366,57 @@ int run_projection(const __nv_bfloat16* x, long long x_sb, const da_tensor_t* w,
   return run_gemv(x, x_sb, w, out, B, K, N, ws, scratch, pl.gv, pdl, stream);
 }
 
+// The fused step: attention, grid barrier and tcgen05 projection in one cooperative launch.
+struct FusedPlan {
+  bool ok = false;
+  int npad = 0, kb_per_tile = 0, mtiles = 0, units = 0;
+  size_t part_bytes = 0;
+};
+
+FusedPlan plan_fused(const AttnShape& s, int K, int N, const AttnPlan& ap, const Options& o) {
+  FusedPlan f;
+  if (!o.fused || o.oproj_path == 1 || s.B > 128 || K % 64) return f;
+  f.npad = s.B <= 16 ? 16 : (s.B <= 32 ? 32 : (s.B <= 64 ? 64 : 128));
+  f.kb_per_tile = K / 64;
+  f.mtiles = (N + 127) / 128;
+  f.units = f.mtiles * f.kb_per_tile;
+  const int pb = std::min(ap.grid, f.units);
+  // a CTA must cover at most two column tiles (two TMEM accumulator regions)
+  if ((f.units + pb - 1) / pb > f.kb_per_tile + 1) return f;
+  if (f.mtiles > (int)kMaxCounters) return f;
+  f.part_bytes = align_up((size_t)(pb + f.mtiles) * s.B * 128 * 4, 256);
+  f.ok = true;
+  return f;
+}
+
+struct FusedArgs {
+  const FusedPlan* plan;
+  const da_tensor_t* w;
+  const da_tensor_t* out;
+  float* part;
+  int K, N;
+};
+
 int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t* v, const da_tensor_t* lens,
                   const AttnShape& s, const AttnPlan& pl, char* ws, char* scratch, __nv_bfloat16* attn,
                   long long a_sb, long long a_sh, float* scores, long long s_sb, long long s_sh, float scale,
-                  cudaStream_t stream, const void* prefetch = nullptr, long long prefetch_bytes = 0) {
+                  cudaStream_t stream, const void* prefetch = nullptr, long long prefetch_bytes = 0,
+                  const FusedArgs* fused = nullptr) {
   AttnParams p;
   memset(&p, 0, sizeof(p));
+  if (fused) {
+    DA_TRY(encode_2d_map(&p.tm_w, fused->w->data, fused->K, fused->N, fused->w->stride[0], 64));
+    DA_TRY(encode_2d_map(&p.tm_x, attn, s.B, fused->K, a_sb, fused->plan->npad));
+    p.y = static_cast<__nv_bfloat16*>(fused->out->data);
+    p.y_sb = fused->out->stride[0];
+    p.proj_part = fused->part;
+    p.proj_counters = reinterpret_cast<int*>(ws + kGemvCntOff);
+    p.grid_sync = reinterpret_cast<int*>(ws + kGridSyncOff);
+    p.N = fused->N;
+    p.K = fused->K;
+    p.kb_per_tile = fused->plan->kb_per_tile;
+    p.units = fused->plan->units;
+  }
   DA_TRY(encode_kv_map(&p.tm_k, k));
   if (v) DA_TRY(encode_kv_map(&p.tm_v, v));
   else p.tm_v = p.tm_k;
@@ -396,7 +443,12 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
   p.stages = (int)options_snapshot().attn_stages;
   p.prefetch = static_cast<const char*>(prefetch);
   p.prefetch_bytes = prefetch ? (prefetch_bytes & ~15ll) : 0;
-  return launch_attention(p, pl.grid, pl.nb, scores != nullptr, stream) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+  const cudaError_t e = launch_attention(p, pl.grid, pl.nb, scores != nullptr, stream, fused ? fused->plan->npad : 0);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    cudaGetLastError();
+    return DA_ERR_UNSUPPORTED;  // the caller falls back to two launches
+  }
+  return e == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
 }  // namespace
@@ -432,6 +484,7 @@ int decode_attn_set_option(const char* key, int64_t value) {
   else if (!strcmp(key, "pdl") && (value == 0 || value == 1)) g_opt.pdl = value;
   else if (!strcmp(key, "l2_prefetch") && (value == 0 || value == 1)) g_opt.l2_prefetch = value;
   else if (!strcmp(key, "attn_stages") && (value == 4 || value == 6)) g_opt.attn_stages = value;
+  else if (!strcmp(key, "fused") && (value == 0 || value == 1)) g_opt.fused = value;
   else return DA_ERR_OPTION;
   return DA_OK;
 }
@@ -446,6 +499,7 @@ int decode_attn_get_option(const char* key, int64_t* value) {
   else if (!strcmp(key, "pdl")) *value = g_opt.pdl;
   else if (!strcmp(key, "l2_prefetch")) *value = g_opt.l2_prefetch;
   else if (!strcmp(key, "attn_stages")) *value = g_opt.attn_stages;
+  else if (!strcmp(key, "fused")) *value = g_opt.fused;
   else return DA_ERR_OPTION;
   return DA_OK;
 }
@@ -579,9 +633,21 @@ int decode_attn_fwd(const da_tensor_t* q, const da_tensor_t* k_cache, const da_t
   if (s.B == 0) return DA_OK;
   const Options o = options_snapshot();
   const AttnPlan ap = plan_attention(s, o);
-  const ProjPlan gp = plan_projection(s.B, (int)K, (int)N, o);
   const size_t attn_bytes = align_up((size_t)s.B * K * 2, 256);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const FusedPlan fp = plan_fused(s, (int)K, (int)N, ap, o);
+  if (fp.ok) {  // one launch: attention, grid barrier, projection
+    char* ws = nullptr;
+    DA_TRY(workspace_get(ap.bytes + attn_bytes + fp.part_bytes, st, &ws));
+    char* scratch = ws + kHeaderBytes;
+    __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(scratch + ap.bytes);
+    const FusedArgs fa{&fp, o_weight, out, reinterpret_cast<float*>(scratch + ap.bytes + attn_bytes), (int)K, (int)N};
+    const long long w_span = ((long long)(K - 1) * o_weight->stride[0] + N) * 2;
+    const int rc = run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, kHeadDim, nullptr, 0, 0,
+                                 scale, st, o.l2_prefetch ? o_weight->data : nullptr, w_span, &fa);
+    if (rc != DA_ERR_UNSUPPORTED) return rc;  // else: not co-resident here, take two launches
+  }
+  const ProjPlan gp = plan_projection(s.B, (int)K, (int)N, o);
   char* ws = nullptr;
   DA_TRY(workspace_get(ap.bytes + attn_bytes + gp.bytes, st, &ws));
   char* scratch = ws + kHeaderBytes;

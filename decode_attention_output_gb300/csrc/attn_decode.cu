@@ -84,8 +84,194 @@ __device__ __forceinline__ uint32_t mask_tokens(uint32_t v, int tok, int valid) 
   return v & (lo | hi);
 }
 
-template <int NB, bool SCORES, int S>
+// ---------------------------------------------------------------- fused step
+// Phase B of the fused step projects the attention output X [B][K] with W_o [K][N]
+// on tcgen05: y^T[n][b] = W_o^T[n][k] . X^T[k][b] (swap-AB: M = 128 hidden columns,
+// N = batch padded to NPAD). Work unit = one column tile (128 columns) x one 64-row
+// k-block of W_o; the units are laid end to end (column tile major) and each CTA
+// takes an equal contiguous range, so a CTA covers at most two column tiles (the
+// host checks it) and accumulates each in its own TMEM region.
+struct ProjSplit {
+  int PB;             // CTAs with phase-B work
+  long long u0, u1;   // this CTA's units
+};
+
+__device__ __forceinline__ ProjSplit proj_split(const AttnParams& p, int cta) {
+  ProjSplit r;
+  r.PB = min((int)gridDim.x, p.units);
+  r.u0 = cta < r.PB ? (long long)cta * p.units / r.PB : 0;
+  r.u1 = cta < r.PB ? (long long)(cta + 1) * p.units / r.PB : 0;
+  return r;
+}
+
+// Waits until every CTA of the grid has arrived (bounded), then counts this CTA's
+// departure; the last one to leave resets both counters for the next launch.
+__device__ __forceinline__ bool grid_barrier_wait(int* sync, int n, int* err, volatile int* abort_flag) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (ld_acquire_gpu(sync) < n) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, kErrGridSync);
+      *abort_flag = 1;
+      return false;
+    }
+    __nanosleep(64);
+  }
+  if (atomic_add_acq_rel_gpu(sync + 1, 1) == n - 1) {
+    sync[0] = 0;
+    sync[1] = 0;
+  }
+  return true;
+}
+
+// Phase-B producer: refills the (now free) K/V ring with W_o tiles right away, and
+// with X tiles once the grid barrier says every attention output is written.
+template <int NPAD, int S>
+__device__ void fused_producer(const AttnParams& p, uint32_t ring, uint64_t* bars, int it_a, int* flags) {
+  constexpr uint32_t kXBytes = NPAD * 128;  // NPAD rows x 64 k x bf16
+  constexpr int SB = proj_stages(NPAD), kStageB = proj_stage_bytes(NPAD);
+  auto empty_a = [&](int s) { return smem_u32(bars + S + s); };
+  auto full_b = [&](int s) { return smem_u32(bars + 2 * S + s); };
+  auto empty_b = [&](int s) { return smem_u32(bars + 2 * S + 8 + s); };
+  // the last phase-A fill of every stage must have been consumed
+  for (int k = it_a > S ? it_a - S : 0; k < it_a; ++k)
+    mbar_wait_bounded(empty_a(k % S), (k / S) & 1, p.err, kErrWaitEmpty, flags);
+  const ProjSplit ps = proj_split(p, blockIdx.x);
+  const int nu = (int)(ps.u1 - ps.u0);
+  const int pre = nu < SB ? nu : SB;
+  prefetch_tensormap(&p.tm_w);
+  prefetch_tensormap(&p.tm_x);
+  for (int j = 0; j < pre; ++j) {
+    const int unit = (int)ps.u0 + j, tile = unit / p.kb_per_tile, kb = unit - tile * p.kb_per_tile;
+    const uint32_t dst = ring + j * kStageB;
+    mbar_arrive_expect_tx(full_b(j), kProjWBytes + kXBytes);
+    tma_load_2d(dst, &p.tm_w, full_b(j), tile * 128, kb * 64);
+    tma_load_2d(dst + 8192, &p.tm_w, full_b(j), tile * 128 + 64, kb * 64);
+  }
+  grid_barrier_wait(p.grid_sync, gridDim.x, p.err, flags);
+  fence_proxy_async_global();  // X was written by other CTAs' generic stores; TMA reads it
+  for (int j = 0; j < pre; ++j) {
+    const int unit = (int)ps.u0 + j, tile = unit / p.kb_per_tile, kb = unit - tile * p.kb_per_tile;
+    tma_load_2d(ring + j * kStageB + kProjWBytes, &p.tm_x, full_b(j), kb * 64, 0);
+  }
+  for (int j = pre; j < nu; ++j) {
+    const int s = j % SB;
+    const uint32_t ph = (j / SB) & 1;
+    mbar_wait_bounded(empty_b(s), ph ^ 1, p.err, kErrWaitEmpty, flags);
+    const int unit = (int)ps.u0 + j, tile = unit / p.kb_per_tile, kb = unit - tile * p.kb_per_tile;
+    const uint32_t dst = ring + s * kStageB;
+    mbar_arrive_expect_tx(full_b(s), kProjWBytes + kXBytes);
+    tma_load_2d(dst, &p.tm_w, full_b(s), tile * 128, kb * 64);
+    tma_load_2d(dst + 8192, &p.tm_w, full_b(s), tile * 128 + 64, kb * 64);
+    tma_load_2d(dst + kProjWBytes, &p.tm_x, full_b(s), kb * 64, 0);
+  }
+  for (int k = nu > SB ? nu - SB : 0; k < nu; ++k)  // no copies in flight at exit
+    mbar_wait_bounded(full_b(k % SB), (k / SB) & 1, p.err, kErrWaitDrain, nullptr, kWaitLimitNs / 10);
+}
+
+// Phase-B MMA issuer (one thread): four tcgen05.mma per unit into the TMEM region of
+// its column tile; each stage is released by tcgen05.commit, each region's
+// accumulator is announced when the tile's last unit of this CTA is issued.
+template <int NPAD, int S>
+__device__ void fused_mma(const AttnParams& p, uint32_t ring, uint64_t* bars, uint32_t tmem, int* flags) {
+  constexpr uint32_t kIdesc = umma_idesc_bf16(128, NPAD, /*A MN-major*/ true, /*B K-major*/ false);
+  constexpr int SB = proj_stages(NPAD), kStageB = proj_stage_bytes(NPAD);
+  auto full_b = [&](int s) { return smem_u32(bars + 2 * S + s); };
+  auto empty_b = [&](int s) { return smem_u32(bars + 2 * S + 8 + s); };
+  const ProjSplit ps = proj_split(p, blockIdx.x);
+  const int nu = (int)(ps.u1 - ps.u0);
+  const int tile0 = nu > 0 ? (int)(ps.u0 / p.kb_per_tile) : 0;
+  for (int j = 0; j < nu; ++j) {
+    const int s = j % SB;
+    mbar_wait_bounded(full_b(s), (j / SB) & 1, p.err, kErrWaitFull, flags);
+    tc_fence_after_sync();
+    const int unit = (int)ps.u0 + j, tile = unit / p.kb_per_tile, kb = unit - tile * p.kb_per_tile;
+    const int region = tile - tile0;
+    const uint32_t a = ring + s * kStageB, bsm = a + kProjWBytes;
+    const bool first = (j == 0) || (kb == 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t adesc = umma_smem_desc(a + kk * 16 * 128, 64 * 128, 1024);
+      const uint64_t bdesc = umma_smem_desc(bsm + kk * 32, 16, 1024);
+      umma_bf16(tmem + region * NPAD, adesc, bdesc, kIdesc, !(first && kk == 0));
+    }
+    umma_commit(empty_b(s));
+    if (j == nu - 1 || kb == p.kb_per_tile - 1) umma_commit(smem_u32(bars + 2 * S + 16 + region));
+  }
+}
+
+// CTA of phase B holding unit u.
+__device__ __forceinline__ int proj_cta_of(long long u, int units, int PB) {
+  return (int)(((u + 1) * (long long)PB - 1) / units);
+}
+
+// Phase-B epilogue (warps 0-3, TMEM lanes 0-127 = the tile's 128 columns): bf16 out
+// when one CTA covered the whole column tile, else fp32 partials that the last
+// CTA of the tile sums in a fixed order (atomic counter, no waiting).
+template <int NPAD, int S>
+__device__ void fused_epilogue(const AttnParams& p, uint64_t* bars, uint32_t tmem, int* flags, int warp, int lane,
+                               int tid) {
+  const ProjSplit ps = proj_split(p, blockIdx.x);
+  if (ps.u1 <= ps.u0) return;
+  const int kb = p.kb_per_tile;
+  const int tile0 = (int)(ps.u0 / kb), tile1 = (int)((ps.u1 - 1) / kb);
+  for (int tile = tile0; tile <= tile1; ++tile) {
+    const int region = tile - tile0;
+    mbar_wait_bounded(smem_u32(bars + 2 * S + 16 + region), 0, p.err, kErrWaitMma, flags);
+    tc_fence_after_sync();
+    float acc[NPAD];
+#pragma unroll
+    for (int c = 0; c < NPAD / 16; ++c) {
+      uint32_t r[16];
+      tmem_ld_32x32b_x16(tmem + ((uint32_t)(warp * 32) << 16) + region * NPAD + c * 16, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[c * 16 + i] = __uint_as_float(r[i]);
+    }
+    const int m = warp * 32 + lane, n = tile * 128 + m;
+    const bool n_ok = n < p.N;
+    const int first = proj_cta_of((long long)tile * kb, p.units, ps.PB);
+    const int last = proj_cta_of((long long)tile * kb + kb - 1, p.units, ps.PB);
+    const int np = last - first + 1;
+    if (np == 1) {
+#pragma unroll
+      for (int b = 0; b < NPAD; ++b)
+        if (n_ok && b < p.B) p.y[(long long)b * p.y_sb + n] = __float2bfloat16_rn(acc[b]);
+      continue;
+    }
+    const long long slot = (long long)blockIdx.x + tile;
+#pragma unroll
+    for (int b = 0; b < NPAD; ++b)
+      if (b < p.B) p.proj_part[(slot * p.B + b) * 128 + m] = acc[b];
+    named_bar_sync(2, 128);  // every epilogue thread's partial stores precede the release
+    if (tid == 0) flags[2] = (atomic_add_acq_rel_gpu(p.proj_counters + tile, 1) == np - 1);
+    named_bar_sync(2, 128);
+    if (flags[2]) {  // the last part of this column tile: sum all parts in order
+#pragma unroll
+      for (int b = 0; b < NPAD; ++b) acc[b] = 0.f;
+      constexpr int kParts = NPAD >= 64 ? 1 : 64 / NPAD;  // about 64 loads in flight per thread
+      for (int p0 = 0; p0 < np; p0 += kParts) {
+#pragma unroll
+        for (int u = 0; u < kParts; ++u) {
+          const int pc = p0 + u;
+#pragma unroll
+          for (int b = 0; b < NPAD; ++b)
+            if (pc < np && b < p.B)
+              acc[b] += __ldcg(p.proj_part + (((long long)first + pc + tile) * p.B + b) * 128 + m);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < NPAD; ++b)
+        if (n_ok && b < p.B) p.y[(long long)b * p.y_sb + n] = __float2bfloat16_rn(acc[b]);
+      if (tid == 0) p.proj_counters[tile] = 0;  // ready for the next call
+    }
+    named_bar_sync(2, 128);  // flags[2] is reused by the next tile
+  }
+}
+
+template <int NB, bool SCORES, int S, int NPAD>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __grid_constant__ AttnParams p) {
+  constexpr bool kFused = NPAD > 0;
+  constexpr int kTmemCols = NPAD <= 16 ? 32 : 2 * NPAD;  // two accumulator regions
   constexpr int HP = 8 * NB;  // heads per group, padded to the MMA width
   const int B = p.B, Hkv = p.Hkv, G = p.G, Lcap = p.Lcap;
   static_assert(S % kGroups == 0, "a stage must always be consumed by the same group");
@@ -113,9 +299,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), kGroupWarps);
     }
+    if (kFused) {
+      for (int s = 0; s < 8; ++s) {
+        mbar_init(smem_u32(bars + 2 * S + s), 1);      // phase-B full: the producer's expect-tx
+        mbar_init(smem_u32(bars + 2 * S + 8 + s), 1);  // phase-B empty: one tcgen05.commit
+      }
+      mbar_init(smem_u32(bars + 2 * S + 16), 1);  // accumulator of the first column tile
+      mbar_init(smem_u32(bars + 2 * S + 17), 1);  // ... and of the second
+    }
     flags[0] = 0;
     flags[1] = 0;
+    flags[2] = 0;
     fence_barrier_init();
+  }
+  if (kFused && warp == 0) {  // TMEM for the projection accumulators (one CTA per SM)
+    tmem_alloc(smem_u32(flags + 3), kTmemCols);
+    tmem_relinquish();
   }
   // Padded head rows of the q slots stay zero for the whole kernel.
   for (int i = tid; i < (int)(S * kFixed.q_slot() / 16); i += kAttnThreads)
@@ -140,7 +339,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
     }
     if (lane == 0) prefix[0] = 0;
   }
+  if (kFused) tc_fence_before_sync();
   __syncthreads();
+  if (kFused) tc_fence_after_sync();
+  const uint32_t tmem = kFused ? (uint32_t)flags[3] : 0u;
   // The projection kernel (launched with programmatic dependent launch) may now be
   // scheduled; it waits for this grid's completion before it reads our output.
   pdl_launch_dependents();
@@ -155,7 +357,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
 
   if (warp == kGroups * kGroupWarps) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && start < end) {
+    if (lane == 0) {
+     int it = 0;
+     if (start < end) {
       prefetch_tensormap(&p.tm_k);
       if (!SCORES) prefetch_tensormap(&p.tm_v);
       const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read exactly once
@@ -168,7 +372,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
       long long pf_next = pf_begin;
       Cursor c = cursor_at(start, prefix, B, Hkv);
       long long seg0 = start;
-      int it = 0;
       for (long long x = start; x < end; ++x, ++it) {
         if (x != start) {
           cursor_next(c, prefix, B, Hkv);
@@ -206,6 +409,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
       for (int k = it > S ? it - S : 0; k < it; ++k)
         mbar_wait_bounded(full_bar(k % S), (k / S) & 1, p.err, kErrWaitDrain, nullptr,
                           kWaitLimitNs / 10);
+     }
+     if constexpr (kFused) fused_producer<NPAD, S>(p, ring, bars, it, flags);
     }
   } else {
     // ------------------------------------------------------------ consumers
@@ -514,39 +719,76 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
         }
       }
     }
+    if constexpr (kFused) {
+      // This CTA's attention outputs (its own segments and every merge it performed)
+      // are written: arrive at the grid barrier (release covers all consumer stores).
+      named_bar_sync(1, kConsumerThreads);
+      if (tid == 0) atomic_add_acq_rel_gpu(p.grid_sync, 1);
+      if (warp == kGroupWarps) {  // first warp of group 1 issues the MMAs
+        if (lane == 0) fused_mma<NPAD, S>(p, ring, bars, tmem, flags);
+        __syncwarp();
+      } else if (warp < kGroupWarps) {  // group 0 drains TMEM
+        fused_epilogue<NPAD, S>(p, bars, tmem, flags, warp, lane, tid);
+        tc_fence_before_sync();
+      }
+    }
   }
   __syncwarp();
   __syncthreads();
+  if (kFused && warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
-template <int NB, bool SCORES, int S>
+template <int NB, bool SCORES, int S, int NPAD>
 cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
-  // The shared-memory opt-in is a per-device function attribute: set it once per
-  // device, sized for the largest batch this instance serves.
+  // The shared-memory opt-in is a per-device function attribute: set it once per device.
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attn_decode_kernel<NB, SCORES, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_decode_kernel<NB, SCORES, S, NPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kMaxDynSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  attn_decode_kernel<NB, SCORES, S><<<grid, kAttnThreads, attn_smem_bytes(p.B, NB, S), stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = attn_smem_bytes(p.B, NB, S);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // the fused step's grid barrier needs every CTA resident
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = NPAD > 0 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<NB, SCORES, S, NPAD>, p);
 }
 
 template <int NB, bool SCORES>
 cudaError_t launch_nb(const AttnParams& p, int grid, cudaStream_t stream) {
-  if (attn_stages_for(p.B, NB, p.stages) == kMaxStages) return launch_one<NB, SCORES, kMaxStages>(p, grid, stream);
-  return launch_one<NB, SCORES, 4>(p, grid, stream);
+  if (attn_stages_for(p.B, NB, p.stages) == kMaxStages) return launch_one<NB, SCORES, kMaxStages, 0>(p, grid, stream);
+  return launch_one<NB, SCORES, 4, 0>(p, grid, stream);
+}
+
+template <int NB>
+cudaError_t launch_fused(const AttnParams& p, int grid, int npad, cudaStream_t stream) {
+  switch (npad) {
+    case 16: return launch_one<NB, false, 4, 16>(p, grid, stream);
+    case 32: return launch_one<NB, false, 4, 32>(p, grid, stream);
+    case 64: return launch_one<NB, false, 4, 64>(p, grid, stream);
+    default: return launch_one<NB, false, 4, 128>(p, grid, stream);
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_attention(const AttnParams& p, int grid, int nb, bool scores_only, cudaStream_t stream) {
+cudaError_t launch_attention(const AttnParams& p, int grid, int nb, bool scores_only, cudaStream_t stream,
+                             int npad) {
+  if (npad > 0) return nb == 1 ? launch_fused<1>(p, grid, npad, stream) : launch_fused<2>(p, grid, npad, stream);
   if (nb == 1) return scores_only ? launch_nb<1, true>(p, grid, stream) : launch_nb<1, false>(p, grid, stream);
   return scores_only ? launch_nb<2, true>(p, grid, stream) : launch_nb<2, false>(p, grid, stream);
 }

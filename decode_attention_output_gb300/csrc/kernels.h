@@ -41,7 +41,8 @@ struct AttnSmem {
     return off_merge_o() + (size_t)kGroupWarps * heads() * kMergeRow * 4;
   }
   __host__ __device__ constexpr size_t off_bars() const { return off_merge_ml() + (size_t)kGroupWarps * heads() * 2 * 4; }
-  __host__ __device__ constexpr size_t off_flags() const { return off_bars() + 2 * stages * 8; }
+  // barriers: full[S], empty[S] (attention); full[8], empty[8], accum[2] (fused projection)
+  __host__ __device__ constexpr size_t off_flags() const { return off_bars() + (2 * stages + 18) * 8; }
   __host__ __device__ constexpr size_t off_prefix() const { return off_flags() + 16; }
   __host__ __device__ constexpr size_t off_lens() const { return off_prefix() + (size_t)(batch + 1) * 4; }
   __host__ __device__ constexpr size_t total() const { return 1024 + off_lens() + (size_t)batch * 4; }
@@ -78,10 +79,30 @@ struct AttnParams {
   const char* prefetch;
   long long prefetch_bytes;
   int stages;            // requested pipeline depth (4 or 6)
+  // Fused step only (decode_attn_fwd in one launch): the projection of this kernel's
+  // own attention output (attn, contiguous [B][K]) by W_o, on tcgen05 after a grid barrier.
+  CUtensorMap tm_w;      // W_o [K][N] bf16: box 64 columns x 64 rows, 128B swizzle
+  CUtensorMap tm_x;      // attention output [B][K] bf16: box 64 k x npad rows, 128B swizzle
+  __nv_bfloat16* y;      // [B][N]
+  long long y_sb;
+  float* proj_part;      // [slots][B][128] fp32 split-K partials
+  int* proj_counters;    // [column tiles], zero between calls
+  int* grid_sync;        // [2]: arrivals, departures of the grid barrier, zero between calls
+  int N, K, kb_per_tile, units;  // units = column tiles x k-blocks of 64
 };
 
-// grid = number of persistent CTAs; nb = 1 for G <= 8, 2 for G <= 16.
-cudaError_t launch_attention(const AttnParams& p, int grid, int nb, bool scores_only, cudaStream_t stream);
+constexpr int kProjWBytes = 2 * 64 * 128;  // one stage of W_o: 128 columns x 64 k-rows
+// Phase-B stages re-cut the attention ring (kStages x kStageBytes) into W_o + X tiles.
+__host__ __device__ constexpr int proj_stage_bytes(int npad) { return kProjWBytes + ((npad * 128 + 1023) / 1024) * 1024; }
+__host__ __device__ constexpr int proj_stages(int npad) {
+  return (4 * kStageBytes) / proj_stage_bytes(npad) < 8 ? (4 * kStageBytes) / proj_stage_bytes(npad) : 8;
+}
+
+// grid = number of persistent CTAs; nb = 1 for G <= 8, 2 for G <= 16; npad = 0 for the
+// attention alone, else the batch padding (16/32/64/128) of the fused projection
+// (a cooperative launch: every CTA must be resident for the grid barrier).
+cudaError_t launch_attention(const AttnParams& p, int grid, int nb, bool scores_only, cudaStream_t stream,
+                             int npad = 0);
 
 // ------------------------------------------------------- projection: GEMV path
 constexpr int kGemvThreads = 256;

@@ -16,6 +16,7 @@ enum : int {
   kErrWaitDrain = 4,     // in-flight copies did not land before exit
   kErrWaitMma = 8,       // tensor-core completion never arrived
   kErrTmem = 16,         // TMEM allocation failed
+  kErrGridSync = 32,     // the fused step's grid barrier did not complete
 };
 
 // Two seconds: a kernel of this library runs for milliseconds at most.
@@ -219,6 +220,18 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* addr, int v) {
   int old;
   asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
   return old;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* addr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
+// Orders this thread's generic-proxy view of global memory before its later
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

@@ -178,6 +178,10 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *                   the prefetch competes with the K/V stream)
  *   "attn_stages"   4 (default) or 6: depth of the attention kernel's K/V ring
  *                   (6 only when it fits in shared memory for the batch)
+ *   "fused"         0 (default): decode_attn_fwd runs two launches (attention,
+ *                   projection); 1: one persistent cooperative launch (attention,
+ *                   a bounded grid barrier, tcgen05 projection) when batch <= 128
+ *                   (correct, but measured slower on GB300 so far)
  * Returns DA_OK or DA_ERR_OPTION.
  */
 int decode_attn_set_option(const char* key, int64_t value);

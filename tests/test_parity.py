@@ -304,3 +304,64 @@ def test_fused_step_on_each_projection_path(orc, path):
     ref_attn, ref_out = oracle_decode(orc, x)
     assert_bf16_close(f64(attn), ref_attn, f"path {path} attention")
     assert_bf16_close(f64(out), ref_out, f"path {path} output")
+
+
+# ------------------------------------------------------------- fused decode step
+class _Opt:
+    def __init__(self, **kv):
+        self.kv = kv
+
+    def __enter__(self):
+        self.old = {k: da.decode_attn_get_option(k) for k in self.kv}
+        for k, v in self.kv.items():
+            da.decode_attn_set_option(k, v)
+
+    def __exit__(self, *exc):
+        for k, v in self.old.items():
+            da.decode_attn_set_option(k, v)
+
+
+FUSED_CASES = [
+    W("f_b1_g4", 1, 32, 8, 700, 4096, (700,)),
+    W("f_b3_g4_ragged", 3, 8, 2, 300, 256, (300, 0, 129)),
+    W("f_b8_g8", 8, 16, 2, 200, 384, (200, 1, 64, 65, 199, 128, 3, 100)),
+    W("f_b17_g16", 17, 32, 2, 130, 264, tuple([130, 1] * 8 + [64])),
+    W("f_b40_g4", 40, 8, 2, 90, 512, tuple(int(x) for x in np.random.default_rng(5).integers(0, 91, 40))),
+    W("f_b100_g1", 100, 4, 4, 70, 128, tuple(int(x) for x in np.random.default_rng(6).integers(1, 71, 100))),
+]
+
+
+@pytest.mark.parametrize("w", FUSED_CASES, ids=[c.name for c in FUSED_CASES])
+def test_fused_step_matches_oracle_and_two_launches(orc, w):
+    """decode_attn_fwd as one persistent launch (attention, grid barrier, tcgen05
+    projection) against the oracle and against the two-launch path."""
+    with _Opt(fused=1):
+        x, attn, out = _run(w, seed=17)
+    with _Opt(fused=0):
+        out2 = torch.full_like(out, float("nan"))
+        da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out2, x["scale"])
+        torch.cuda.synchronize()
+    assert da.decode_attn_device_error() == 0
+    ref_attn, ref_out = oracle_decode(orc, x)
+    assert_bf16_close(f64(out), ref_out, f"{w.name} fused output")
+    assert_bf16_close(f64(out2), ref_out, f"{w.name} two-launch output")
+
+
+def test_fused_step_integer_exact():
+    """Integer attention outputs (V rows constant per KV head make every output an
+    integer) and W in {-1, 0, 1}: the fused projection is the exact integer product."""
+    B, Hq, Hkv, L, N = 8, 32, 8, 333, 384
+    w = W("f_int", B, Hq, Hkv, L, N, (L,) * B)
+    x = synth.make_inputs(w, seed=3, device=DEV)
+    vals = torch.randint(-3, 4, (B, Hkv, 1, 128), generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    x["v_cache"][:] = vals.to(DEV)  # softmax weights sum to one: attention = that row exactly
+    wi = torch.randint(-1, 2, (Hq * 128, N), generator=torch.Generator().manual_seed(5))
+    attn_ref = vals[:, :, 0].repeat_interleave(Hq // Hkv, dim=1).reshape(B, Hq * 128).long()
+    ref = (attn_ref @ wi.long()).double().to(torch.bfloat16)
+    out = torch.full((B, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    with _Opt(fused=1):
+        da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], wi.to(torch.bfloat16).to(DEV), out,
+                           x["scale"])
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_error() == 0
+    assert torch.equal(out.cpu(), ref)

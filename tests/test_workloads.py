@@ -40,11 +40,12 @@ def test_workload_sampled_rows(orc, name):
     torch.cuda.synchronize()
     assert da.decode_attn_device_error() == 0
     assert torch.isfinite(out.float()).all() and torch.isfinite(attn.float()).all()
-    # the fused step projects the same attention the attention-only entry returns
+    # the whole step agrees with projecting the attention-only result (split-K orders
+    # may differ, so within the bf16 tolerance rather than bit for bit)
     out2 = torch.empty_like(out)
     da.decode_attn_oproj(attn.view(w.B, w.Hq * 128), x["o_weight"], out2)
     torch.cuda.synchronize()
-    assert torch.equal(out, out2)
+    assert_bf16_close(f64(out), f64(out2), f"{name} fused vs two-launch")
 
     lens = x["seq_lens"].cpu().numpy()
     rows = sorted({0, w.B - 1, int(np.argmax(lens)), int(np.argmin(lens))})
