@@ -246,22 +246,32 @@ __device__ void fused_epilogue(const AttnParams& p, uint64_t* bars, uint32_t tme
     if (tid == 0) flags[2] = (atomic_add_acq_rel_gpu(p.proj_counters + tile, 1) == np - 1);
     named_bar_sync(2, 128);
     if (flags[2]) {  // the last part of this column tile: sum all parts in order
+      // batch rows in chunks of up to 32; per pass about 64 loads from clamped (always
+      // valid) addresses are in flight, masked afterwards; parts are added in order
+      constexpr int kChunk = NPAD < 32 ? NPAD : 32;
+      constexpr int kParts = 64 / kChunk;
+      for (int bc = 0; bc < p.B; bc += kChunk) {
+        float sum[kChunk];
 #pragma unroll
-      for (int b = 0; b < NPAD; ++b) acc[b] = 0.f;
-      constexpr int kParts = NPAD >= 64 ? 1 : 64 / NPAD;  // about 64 loads in flight per thread
-      for (int p0 = 0; p0 < np; p0 += kParts) {
+        for (int b = 0; b < kChunk; ++b) sum[b] = 0.f;
+        for (int p0 = 0; p0 < np; p0 += kParts) {
+          float v[kParts][kChunk];
 #pragma unroll
-        for (int u = 0; u < kParts; ++u) {
-          const int pc = p0 + u;
+          for (int u = 0; u < kParts; ++u) {
+            const int pc = min(p0 + u, np - 1);
 #pragma unroll
-          for (int b = 0; b < NPAD; ++b)
-            if (pc < np && b < p.B)
-              acc[b] += __ldcg(p.proj_part + (((long long)first + pc + tile) * p.B + b) * 128 + m);
+            for (int b = 0; b < kChunk; ++b)
+              v[u][b] = __ldcg(p.proj_part + (((long long)first + pc + tile) * p.B + min(bc + b, p.B - 1)) * 128 + m);
+          }
+#pragma unroll
+          for (int u = 0; u < kParts; ++u)
+#pragma unroll
+            for (int b = 0; b < kChunk; ++b) sum[b] += (p0 + u < np) ? v[u][b] : 0.f;
         }
-      }
 #pragma unroll
-      for (int b = 0; b < NPAD; ++b)
-        if (n_ok && b < p.B) p.y[(long long)b * p.y_sb + n] = __float2bfloat16_rn(acc[b]);
+        for (int b = 0; b < kChunk; ++b)
+          if (n_ok && bc + b < p.B) p.y[(long long)(bc + b) * p.y_sb + n] = __float2bfloat16_rn(sum[b]);
+      }
       if (tid == 0) p.proj_counters[tile] = 0;  // ready for the next call
     }
     named_bar_sync(2, 128);  // flags[2] is reused by the next tile
@@ -695,13 +705,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
             for (int h = tid >> 7; h < G; h += 2) {
               float acc = 0.f;
               for (int p0 = 0; p0 < n_parts; p0 += 8) {
+                // clamped (always valid) addresses: eight loads in flight, masked afterwards
+                float v[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                  const int pc = p0 + u;
-                  if (pc < n_parts)
-                    acc += wpart[h * n_parts + pc] *
-                           __ldcg(p.part_o + (((long long)first_cta + pc + seq) * p.gpad + h) * kHeadDim + d);
+                  const int pc = min(p0 + u, n_parts - 1);
+                  v[u] = __ldcg(p.part_o + (((long long)first_cta + pc + seq) * p.gpad + h) * kHeadDim + d);
                 }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                  if (p0 + u < n_parts) acc += wpart[h * n_parts + p0 + u] * v[u];
               }
               p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc);
             }

@@ -118,14 +118,21 @@ __global__ void __launch_bounds__(kGemvThreads, 2) oproj_gemv_kernel(const __gri
 #pragma unroll
     for (int b = 0; b < BT; ++b) sum[b] = 0.f;
     // slice s is added after slice s-1 (a fixed order); eight slices' loads go out together
+    // clamped (always valid) addresses: a batch of loads in flight at once, masked afterwards
+    const int cc = c_ok ? c : p.N - 1;
+    const int bmax = p.B - 1;
     for (int s0 = 0; s0 < p.ksplit; s0 += 8) {
+      float v[8][BT];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int s = s0 + u;
+        const int s = min(s0 + u, p.ksplit - 1);
 #pragma unroll
-        for (int b = 0; b < BT; ++b)
-          if (c_ok && s < p.ksplit && b0 + b < p.B) sum[b] += __ldcg(p.part + ((long long)s * p.B + b0 + b) * p.N + c);
+        for (int b = 0; b < BT; ++b) v[u][b] = __ldcg(p.part + ((long long)s * p.B + min(b0 + b, bmax)) * p.N + cc);
       }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int b = 0; b < BT; ++b) sum[b] += (s0 + u < p.ksplit) ? v[u][b] : 0.f;
     }
 #pragma unroll
     for (int b = 0; b < BT; ++b)

@@ -156,24 +156,33 @@ __global__ void __launch_bounds__(kUmmaThreads, 2) oproj_umma_kernel(const __gri
     __syncthreads();
     if (*flag) {  // last k-slice of this column tile: sum all slices in order
       const int nb_valid = p.B - b0 < NPAD ? p.B - b0 : NPAD;
+      const int nc = n_ok ? n : p.N - 1;
+      // batch rows in chunks of up to 32; per pass about 64 loads from clamped (always
+      // valid) addresses are in flight, masked afterwards; slices are added in order
+      constexpr int kChunk = NPAD < 32 ? NPAD : 32;
+      constexpr int kSlices = 64 / kChunk;
+      for (int bc = 0; bc < nb_valid; bc += kChunk) {
+        float sum[kChunk];
 #pragma unroll
-      for (int b = 0; b < NPAD; ++b) acc[b] = 0.f;
-      // slice s is added after slice s-1 for every output (a fixed order); the loads of
-      // a batch of slices are independent and go out together
-      constexpr int kSlices = NPAD >= 64 ? 1 : 64 / NPAD;  // about 64 loads in flight per thread
-      for (int s0 = 0; s0 < p.ksplit; s0 += kSlices) {
+        for (int b = 0; b < kChunk; ++b) sum[b] = 0.f;
+        for (int s0 = 0; s0 < p.ksplit; s0 += kSlices) {
+          float v[kSlices][kChunk];
 #pragma unroll
-        for (int u = 0; u < kSlices; ++u) {
-          const int s = s0 + u;
+          for (int u = 0; u < kSlices; ++u) {
+            const int sl = min(s0 + u, p.ksplit - 1);
 #pragma unroll
-          for (int b = 0; b < NPAD; ++b)
-            if (n_ok && s < p.ksplit && b < nb_valid)
-              acc[b] += __ldcg(p.part + ((long long)s * p.B + b0 + b) * p.N + n);
+            for (int b = 0; b < kChunk; ++b)
+              v[u][b] = __ldcg(p.part + ((long long)sl * p.B + b0 + min(bc + b, nb_valid - 1)) * p.N + nc);
+          }
+#pragma unroll
+          for (int u = 0; u < kSlices; ++u)
+#pragma unroll
+            for (int b = 0; b < kChunk; ++b) sum[b] += (s0 + u < p.ksplit) ? v[u][b] : 0.f;
         }
-      }
 #pragma unroll
-      for (int b = 0; b < NPAD; ++b)
-        if (n_ok && b < nb_valid) p.y[(long long)(b0 + b) * p.y_sb + n] = __float2bfloat16_rn(acc[b]);
+        for (int b = 0; b < kChunk; ++b)
+          if (n_ok && bc + b < nb_valid) p.y[(long long)(b0 + bc + b) * p.y_sb + n] = __float2bfloat16_rn(sum[b]);
+      }
       if (tid == 0) *counter = 0;
     }
   }
