@@ -28,6 +28,7 @@ struct Options {
   int64_t l2_prefetch = 0;  // fused step: the attention kernel pulls W_o into L2 (measured slower: off)
   int64_t attn_stages = 4;  // attention pipeline depth, 4 or 6 (6 measured slower)
   int64_t fused = 0;        // decode_attn_fwd as one persistent launch (measured slower so far: off)
+  int64_t fused_attn_ctas = 0;  // attention workers of the fused step (0: about 4 tiles each)
 };
 std::mutex g_mu;
 Options g_opt;
@@ -369,7 +370,7 @@ int run_projection(const __nv_bfloat16* x, long long x_sb, const da_tensor_t* w,
 // The fused step: attention, grid barrier and tcgen05 projection in one cooperative launch.
 struct FusedPlan {
   bool ok = false;
-  int npad = 0, kb_per_tile = 0, mtiles = 0, units = 0;
+  int npad = 0, kb_per_tile = 0, mtiles = 0, units = 0, attn_workers = 0;
   size_t part_bytes = 0;
 };
 
@@ -385,6 +386,12 @@ FusedPlan plan_fused(const AttnShape& s, int K, int N, const AttnPlan& ap, const
   if ((f.units + pb - 1) / pb > f.kb_per_tile + 1) return f;
   if (f.mtiles > (int)kMaxCounters) return f;
   f.part_bytes = align_up((size_t)(pb + f.mtiles) * s.B * 128 * 4, 256);
+  // Attention workers: about four tiles each (from the cache capacity, an upper bound
+  // of the device-side lengths), so that with short sequences the other CTAs start on
+  // W_o at once. The attention partial slots are sized for the full grid anyway.
+  const long long tiles = (long long)s.B * s.Hkv * ((s.Lcap + kTile - 1) / kTile);
+  f.attn_workers = o.fused_attn_ctas > 0 ? (int)std::min<long long>(o.fused_attn_ctas, ap.grid)
+                                         : (int)std::max<long long>(1, std::min<long long>(ap.grid, (tiles + 3) / 4));
   f.ok = true;
   return f;
 }
@@ -417,6 +424,7 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
     p.kb_per_tile = fused->plan->kb_per_tile;
     p.units = fused->plan->units;
   }
+
   DA_TRY(encode_kv_map(&p.tm_k, k));
   if (v) DA_TRY(encode_kv_map(&p.tm_v, v));
   else p.tm_v = p.tm_k;
@@ -441,6 +449,7 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
   p.gpad = pl.gpad;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.stages = (int)options_snapshot().attn_stages;
+  p.attn_workers = fused ? fused->plan->attn_workers : pl.grid;
   p.prefetch = static_cast<const char*>(prefetch);
   p.prefetch_bytes = prefetch ? (prefetch_bytes & ~15ll) : 0;
   const cudaError_t e = launch_attention(p, pl.grid, pl.nb, scores != nullptr, stream, fused ? fused->plan->npad : 0);
@@ -485,6 +494,7 @@ int decode_attn_set_option(const char* key, int64_t value) {
   else if (!strcmp(key, "l2_prefetch") && (value == 0 || value == 1)) g_opt.l2_prefetch = value;
   else if (!strcmp(key, "attn_stages") && (value == 4 || value == 6)) g_opt.attn_stages = value;
   else if (!strcmp(key, "fused") && (value == 0 || value == 1)) g_opt.fused = value;
+  else if (!strcmp(key, "fused_attn_ctas") && value >= 0 && value <= kMaxAttnCtas) g_opt.fused_attn_ctas = value;
   else return DA_ERR_OPTION;
   return DA_OK;
 }
@@ -500,6 +510,7 @@ int decode_attn_get_option(const char* key, int64_t* value) {
   else if (!strcmp(key, "l2_prefetch")) *value = g_opt.l2_prefetch;
   else if (!strcmp(key, "attn_stages")) *value = g_opt.attn_stages;
   else if (!strcmp(key, "fused")) *value = g_opt.fused;
+  else if (!strcmp(key, "fused_attn_ctas")) *value = g_opt.fused_attn_ctas;
   else return DA_ERR_OPTION;
   return DA_OK;
 }

@@ -132,15 +132,25 @@ __device__ void fused_producer(const AttnParams& p, uint32_t ring, uint64_t* bar
   auto empty_a = [&](int s) { return smem_u32(bars + S + s); };
   auto full_b = [&](int s) { return smem_u32(bars + 2 * S + s); };
   auto empty_b = [&](int s) { return smem_u32(bars + 2 * S + 8 + s); };
-  // the last phase-A fill of every stage must have been consumed
-  for (int k = it_a > S ? it_a - S : 0; k < it_a; ++k)
-    mbar_wait_bounded(empty_a(k % S), (k / S) & 1, p.err, kErrWaitEmpty, flags);
   const ProjSplit ps = proj_split(p, blockIdx.x);
   const int nu = (int)(ps.u1 - ps.u0);
   const int pre = nu < SB ? nu : SB;
   prefetch_tensormap(&p.tm_w);
   prefetch_tensormap(&p.tm_x);
-  for (int j = 0; j < pre; ++j) {
+  // Fill phase-B stages from the top of the ring down: a stage only waits for the phase-A
+  // stages it overlaps that were actually used (their last fill must have been consumed),
+  // so CTAs with few attention tiles start on W_o while their attention is still running.
+  int released = S;  // phase-A stages [released, S) are known free
+  for (int jj = pre - 1; jj >= 0; --jj) {
+    const int j = jj;
+    const int lo_a = (j * kStageB) / kStageBytes;  // lowest phase-A stage this phase-B stage touches
+    while (released > lo_a) {
+      --released;
+      if (released < it_a) {  // stage used in phase A: wait for the consumers of its last fill
+        const int k = released + ((it_a - 1 - released) / S) * S;
+        mbar_wait_bounded(empty_a(released), (k / S) & 1, p.err, kErrWaitEmpty, flags);
+      }
+    }
     const int unit = (int)ps.u0 + j, tile = unit / p.kb_per_tile, kb = unit - tile * p.kb_per_tile;
     const uint32_t dst = ring + j * kStageB;
     mbar_arrive_expect_tx(full_b(j), kProjWBytes + kXBytes);
@@ -361,7 +371,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   const int cta = blockIdx.x;
   // P workers share the T tiles; with P <= T every range is non-empty, so the CTAs
   // cta_of(first tile) .. cta_of(last tile) of a sequence all hold a part of it.
-  const int P = T > 0 ? (int)min((long long)gridDim.x, T) : 1;
+  const int P = T > 0 ? (int)min((long long)min((int)gridDim.x, p.attn_workers), T) : 1;
   const long long start = (T > 0 && cta < P) ? (long long)cta * T / P : 0;
   const long long end = (T > 0 && cta < P) ? (long long)(cta + 1) * T / P : 0;
 
@@ -415,7 +425,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
           for (int h = 0; h < G; ++h) bulk_load(qdst + h * kQRowBytes, qsrc + (long long)h * p.q_sh, 256, fb);
         }
       }
-      // Do not leave with copies in flight (only matters if the consumers gave up).
+      // Do not leave with copies in flight (only matters if the consumers gave up; the fused
+      // step's consumers wait for these copies before the CTA can end, so it skips this).
+      if (!kFused)
       for (int k = it > S ? it - S : 0; k < it; ++k)
         mbar_wait_bounded(full_bar(k % S), (k / S) & 1, p.err, kErrWaitDrain, nullptr,
                           kWaitLimitNs / 10);
@@ -704,16 +716,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
             // (b) O[h][d] = sum_p w_p O_p[h][d]: the loads of eight parts go out together
             for (int h = tid >> 7; h < G; h += 2) {
               float acc = 0.f;
-              for (int p0 = 0; p0 < n_parts; p0 += 8) {
-                // clamped (always valid) addresses: eight loads in flight, masked afterwards
-                float v[8];
+              for (int p0 = 0; p0 < n_parts; p0 += 16) {
+                // clamped (always valid) addresses: sixteen loads in flight, masked afterwards
+                float v[16];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < 16; ++u) {
                   const int pc = min(p0 + u, n_parts - 1);
                   v[u] = __ldcg(p.part_o + (((long long)first_cta + pc + seq) * p.gpad + h) * kHeadDim + d);
                 }
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
+                for (int u = 0; u < 16; ++u)
                   if (p0 + u < n_parts) acc += wpart[h * n_parts + p0 + u] * v[u];
               }
               p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc);

@@ -89,6 +89,8 @@ struct AttnParams {
   int* proj_counters;    // [column tiles], zero between calls
   int* grid_sync;        // [2]: arrivals, departures of the grid barrier, zero between calls
   int N, K, kb_per_tile, units;  // units = column tiles x k-blocks of 64
+  int attn_workers;      // CTAs that take attention tiles (<= grid); the fused step may leave
+                         // some CTAs free to start on W_o at once
 };
 
 constexpr int kProjWBytes = 2 * 64 * 128;  // one stage of W_o: 128 columns x 64 k-rows

@@ -182,6 +182,8 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *                   projection); 1: one persistent cooperative launch (attention,
  *                   a bounded grid barrier, tcgen05 projection) when batch <= 128
  *                   (correct, but measured slower on GB300 so far)
+ *   "fused_attn_ctas" attention workers of the fused step (0: about four 64-token
+ *                   tiles each, at most one per SM; the other CTAs start on o_weight)
  * Returns DA_OK or DA_ERR_OPTION.
  */
 int decode_attn_set_option(const char* key, int64_t value);
