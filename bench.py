@@ -33,7 +33,7 @@ if ROOT not in sys.path:
 METRIC = "decode attn+o_proj µs/step and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 DEFAULT_WORKLOAD = "b8_h32x8_l8k"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["attn_decode.cu", "ptx.cuh", "kernels.h"]
+KERNEL_SOURCES = ["attn_decode.cuh", "attn_decode.cu", "ptx.cuh", "kernels.h"]
 
 
 def parse():

@@ -124,18 +124,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 4-D map over a [B][Hkv][Lcap][128] bf16 cache; box = 64 dims x 64 tokens.
+// 4-D map over a [B][Hkv][Lcap][D] bf16 cache; box = 64 dims x tile_tokens(D) tokens.
 int encode_kv_map(CUtensorMap* map, const da_tensor_t* t) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return DA_ERR_CUDA;
-  const int64_t B = t->shape[0], H = t->shape[1], L = t->shape[2];
+  const int64_t B = t->shape[0], H = t->shape[1], L = t->shape[2], D = t->shape[3];
   // a stride of an extent-1 dimension is never used; give it a harmless legal value
-  const int64_t st = L == 1 ? 128 : t->stride[2];
+  const int64_t st = L == 1 ? D : t->stride[2];
   const int64_t sh = H == 1 ? st * L : t->stride[1];
   const int64_t sb = B == 1 ? sh * H : t->stride[0];
-  cuuint64_t dims[4] = {128, (cuuint64_t)L, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)H, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)st * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)kTile, 1, 1};
+  cuuint32_t box[4] = {64, (cuuint32_t)tile_tokens((int)D), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -195,7 +195,7 @@ int check_tensor(const da_tensor_t* t, int dtype, int ndim, Use use) {
   } while (0)
 
 struct AttnShape {
-  int B, Hq, Hkv, G, Lcap;
+  int B, Hq, Hkv, G, Lcap, D;
 };
 
 int check_attention_inputs(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t* v,
@@ -206,8 +206,9 @@ int check_attention_inputs(const da_tensor_t* q, const da_tensor_t* k, const da_
   if (!lens) return DA_ERR_NULL;
   if (lens->dtype != DA_DTYPE_I32) return DA_ERR_DTYPE;
   if (lens->ndim != 1) return DA_ERR_SHAPE;
-  const int64_t B = q->shape[0], Hq = q->shape[1], Hkv = k->shape[1], Lcap = k->shape[2];
-  if (q->shape[2] != kHeadDim || k->shape[3] != kHeadDim) return DA_ERR_SHAPE;
+  const int64_t B = q->shape[0], Hq = q->shape[1], Hkv = k->shape[1], Lcap = k->shape[2], D = q->shape[2];
+  if (k->shape[3] != D) return DA_ERR_SHAPE;
+  if (D != kHeadDim && D != kHeadDimWide) return DA_ERR_SHAPE;
   if (k->shape[0] != B || lens->shape[0] != B) return DA_ERR_SHAPE;
   if (need_v)
     for (int i = 0; i < 4; ++i)
@@ -223,12 +224,14 @@ int check_attention_inputs(const da_tensor_t* q, const da_tensor_t* k, const da_
   if (B > DA_MAX_BATCH) return DA_ERR_UNSUPPORTED;
   if (B * Hkv > (int64_t)kMaxCounters) return DA_ERR_UNSUPPORTED;
   if (Lcap > (int64_t)1 << 30) return DA_ERR_UNSUPPORTED;
-  if (B * Hkv * ((Lcap + kTile - 1) / kTile) >= ((int64_t)1 << 31)) return DA_ERR_UNSUPPORTED;
+  const int64_t tt = tile_tokens((int)D);
+  if (B * Hkv * ((Lcap + tt - 1) / tt) >= ((int64_t)1 << 31)) return DA_ERR_UNSUPPORTED;
   s->B = (int)B;
   s->Hq = (int)Hq;
   s->Hkv = (int)Hkv;
   s->G = (int)(Hq / Hkv);
   s->Lcap = (int)Lcap;
+  s->D = (int)D;
   return DA_OK;
 }
 
@@ -249,7 +252,7 @@ AttnPlan plan_attention(const AttnShape& s, const Options& o) {
   const size_t slots = (size_t)pl.grid + (size_t)s.B * s.Hkv;
   pl.part_ml_off = 0;
   pl.part_o_off = align_up(slots * pl.gpad * 2 * 4, 256);
-  pl.bytes = pl.part_o_off + align_up(slots * pl.gpad * kHeadDim * 4, 256);
+  pl.bytes = pl.part_o_off + align_up(slots * pl.gpad * s.D * 4, 256);
   return pl;
 }
 
@@ -376,7 +379,7 @@ struct FusedPlan {
 
 FusedPlan plan_fused(const AttnShape& s, int K, int N, const AttnPlan& ap, const Options& o) {
   FusedPlan f;
-  if (!o.fused || o.oproj_path == 1 || s.B > 128 || K % 64) return f;
+  if (!o.fused || o.oproj_path == 1 || s.B > 128 || K % 64 || s.D != kHeadDim) return f;
   f.npad = s.B <= 16 ? 16 : (s.B <= 32 ? 32 : (s.B <= 64 ? 64 : 128));
   f.kb_per_tile = K / 64;
   f.mtiles = (N + 127) / 128;
@@ -389,7 +392,7 @@ FusedPlan plan_fused(const AttnShape& s, int K, int N, const AttnPlan& ap, const
   // Attention workers: about four tiles each (from the cache capacity, an upper bound
   // of the device-side lengths), so that with short sequences the other CTAs start on
   // W_o at once. The attention partial slots are sized for the full grid anyway.
-  const long long tiles = (long long)s.B * s.Hkv * ((s.Lcap + kTile - 1) / kTile);
+  const long long tiles = (long long)s.B * s.Hkv * ((s.Lcap + kTile - 1) / kTile);  // D = 128 tiles
   f.attn_workers = o.fused_attn_ctas > 0 ? (int)std::min<long long>(o.fused_attn_ctas, ap.grid)
                                          : (int)std::max<long long>(1, std::min<long long>(ap.grid, (tiles + 3) / 4));
   f.ok = true;
@@ -452,7 +455,8 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
   p.attn_workers = fused ? fused->plan->attn_workers : pl.grid;
   p.prefetch = static_cast<const char*>(prefetch);
   p.prefetch_bytes = prefetch ? (prefetch_bytes & ~15ll) : 0;
-  const cudaError_t e = launch_attention(p, pl.grid, pl.nb, scores != nullptr, stream, fused ? fused->plan->npad : 0);
+  const cudaError_t e =
+      launch_attention(p, pl.grid, pl.nb, s.D, scores != nullptr, stream, fused ? fused->plan->npad : 0);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
     cudaGetLastError();
     return DA_ERR_UNSUPPORTED;  // the caller falls back to two launches
@@ -520,7 +524,7 @@ int decode_attn_only(const da_tensor_t* q, const da_tensor_t* k_cache, const da_
   AttnShape s;
   DA_TRY(check_attention_inputs(q, k_cache, v_cache, seq_lens, true, &s));
   DA_TRY(check_tensor(attn_out, DA_DTYPE_BF16, 3, kOutput));
-  if (attn_out->shape[0] != s.B || attn_out->shape[1] != s.Hq || attn_out->shape[2] != kHeadDim)
+  if (attn_out->shape[0] != s.B || attn_out->shape[1] != s.Hq || attn_out->shape[2] != s.D)
     return DA_ERR_SHAPE;
   if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
   if (s.B == 0) return DA_OK;
@@ -576,7 +580,7 @@ int decode_attn_only_noalloc(const da_tensor_t* q, const da_tensor_t* k_cache, c
   AttnShape s;
   DA_TRY(check_attention_inputs(q, k_cache, v_cache, seq_lens, true, &s));
   DA_TRY(check_tensor(attn_out, DA_DTYPE_BF16, 3, kOutput));
-  if (attn_out->shape[0] != s.B || attn_out->shape[1] != s.Hq || attn_out->shape[2] != kHeadDim)
+  if (attn_out->shape[0] != s.B || attn_out->shape[1] != s.Hq || attn_out->shape[2] != s.D)
     return DA_ERR_SHAPE;
   if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
   if (s.B == 0) return DA_OK;
@@ -636,7 +640,7 @@ int decode_attn_fwd(const da_tensor_t* q, const da_tensor_t* k_cache, const da_t
   DA_TRY(check_attention_inputs(q, k_cache, v_cache, seq_lens, true, &s));
   DA_TRY(check_tensor(o_weight, DA_DTYPE_BF16, 2, kInput16));
   DA_TRY(check_tensor(out, DA_DTYPE_BF16, 2, kOutput));
-  const int64_t K = (int64_t)s.Hq * kHeadDim, N = o_weight->shape[1];
+  const int64_t K = (int64_t)s.Hq * s.D, N = o_weight->shape[1];
   if (o_weight->shape[0] != K || out->shape[0] != s.B || out->shape[1] != N) return DA_ERR_SHAPE;
   if (N <= 0 || N % 8) return DA_ERR_SHAPE;
   if (N > (1 << 30) || K > (1 << 30)) return DA_ERR_UNSUPPORTED;
@@ -654,7 +658,7 @@ int decode_attn_fwd(const da_tensor_t* q, const da_tensor_t* k_cache, const da_t
     __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(scratch + ap.bytes);
     const FusedArgs fa{&fp, o_weight, out, reinterpret_cast<float*>(scratch + ap.bytes + attn_bytes), (int)K, (int)N};
     const long long w_span = ((long long)(K - 1) * o_weight->stride[0] + N) * 2;
-    const int rc = run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, kHeadDim, nullptr, 0, 0,
+    const int rc = run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, s.D, nullptr, 0, 0,
                                  scale, st, o.l2_prefetch ? o_weight->data : nullptr, w_span, &fa);
     if (rc != DA_ERR_UNSUPPORTED) return rc;  // else: not co-resident here, take two launches
   }
@@ -665,7 +669,7 @@ int decode_attn_fwd(const da_tensor_t* q, const da_tensor_t* k_cache, const da_t
   __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(scratch + ap.bytes);
   // W_o span: rows 0..K-1 of stride w_sk, the last row N wide
   const long long w_span = ((long long)(K - 1) * o_weight->stride[0] + N) * 2;
-  DA_TRY(run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, kHeadDim, nullptr, 0, 0, scale,
+  DA_TRY(run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, s.D, nullptr, 0, 0, scale,
                        st, o.l2_prefetch ? o_weight->data : nullptr, w_span));
   return run_projection(attn, K, o_weight, out, s.B, (int)K, (int)N, ws, scratch + ap.bytes + attn_bytes, gp,
                         o.pdl != 0, st);

@@ -1,0 +1,826 @@
+// attn_decode.cuh -- persistent split-KV decode attention for sm_103a (the kernel
+// template; attn_decode.cu instantiates head dim 128 and the fused step,
+// attn_decode_d256.cu head dim 256).
+//
+// Computes, for every batch row b and query head h (KV head j = h / G),
+//   S = q . K^T over t < L_b (the page's scores_fp32, fp32),
+//   P = softmax(scale * S),  O = P . V  (the page's attn_output, bf16),
+// the three-matmul decode attention of the page "PyPTO 开箱性能调优实战 Decode
+// Attention 多 Matmul 独立 TileShape 配置 F-16", section "代码对比", with the
+// QK^T and attn.V shapes of its table "三个 Matmul 的 Shape 特征分析".
+//
+// Design (GB300):
+//  * Work unit = one tile (64 tokens at D = 128, 32 at D = 256: 32 KB of K+V
+//    either way) of one (batch, KV-head) sequence. All tiles of
+//    the batch are laid end to end and each persistent CTA takes an equal,
+//    contiguous range of them, so ragged batches stay balanced. A range may end
+//    or start inside a sequence: each CTA emits one partial (m, l, O) per
+//    sequence it touches; the CTA that finishes a sequence last (an atomic
+//    completion counter, no waiting) merges the partials with the log-sum-exp
+//    rule and writes bf16.
+//  * One producer warp streams K and V tiles with 4-D TMA (128-byte swizzle,
+//    two 64-dim boxes per tile) into a 4- or 6-stage shared-memory ring guarded by
+//    mbarriers; q rows arrive by 1-D bulk copy with a sequence's first tiles.
+//    At D = 256 a tile is four 64-dim boxes of 32 tokens.
+//  * Two consumer groups of four warps take alternate stages, so two tiles are
+//    in compute at once per SM. Each warp owns 16 tokens of a stage and all G
+//    query heads of the group (every K/V byte is read once). S^T = K . Q^T runs
+//    on mma.sync m16n8k16 with tokens as M and heads as N (G <= 8 fills one
+//    8-wide N block); the online softmax runs in registers (running max / sum,
+//    shuffle reductions, exp2 with scale*log2e folded); P is rounded to bf16 and
+//    moved into the B-operand layout with movmatrix; O^T = V^T . P^T accumulates
+//    in fp32 registers. At the end of a sequence segment the eight warps' states
+//    are merged (pairwise in registers, then across four warps in shared memory).
+//  * D = 256 (a GQA decode whose QK^T contracts D in two 128-wide halves and whose
+//    attn.V has N = D split in two, page "PyPTO 开箱性能调优实战 Decode Attention
+//    多 Matmul 独立 TileShape 配置 F-16", section "仓库源码佐证"): the warps of a group
+//    pair up on 16 tokens; both compute the 16 x G scores over all 256 dims (the
+//    tensor pipe is mostly idle, so the duplicate QK^T is cheap) and hence the same
+//    softmax state, and each accumulates one 128-dim half of O. Registers per
+//    thread stay those of D = 128 except the q fragments, which double.
+#pragma once
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace da {
+namespace {
+
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// Position of the current tile in the flattened tile order.
+struct Cursor {
+  int b, kvh, j, nt;  // batch row, KV head, tile index in the sequence, tiles in the sequence
+};
+
+// prefix[b] = KV heads x tiles of all batch rows before b; prefix[B] = total tiles.
+__device__ __forceinline__ Cursor cursor_at(long long x, const int* prefix, int B, int Hkv) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  Cursor c;
+  c.b = lo;
+  c.nt = (prefix[lo + 1] - prefix[lo]) / Hkv;
+  const int r = (int)(x - prefix[lo]);
+  c.kvh = r / c.nt;
+  c.j = r - c.kvh * c.nt;
+  return c;
+}
+
+// Advances to the next tile (only called while one exists).
+__device__ __forceinline__ void cursor_next(Cursor& c, const int* prefix, int B, int Hkv) {
+  if (++c.j < c.nt) return;
+  c.j = 0;
+  if (++c.kvh < Hkv) return;
+  c.kvh = 0;
+  do {
+    ++c.b;
+  } while (c.b < B - 1 && prefix[c.b + 1] == prefix[c.b]);
+  c.nt = (prefix[c.b + 1] - prefix[c.b]) / Hkv;
+}
+
+// CTA whose range [i*T/P, (i+1)*T/P) holds tile x.
+__device__ __forceinline__ int cta_of(long long x, long long T, int P) {
+  return (int)(((x + 1) * (long long)P - 1) / T);
+}
+
+__device__ __forceinline__ int clamp_len(int L, int Lcap) { return L < 0 ? 0 : (L > Lcap ? Lcap : L); }
+
+// Keep the bf16 halves of v whose token index (tok for the low half, tok + 1 for
+// the high half) is below `valid`.
+__device__ __forceinline__ uint32_t mask_tokens(uint32_t v, int tok, int valid) {
+  const uint32_t lo = tok < valid ? 0x0000ffffu : 0u;
+  const uint32_t hi = tok + 1 < valid ? 0xffff0000u : 0u;
+  return v & (lo | hi);
+}
+
+// ---------------------------------------------------------------- fused step
+// Phase B of the fused step projects the attention output X [B][K] with W_o [K][N]
+// on tcgen05: y^T[n][b] = W_o^T[n][k] . X^T[k][b] (swap-AB: M = 128 hidden columns,
+// N = batch padded to NPAD). Work unit = one column tile (128 columns) x one 64-row
+// k-block of W_o; the units are laid end to end (column tile major) and each CTA
+// takes an equal contiguous range, so a CTA covers at most two column tiles (the
+// host checks it) and accumulates each in its own TMEM region.
+struct ProjSplit {
+  int PB;             // CTAs with phase-B work
+  long long u0, u1;   // this CTA's units
+};
+
+__device__ __forceinline__ ProjSplit proj_split(const AttnParams& p, int cta) {
+  ProjSplit r;
+  r.PB = min((int)gridDim.x, p.units);
+  r.u0 = cta < r.PB ? (long long)cta * p.units / r.PB : 0;
+  r.u1 = cta < r.PB ? (long long)(cta + 1) * p.units / r.PB : 0;
+  return r;
+}
+
+// Waits until every CTA of the grid has arrived (bounded), then counts this CTA's
+// departure; the last one to leave resets both counters for the next launch.
+__device__ __forceinline__ bool grid_barrier_wait(int* sync, int n, int* err, volatile int* abort_flag) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (ld_acquire_gpu(sync) < n) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, kErrGridSync);
+      *abort_flag = 1;
+      return false;
+    }
+    __nanosleep(64);
+  }
+  if (atomic_add_acq_rel_gpu(sync + 1, 1) == n - 1) {
+    sync[0] = 0;
+    sync[1] = 0;
+  }
+  return true;
+}
+
+// Phase-B producer: refills the (now free) K/V ring with W_o tiles right away, and
+// with X tiles once the grid barrier says every attention output is written.
+template <int NPAD, int S>
+__device__ void fused_producer(const AttnParams& p, uint32_t ring, uint64_t* bars, int it_a, int* flags) {
+  constexpr uint32_t kXBytes = NPAD * 128;  // NPAD rows x 64 k x bf16
+  constexpr int SB = proj_stages(NPAD), kStageB = proj_stage_bytes(NPAD);
+  auto empty_a = [&](int s) { return smem_u32(bars + S + s); };
+  auto full_b = [&](int s) { return smem_u32(bars + 2 * S + s); };
+  auto empty_b = [&](int s) { return smem_u32(bars + 2 * S + 8 + s); };
+  const ProjSplit ps = proj_split(p, blockIdx.x);
+  const int nu = (int)(ps.u1 - ps.u0);
+  const int pre = nu < SB ? nu : SB;
+  prefetch_tensormap(&p.tm_w);
+  prefetch_tensormap(&p.tm_x);
+  // Fill phase-B stages from the top of the ring down: a stage only waits for the phase-A
+  // stages it overlaps that were actually used (their last fill must have been consumed),
+  // so CTAs with few attention tiles start on W_o while their attention is still running.
+  int released = S;  // phase-A stages [released, S) are known free
+  for (int jj = pre - 1; jj >= 0; --jj) {
+    const int j = jj;
+    const int lo_a = (j * kStageB) / kStageBytes;  // lowest phase-A stage this phase-B stage touches
+    while (released > lo_a) {
+      --released;
+      if (released < it_a) {  // stage used in phase A: wait for the consumers of its last fill
+        const int k = released + ((it_a - 1 - released) / S) * S;
+        mbar_wait_bounded(empty_a(released), (k / S) & 1, p.err, kErrWaitEmpty, flags);
+      }
+    }
+    const int unit = (int)ps.u0 + j, tile = unit / p.kb_per_tile, kb = unit - tile * p.kb_per_tile;
+    const uint32_t dst = ring + j * kStageB;
+    mbar_arrive_expect_tx(full_b(j), kProjWBytes + kXBytes);
+    tma_load_2d(dst, &p.tm_w, full_b(j), tile * 128, kb * 64);
+    tma_load_2d(dst + 8192, &p.tm_w, full_b(j), tile * 128 + 64, kb * 64);
+  }
+  grid_barrier_wait(p.grid_sync, gridDim.x, p.err, flags);
+  fence_proxy_async_global();  // X was written by other CTAs' generic stores; TMA reads it
+  for (int j = 0; j < pre; ++j) {
+    const int unit = (int)ps.u0 + j, tile = unit / p.kb_per_tile, kb = unit - tile * p.kb_per_tile;
+    tma_load_2d(ring + j * kStageB + kProjWBytes, &p.tm_x, full_b(j), kb * 64, 0);
+  }
+  for (int j = pre; j < nu; ++j) {
+    const int s = j % SB;
+    const uint32_t ph = (j / SB) & 1;
+    mbar_wait_bounded(empty_b(s), ph ^ 1, p.err, kErrWaitEmpty, flags);
+    const int unit = (int)ps.u0 + j, tile = unit / p.kb_per_tile, kb = unit - tile * p.kb_per_tile;
+    const uint32_t dst = ring + s * kStageB;
+    mbar_arrive_expect_tx(full_b(s), kProjWBytes + kXBytes);
+    tma_load_2d(dst, &p.tm_w, full_b(s), tile * 128, kb * 64);
+    tma_load_2d(dst + 8192, &p.tm_w, full_b(s), tile * 128 + 64, kb * 64);
+    tma_load_2d(dst + kProjWBytes, &p.tm_x, full_b(s), kb * 64, 0);
+  }
+  for (int k = nu > SB ? nu - SB : 0; k < nu; ++k)  // no copies in flight at exit
+    mbar_wait_bounded(full_b(k % SB), (k / SB) & 1, p.err, kErrWaitDrain, nullptr, kWaitLimitNs / 10);
+}
+
+// Phase-B MMA issuer (one thread): four tcgen05.mma per unit into the TMEM region of
+// its column tile; each stage is released by tcgen05.commit, each region's
+// accumulator is announced when the tile's last unit of this CTA is issued.
+template <int NPAD, int S>
+__device__ void fused_mma(const AttnParams& p, uint32_t ring, uint64_t* bars, uint32_t tmem, int* flags) {
+  constexpr uint32_t kIdesc = umma_idesc_bf16(128, NPAD, /*A MN-major*/ true, /*B K-major*/ false);
+  constexpr int SB = proj_stages(NPAD), kStageB = proj_stage_bytes(NPAD);
+  auto full_b = [&](int s) { return smem_u32(bars + 2 * S + s); };
+  auto empty_b = [&](int s) { return smem_u32(bars + 2 * S + 8 + s); };
+  const ProjSplit ps = proj_split(p, blockIdx.x);
+  const int nu = (int)(ps.u1 - ps.u0);
+  const int tile0 = nu > 0 ? (int)(ps.u0 / p.kb_per_tile) : 0;
+  for (int j = 0; j < nu; ++j) {
+    const int s = j % SB;
+    mbar_wait_bounded(full_b(s), (j / SB) & 1, p.err, kErrWaitFull, flags);
+    tc_fence_after_sync();
+    const int unit = (int)ps.u0 + j, tile = unit / p.kb_per_tile, kb = unit - tile * p.kb_per_tile;
+    const int region = tile - tile0;
+    const uint32_t a = ring + s * kStageB, bsm = a + kProjWBytes;
+    const bool first = (j == 0) || (kb == 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t adesc = umma_smem_desc(a + kk * 16 * 128, 64 * 128, 1024);
+      const uint64_t bdesc = umma_smem_desc(bsm + kk * 32, 16, 1024);
+      umma_bf16(tmem + region * NPAD, adesc, bdesc, kIdesc, !(first && kk == 0));
+    }
+    umma_commit(empty_b(s));
+    if (j == nu - 1 || kb == p.kb_per_tile - 1) umma_commit(smem_u32(bars + 2 * S + 16 + region));
+  }
+}
+
+// CTA of phase B holding unit u.
+__device__ __forceinline__ int proj_cta_of(long long u, int units, int PB) {
+  return (int)(((u + 1) * (long long)PB - 1) / units);
+}
+
+// Phase-B epilogue (warps 0-3, TMEM lanes 0-127 = the tile's 128 columns): bf16 out
+// when one CTA covered the whole column tile, else fp32 partials that the last
+// CTA of the tile sums in a fixed order (atomic counter, no waiting).
+template <int NPAD, int S>
+__device__ void fused_epilogue(const AttnParams& p, uint64_t* bars, uint32_t tmem, int* flags, int warp, int lane,
+                               int tid) {
+  const ProjSplit ps = proj_split(p, blockIdx.x);
+  if (ps.u1 <= ps.u0) return;
+  const int kb = p.kb_per_tile;
+  const int tile0 = (int)(ps.u0 / kb), tile1 = (int)((ps.u1 - 1) / kb);
+  for (int tile = tile0; tile <= tile1; ++tile) {
+    const int region = tile - tile0;
+    mbar_wait_bounded(smem_u32(bars + 2 * S + 16 + region), 0, p.err, kErrWaitMma, flags);
+    tc_fence_after_sync();
+    float acc[NPAD];
+#pragma unroll
+    for (int c = 0; c < NPAD / 16; ++c) {
+      uint32_t r[16];
+      tmem_ld_32x32b_x16(tmem + ((uint32_t)(warp * 32) << 16) + region * NPAD + c * 16, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[c * 16 + i] = __uint_as_float(r[i]);
+    }
+    const int m = warp * 32 + lane, n = tile * 128 + m;
+    const bool n_ok = n < p.N;
+    const int first = proj_cta_of((long long)tile * kb, p.units, ps.PB);
+    const int last = proj_cta_of((long long)tile * kb + kb - 1, p.units, ps.PB);
+    const int np = last - first + 1;
+    if (np == 1) {
+#pragma unroll
+      for (int b = 0; b < NPAD; ++b)
+        if (n_ok && b < p.B) p.y[(long long)b * p.y_sb + n] = __float2bfloat16_rn(acc[b]);
+      continue;
+    }
+    const long long slot = (long long)blockIdx.x + tile;
+#pragma unroll
+    for (int b = 0; b < NPAD; ++b)
+      if (b < p.B) p.proj_part[(slot * p.B + b) * 128 + m] = acc[b];
+    named_bar_sync(2, 128);  // every epilogue thread's partial stores precede the release
+    if (tid == 0) flags[2] = (atomic_add_acq_rel_gpu(p.proj_counters + tile, 1) == np - 1);
+    named_bar_sync(2, 128);
+    if (flags[2]) {  // the last part of this column tile: sum all parts in order
+      // batch rows in chunks of up to 32; per pass about 64 loads from clamped (always
+      // valid) addresses are in flight, masked afterwards; parts are added in order
+      constexpr int kChunk = NPAD < 32 ? NPAD : 32;
+      constexpr int kParts = 64 / kChunk;
+      for (int bc = 0; bc < p.B; bc += kChunk) {
+        float sum[kChunk];
+#pragma unroll
+        for (int b = 0; b < kChunk; ++b) sum[b] = 0.f;
+        for (int p0 = 0; p0 < np; p0 += kParts) {
+          float v[kParts][kChunk];
+#pragma unroll
+          for (int u = 0; u < kParts; ++u) {
+            const int pc = min(p0 + u, np - 1);
+#pragma unroll
+            for (int b = 0; b < kChunk; ++b)
+              v[u][b] = __ldcg(p.proj_part + (((long long)first + pc + tile) * p.B + min(bc + b, p.B - 1)) * 128 + m);
+          }
+#pragma unroll
+          for (int u = 0; u < kParts; ++u)
+#pragma unroll
+            for (int b = 0; b < kChunk; ++b) sum[b] += (p0 + u < np) ? v[u][b] : 0.f;
+        }
+#pragma unroll
+        for (int b = 0; b < kChunk; ++b)
+          if (n_ok && bc + b < p.B) p.y[(long long)(bc + b) * p.y_sb + n] = __float2bfloat16_rn(sum[b]);
+      }
+      if (tid == 0) p.proj_counters[tile] = 0;  // ready for the next call
+    }
+    named_bar_sync(2, 128);  // flags[2] is reused by the next tile
+  }
+}
+
+template <int NB, bool SCORES, int S, int NPAD, int DIM>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __grid_constant__ AttnParams p) {
+  constexpr bool kFused = NPAD > 0;
+  constexpr bool kWide = DIM == kHeadDimWide;
+  static_assert(DIM == kHeadDim || (kWide && !kFused), "head dim 128, or 256 without the fused step");
+  constexpr int kT = tile_tokens(DIM);    // tokens per tile
+  constexpr int kBox = box_bytes(DIM);    // one 64-dim box of a tile
+  constexpr int kQRow = q_row_bytes(DIM);
+  constexpr int kKs = DIM / 16;           // k-steps of QK^T
+  constexpr int kTmemCols = NPAD <= 16 ? 32 : 2 * NPAD;  // two accumulator regions
+  constexpr int HP = 8 * NB;  // heads per group, padded to the MMA width
+  const int B = p.B, Hkv = p.Hkv, G = p.G, Lcap = p.Lcap;
+  static_assert(S % kGroups == 0, "a stage must always be consumed by the same group");
+  constexpr AttnSmem kFixed(NB, 0, S, DIM);  // offsets that do not depend on the batch size
+  const AttnSmem lay(NB, B, S, DIM);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+
+  uint8_t* q_slots = smem + kFixed.off_q();
+  float* merge_o = reinterpret_cast<float*>(smem + kFixed.off_merge_o());    // [4][HP][kMergeRow]
+  float* merge_ml = reinterpret_cast<float*>(smem + kFixed.off_merge_ml());  // [4][HP][2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFixed.off_bars());
+  int* flags = reinterpret_cast<int*>(smem + kFixed.off_flags());            // [0] abort, [1] last CTA
+  int* prefix = reinterpret_cast<int*>(smem + lay.off_prefix());             // [B + 1]
+  int* lens = reinterpret_cast<int*>(smem + lay.off_lens());                 // [B], clamped
+  const uint32_t ring = smem_u32(smem);
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), kGroupWarps);
+    }
+    if (kFused) {
+      for (int s = 0; s < 8; ++s) {
+        mbar_init(smem_u32(bars + 2 * S + s), 1);      // phase-B full: the producer's expect-tx
+        mbar_init(smem_u32(bars + 2 * S + 8 + s), 1);  // phase-B empty: one tcgen05.commit
+      }
+      mbar_init(smem_u32(bars + 2 * S + 16), 1);  // accumulator of the first column tile
+      mbar_init(smem_u32(bars + 2 * S + 17), 1);  // ... and of the second
+    }
+    flags[0] = 0;
+    flags[1] = 0;
+    flags[2] = 0;
+    fence_barrier_init();
+  }
+  if (kFused && warp == 0) {  // TMEM for the projection accumulators (one CTA per SM)
+    tmem_alloc(smem_u32(flags + 3), kTmemCols);
+    tmem_relinquish();
+  }
+  // Padded head rows of the q slots stay zero for the whole kernel.
+  for (int i = tid; i < (int)(S * kFixed.q_slot() / 16); i += kAttnThreads)
+    reinterpret_cast<uint4*>(q_slots)[i] = make_uint4(0, 0, 0, 0);
+  if (warp == 1) {  // clamped lengths, and tiles per batch row scanned into prefix
+    int carry = 0;
+    for (int base = 0; base < B; base += 32) {
+      const int b = base + lane;
+      int v = 0;
+      if (b < B) {
+        const int L = clamp_len(__ldg(p.seq_lens + b), Lcap);
+        lens[b] = L;
+        v = ((L + kT - 1) / kT) * Hkv;
+      }
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += n;
+      }
+      if (b < B) prefix[b + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) prefix[0] = 0;
+  }
+  if (kFused) tc_fence_before_sync();
+  __syncthreads();
+  if (kFused) tc_fence_after_sync();
+  const uint32_t tmem = kFused ? (uint32_t)flags[3] : 0u;
+  // The projection kernel (launched with programmatic dependent launch) may now be
+  // scheduled; it waits for this grid's completion before it reads our output.
+  pdl_launch_dependents();
+
+  const long long T = prefix[B];
+  const int cta = blockIdx.x;
+  // P workers share the T tiles; with P <= T every range is non-empty, so the CTAs
+  // cta_of(first tile) .. cta_of(last tile) of a sequence all hold a part of it.
+  const int P = T > 0 ? (int)min((long long)min((int)gridDim.x, p.attn_workers), T) : 1;
+  const long long start = (T > 0 && cta < P) ? (long long)cta * T / P : 0;
+  const long long end = (T > 0 && cta < P) ? (long long)(cta + 1) * T / P : 0;
+
+  if (warp == kGroups * kGroupWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+     int it = 0;
+     if (start < end) {
+      prefetch_tensormap(&p.tm_k);
+      if (!SCORES) prefetch_tensormap(&p.tm_v);
+      const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read exactly once
+      // This CTA's share of the prefetch region, in 4 KB-aligned pieces, one per tile.
+      const uint64_t pf_policy = l2_policy_evict_last();
+      const long long pf_per_cta = ((p.prefetch_bytes + P - 1) / P + 4095) & ~4095ll;
+      const long long pf_begin = min((long long)cta * pf_per_cta, p.prefetch_bytes);
+      const long long pf_end = min(pf_begin + pf_per_cta, p.prefetch_bytes);
+      const long long pf_piece = ((pf_end - pf_begin + (end - start) - 1) / (end - start) + 4095) & ~4095ll;
+      long long pf_next = pf_begin;
+      Cursor c = cursor_at(start, prefix, B, Hkv);
+      long long seg0 = start;
+      for (long long x = start; x < end; ++x, ++it) {
+        if (x != start) {
+          cursor_next(c, prefix, B, Hkv);
+          if (c.j == 0) seg0 = x;
+        }
+        const bool with_q = x - seg0 < kGroups;  // each group's first tile of the segment
+        const int stage = it % S;
+        const uint32_t ph = (it / S) & 1;
+        mbar_wait_bounded(empty_bar(stage), ph ^ 1, p.err, kErrWaitEmpty, flags);
+        const uint32_t fb = full_bar(stage);
+        uint32_t bytes = SCORES ? kKTileBytes : kStageBytes;
+        if (with_q) bytes += G * DIM * 2;
+        mbar_arrive_expect_tx(fb, bytes);
+        const uint32_t kdst = ring + stage * kStageBytes;
+        const int t0 = c.j * kT;
+#pragma unroll
+        for (int bx = 0; bx < DIM / 64; ++bx)
+          tma_load_4d_hint(kdst + bx * kBox, &p.tm_k, fb, bx * 64, t0, c.kvh, c.b, kv_policy);
+        if (!SCORES) {
+#pragma unroll
+          for (int bx = 0; bx < DIM / 64; ++bx)
+            tma_load_4d_hint(kdst + kKTileBytes + bx * kBox, &p.tm_v, fb, bx * 64, t0, c.kvh, c.b, kv_policy);
+        }
+        for (long long todo = min(pf_piece, pf_end - pf_next); todo > 0;) {
+          const long long n = min(todo, 32768ll);
+          bulk_prefetch_l2(p.prefetch + pf_next, (uint32_t)n, pf_policy);
+          pf_next += n;
+          todo -= n;
+        }
+        if (with_q) {
+          const uint32_t qdst = smem_u32(q_slots + stage * kFixed.q_slot());
+          const __nv_bfloat16* qsrc = p.q + (long long)c.b * p.q_sb + (long long)(c.kvh * G) * p.q_sh;
+          for (int h = 0; h < G; ++h) bulk_load(qdst + h * kQRow, qsrc + (long long)h * p.q_sh, DIM * 2, fb);
+        }
+      }
+      // Do not leave with copies in flight (only matters if the consumers gave up; the fused
+      // step's consumers wait for these copies before the CTA can end, so it skips this).
+      if (!kFused)
+      for (int k = it > S ? it - S : 0; k < it; ++k)
+        mbar_wait_bounded(full_bar(k % S), (k / S) & 1, p.err, kErrWaitDrain, nullptr,
+                          kWaitLimitNs / 10);
+     }
+     if constexpr (kFused) fused_producer<NPAD, S>(p, ring, bars, it, flags);
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int grp = warp / kGroupWarps;  // consumer group: takes iterations it % kGroups == grp
+    const int wg = warp % kGroupWarps;   // warp in group
+    // merge/output mapping: thread -> (first head tid / DIM, dim tid % DIM), heads step kHStep
+    constexpr int kHStep = kConsumerThreads / DIM;
+    if (!SCORES) {  // empty sequences produce zero rows
+      for (int s = cta; s < B * Hkv; s += gridDim.x) {
+        const int b = s / Hkv;
+        if (lens[b] != 0) continue;
+        const int kvh = s - b * Hkv;
+        for (int h = tid / DIM; h < G; h += kHStep)
+          p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + (tid % DIM)] = __float2bfloat16_rn(0.f);
+      }
+    }
+    uint32_t qf[NB][kKs][2];
+    float o[8][NB][4];
+    float m_run[NB][2], l_run[NB][2];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      m_run[nb][0] = m_run[nb][1] = kNegInf;
+      l_run[nb][0] = l_run[nb][1] = 0.f;
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb) o[mb][nb][0] = o[mb][nb][1] = o[mb][nb][2] = o[mb][nb][3] = 0.f;
+    }
+    // this warp's first token inside a stage, and (D = 256) its 128-dim half of O
+    const int tb = kWide ? (wg >> 1) * 16 : wg * 16;
+    const int dh = kWide ? (wg & 1) : 0;
+    const float sl2 = p.scale_log2;
+    Cursor c;
+    if (start < end) c = cursor_at(start, prefix, B, Hkv);
+    long long seg0 = start;
+    int it = 0;
+    for (long long x = start; x < end; ++x, ++it) {
+      if (x != start) {
+        cursor_next(c, prefix, B, Hkv);
+        if (c.j == 0) seg0 = x;
+      }
+      const bool last = (x == end - 1) || (c.j == c.nt - 1);
+      if (it % kGroups == grp) {
+        const int t0 = c.j * kT;
+        const int vw = min(kT, lens[c.b] - t0) - tb;  // valid tokens of this warp's 16
+        const int stage = it % S;
+        const uint32_t ph = (it / S) & 1;
+        mbar_wait_bounded(full_bar(stage), ph, p.err, kErrWaitFull, flags);
+        if (x - seg0 < kGroups) {  // this group's first tile of the segment carries q
+          const uint8_t* qs = q_slots + stage * kFixed.q_slot();
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+            for (int ks = 0; ks < kKs; ++ks) {
+              const uint8_t* row = qs + (nb * 8 + g) * kQRow + (ks * 16 + 2 * t) * 2;
+              qf[nb][ks][0] = *reinterpret_cast<const uint32_t*>(row);
+              qf[nb][ks][1] = *reinterpret_cast<const uint32_t*>(row + 16);
+            }
+          }
+        }
+        if (vw > 0) {
+          const uint32_t kbase = ring + stage * kStageBytes;
+          // ---- S^T[16 tokens][8*NB heads] = K_tile . Q^T  (fp32, unscaled)
+          float se[NB][4], so[NB][4];
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) se[nb][i] = so[nb][i] = 0.f;
+          {
+            const int row = tb + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int ks = 0; ks < kKs; ++ks) {
+              const int chunk = 2 * (ks & 3) + (lane >> 4);
+              const uint32_t addr = kbase + (ks >> 2) * kBox + row * 128 + ((chunk ^ (lane & 7)) << 4);
+              uint32_t a[4];
+              ldsm_x4(addr, a[0], a[1], a[2], a[3]);
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb) {
+                if (ks & 1) mma_bf16_16816(so[nb], a, qf[nb][ks][0], qf[nb][ks][1]);
+                else mma_bf16_16816(se[nb], a, qf[nb][ks][0], qf[nb][ks][1]);
+              }
+            }
+          }
+          float s[NB][4];
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s[nb][i] = se[nb][i] + so[nb][i];
+          // fragment element i: token g + 8*(i>>1), head 8*nb + 2t + (i&1)
+          if (SCORES) {
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int head = nb * 8 + 2 * t + (i & 1);
+                const int tok = g + 8 * (i >> 1);
+                if (head < G && tok < vw && dh == 0)  // at D = 256 both warps of a pair hold S
+                  p.scores[(long long)c.b * p.s_sb + (long long)(c.kvh * G + head) * p.s_sh + t0 + tb + tok] =
+                      s[nb][i];
+              }
+          } else {
+            const bool v0 = g < vw, v1 = g + 8 < vw;
+            uint32_t pb[NB][2];
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              const float x0 = v0 ? s[nb][0] * sl2 : kNegInf;
+              const float x1 = v0 ? s[nb][1] * sl2 : kNegInf;
+              const float x2 = v1 ? s[nb][2] * sl2 : kNegInf;
+              const float x3 = v1 ? s[nb][3] * sl2 : kNegInf;
+              float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+              for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+              }
+              const float mn0 = fmaxf(m_run[nb][0], mx0), mn1 = fmaxf(m_run[nb][1], mx1);
+              const float al0 = fast_exp2(m_run[nb][0] - mn0), al1 = fast_exp2(m_run[nb][1] - mn1);
+              m_run[nb][0] = mn0;
+              m_run[nb][1] = mn1;
+              const uint32_t r0 = pack_bf16x2(fast_exp2(x0 - mn0), fast_exp2(x1 - mn1));  // token g
+              const uint32_t r1 = pack_bf16x2(fast_exp2(x2 - mn0), fast_exp2(x3 - mn1));  // token g+8
+              // the sum uses the bf16-rounded weights that enter P.V
+              l_run[nb][0] = l_run[nb][0] * al0 + (bf16lo_to_f32(r0) + bf16lo_to_f32(r1));
+              l_run[nb][1] = l_run[nb][1] * al1 + (bf16hi_to_f32(r0) + bf16hi_to_f32(r1));
+#pragma unroll
+              for (int mb = 0; mb < 8; ++mb) {
+                o[mb][nb][0] *= al0;
+                o[mb][nb][1] *= al1;
+                o[mb][nb][2] *= al0;
+                o[mb][nb][3] *= al1;
+              }
+              pb[nb][0] = movmatrix_trans(r0);  // P[head g][tokens 2t, 2t+1]
+              pb[nb][1] = movmatrix_trans(r1);  // P[head g][tokens 2t+8, 2t+9]
+            }
+            // ---- O^T[128 dims (of half dh)][8*NB heads] += V_tile^T . P^T
+            const uint32_t vbase = kbase + kKTileBytes;
+            const int jm = lane >> 3;
+            const int row = tb + (lane & 7) + (jm >> 1) * 8;
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb) {
+              const int chunk = 2 * (mb & 3) + (jm & 1);
+              const uint32_t addr = vbase + (dh * 2 + (mb >> 2)) * kBox + row * 128 + ((chunk ^ (lane & 7)) << 4);
+              uint32_t a[4];
+              ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
+              if (vw < 16) {  // rows past the sequence may hold anything; P is 0 there
+                a[0] = mask_tokens(a[0], 2 * t, vw);
+                a[1] = mask_tokens(a[1], 2 * t, vw);
+                a[2] = mask_tokens(a[2], 2 * t + 8, vw);
+                a[3] = mask_tokens(a[3], 2 * t + 8, vw);
+              }
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(o[mb][nb], a, pb[nb][0], pb[nb][1]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(stage));
+      }
+
+      if (!SCORES && last) {
+        // ---------------------------------------- finish this sequence segment
+        const int b = c.b, kvh = c.kvh, seq = b * Hkv + kvh;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) l_run[nb][cc] += __shfl_xor_sync(0xffffffffu, l_run[nb][cc], off);
+        float* mo = merge_o + wg * HP * kMergeRow;
+        float* ml = merge_ml + wg * HP * 2;
+        // (1) group 1 hands its state to the partner warp of group 0
+        if (grp == 1) {
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            const int h0 = nb * 8 + 2 * t;
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb) {
+              mo[h0 * kMergeRow + mb * 16 + g] = o[mb][nb][0];
+              mo[(h0 + 1) * kMergeRow + mb * 16 + g] = o[mb][nb][1];
+              mo[h0 * kMergeRow + mb * 16 + g + 8] = o[mb][nb][2];
+              mo[(h0 + 1) * kMergeRow + mb * 16 + g + 8] = o[mb][nb][3];
+            }
+            if (g == 0) {
+              ml[h0 * 2] = m_run[nb][0];
+              ml[h0 * 2 + 1] = l_run[nb][0];
+              ml[h0 * 2 + 2] = m_run[nb][1];
+              ml[h0 * 2 + 3] = l_run[nb][1];
+            }
+          }
+        }
+        named_bar_sync(1, kConsumerThreads);
+        // (2) group 0 merges it into registers and publishes the pair's state
+        if (grp == 0) {
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int h = nb * 8 + 2 * t + cc;
+              const float mp = ml[h * 2], lp = ml[h * 2 + 1];
+              const float mn = fmaxf(m_run[nb][cc], mp);
+              const float mref = mn == kNegInf ? 0.f : mn;  // both empty: stay empty
+              const float a_self = fast_exp2(m_run[nb][cc] - mref), a_part = fast_exp2(mp - mref);
+              l_run[nb][cc] = l_run[nb][cc] * a_self + lp * a_part;
+              m_run[nb][cc] = mn;
+#pragma unroll
+              for (int mb = 0; mb < 8; ++mb) {
+                o[mb][nb][cc] = o[mb][nb][cc] * a_self + mo[h * kMergeRow + mb * 16 + g] * a_part;
+                o[mb][nb][cc + 2] = o[mb][nb][cc + 2] * a_self + mo[h * kMergeRow + mb * 16 + g + 8] * a_part;
+              }
+            }
+          }
+          __syncwarp();
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            const int h0 = nb * 8 + 2 * t;
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb) {
+              mo[h0 * kMergeRow + mb * 16 + g] = o[mb][nb][0];
+              mo[(h0 + 1) * kMergeRow + mb * 16 + g] = o[mb][nb][1];
+              mo[h0 * kMergeRow + mb * 16 + g + 8] = o[mb][nb][2];
+              mo[(h0 + 1) * kMergeRow + mb * 16 + g + 8] = o[mb][nb][3];
+            }
+            if (g == 0) {
+              ml[h0 * 2] = m_run[nb][0];
+              ml[h0 * 2 + 1] = l_run[nb][0];
+              ml[h0 * 2 + 2] = m_run[nb][1];
+              ml[h0 * 2 + 3] = l_run[nb][1];
+            }
+          }
+        }
+        named_bar_sync(1, kConsumerThreads);
+
+        // (3) merge the pair states that hold dim d -- all four at D = 128; at D = 256 the
+        //     two of half d / 128 (warps w0 and w0 + 2, whose partners hold the same softmax
+        //     state for the same tokens): thread -> (head, dim)
+        const long long F = prefix[b] + (long long)kvh * c.nt;  // first tile of this sequence
+        const int first_cta = cta_of(F, T, P), last_cta = cta_of(F + c.nt - 1, T, P);
+        const int n_parts = last_cta - first_cta + 1;
+        constexpr int kHold = kWide ? kGroupWarps / 2 : kGroupWarps;  // warps holding a dim
+        constexpr int kWStep = kGroupWarps / kHold;
+        const int d = tid % DIM, dl = d & 127, w0 = kWide ? (d >> 7) : 0;
+        for (int h = tid / DIM; h < G; h += kHStep) {
+          float M = kNegInf;
+#pragma unroll
+          for (int i = 0; i < kHold; ++i) M = fmaxf(M, merge_ml[((w0 + i * kWStep) * HP + h) * 2]);
+          float lsum = 0.f, acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < kHold; ++i) {
+            const int w = w0 + i * kWStep;
+            const float f = fast_exp2(merge_ml[(w * HP + h) * 2] - M);  // 0 for a pair with no tokens
+            lsum += f * merge_ml[(w * HP + h) * 2 + 1];
+            acc += f * merge_o[(w * HP + h) * kMergeRow + dl];
+          }
+          if (n_parts == 1) {
+            p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
+          } else {
+            const long long slot = (long long)cta + seq;
+            p.part_o[(slot * p.gpad + h) * DIM + d] = acc;
+            if (d == 0) {
+              p.part_ml[(slot * p.gpad + h) * 2] = M;
+              p.part_ml[(slot * p.gpad + h) * 2 + 1] = lsum;
+            }
+          }
+        }
+        if (n_parts > 1) {
+          named_bar_sync(1, kConsumerThreads);  // every thread's partial stores precede the release
+          if (tid == 0) flags[1] = (atomic_add_acq_rel_gpu(p.counters + seq, 1) == n_parts - 1);
+          named_bar_sync(1, kConsumerThreads);  // ... and the acquire precedes every thread's loads
+          if (flags[1]) {  // every other part has landed: merge them all
+            // (a) one warp per head: the parts' (m, l) come in together (a lane per part),
+            //     and the normalised weights exp2(m_p - M) / sum go to shared memory
+            float* wpart = merge_o;  // free again: [G][n_parts]
+            for (int h = warp; h < G; h += kGroups * kGroupWarps) {
+              float M = kNegInf;
+              for (int pc = lane; pc < n_parts; pc += 32)
+                M = fmaxf(M, __ldcg(p.part_ml + (((long long)first_cta + pc + seq) * p.gpad + h) * 2));
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+              float lsum = 0.f;
+              for (int pc = lane; pc < n_parts; pc += 32) {
+                const float* ml2 = p.part_ml + (((long long)first_cta + pc + seq) * p.gpad + h) * 2;
+                const float f = fast_exp2(__ldcg(ml2) - M);
+                wpart[h * n_parts + pc] = f;
+                lsum += f * __ldcg(ml2 + 1);
+              }
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+              __syncwarp();
+              for (int pc = lane; pc < n_parts; pc += 32) wpart[h * n_parts + pc] /= lsum;
+            }
+            named_bar_sync(1, kConsumerThreads);
+            // (b) O[h][d] = sum_p w_p O_p[h][d]: the loads of eight parts go out together
+            for (int h = tid / DIM; h < G; h += kHStep) {
+              float acc = 0.f;
+              for (int p0 = 0; p0 < n_parts; p0 += 16) {
+                // clamped (always valid) addresses: sixteen loads in flight, masked afterwards
+                float v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                  const int pc = min(p0 + u, n_parts - 1);
+                  v[u] = __ldcg(p.part_o + (((long long)first_cta + pc + seq) * p.gpad + h) * DIM + d);
+                }
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                  if (p0 + u < n_parts) acc += wpart[h * n_parts + p0 + u] * v[u];
+              }
+              p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc);
+            }
+            if (tid == 0) p.counters[seq] = 0;  // ready for the next call
+          }
+        }
+        named_bar_sync(1, kConsumerThreads);  // merge scratch and flags free again
+        // the next segment starts from an empty state
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          m_run[nb][0] = m_run[nb][1] = kNegInf;
+          l_run[nb][0] = l_run[nb][1] = 0.f;
+#pragma unroll
+          for (int mb = 0; mb < 8; ++mb) o[mb][nb][0] = o[mb][nb][1] = o[mb][nb][2] = o[mb][nb][3] = 0.f;
+        }
+      }
+    }
+    if constexpr (kFused) {
+      // This CTA's attention outputs (its own segments and every merge it performed)
+      // are written: arrive at the grid barrier (release covers all consumer stores).
+      named_bar_sync(1, kConsumerThreads);
+      if (tid == 0) atomic_add_acq_rel_gpu(p.grid_sync, 1);
+      if (warp == kGroupWarps) {  // first warp of group 1 issues the MMAs
+        if (lane == 0) fused_mma<NPAD, S>(p, ring, bars, tmem, flags);
+        __syncwarp();
+      } else if (warp < kGroupWarps) {  // group 0 drains TMEM
+        fused_epilogue<NPAD, S>(p, bars, tmem, flags, warp, lane, tid);
+        tc_fence_before_sync();
+      }
+    }
+  }
+  __syncwarp();
+  __syncthreads();
+  if (kFused && warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int NB, bool SCORES, int S, int NPAD, int DIM>
+cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
+  // The shared-memory opt-in is a per-device function attribute: set it once per device.
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(attn_decode_kernel<NB, SCORES, S, NPAD, DIM>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDynSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = attn_smem_bytes(p.B, NB, S, DIM);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // the fused step's grid barrier needs every CTA resident
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = NPAD > 0 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<NB, SCORES, S, NPAD, DIM>, p);
+}
+
+}  // namespace
+}  // namespace da

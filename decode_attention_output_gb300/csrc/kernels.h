@@ -11,30 +11,41 @@
 namespace da {
 
 // ----------------------------------------------------------- split-KV attention
+// Head dims the kernel implements: 128, and 256 (the two-halves contraction of a
+// D = 256 GQA decode). A stage always holds 32 KB: a K tile and a V tile of
+// tile_tokens(D) tokens x D dims in 64-dim boxes of 128-byte swizzled rows.
 constexpr int kHeadDim = 128;
-constexpr int kTile = 64;                      // tokens per pipeline stage
+constexpr int kHeadDimWide = 256;
+__host__ __device__ constexpr int tile_tokens(int dim) { return dim == kHeadDimWide ? 32 : 64; }
+constexpr int kTile = 64;                      // tokens per pipeline stage at D = 128
 constexpr int kGroupWarps = 4;                 // consumer warps per group; each owns 16 tokens of a stage
 constexpr int kGroups = 2;                     // consumer groups take alternate stages
 constexpr int kConsumerThreads = kGroups * kGroupWarps * 32;
 constexpr int kAttnThreads = kConsumerThreads + 32;  // + one TMA producer warp
 constexpr int kMaxStages = 6;                  // even stage counts: stage s always belongs to group s % 2
-constexpr int kHalfBytes = kTile * 128;        // 64 tokens x 64 dims x bf16 (one 128B-swizzled box)
-constexpr int kKTileBytes = 2 * kHalfBytes;    // 64 tokens x 128 dims
+constexpr int kKTileBytes = 16384;             // K tile: tile_tokens(D) x D x bf16 (both head dims)
 constexpr int kStageBytes = 2 * kKTileBytes;   // K tile + V tile
-constexpr int kQRowBytes = 272;                // 256 B of q + 16 B pad (conflict-free fragment loads)
+__host__ __device__ constexpr int box_bytes(int dim) { return tile_tokens(dim) * 128; }  // 64 dims of a tile
+__host__ __device__ constexpr int q_row_bytes(int dim) { return dim * 2 + 16; }  // + 16 B pad: conflict-free
+                                                                                 // fragment loads
 constexpr int kMaxGroup = 16;
 constexpr int kMaxBatch = 1024;
-constexpr int kMergeRow = 132;                 // floats per head row of the merge scratch (128 + pad)
+constexpr int kMergeRow = 132;                 // floats per head row of the merge scratch (128 + pad); at
+                                               // D = 256 a warp holds one 128-dim half of the output
 constexpr int kMaxAttnCtas = 512;              // parts per sequence stay <= this: the cross-CTA merge
                                                // keeps G x parts weights in the 4*8*nb*kMergeRow scratch
 static_assert(kMaxAttnCtas <= kGroupWarps * kMergeRow, "merge weights must fit the merge scratch");
+static_assert(tile_tokens(kHeadDim) * kHeadDim * 2 == kKTileBytes, "K tile bytes at D = 128");
+static_assert(tile_tokens(kHeadDimWide) * kHeadDimWide * 2 == kKTileBytes, "K tile bytes at D = 256");
 // Shared-memory carve-up of the attention kernel; nb = 8-head blocks (1 or 2),
-// stages = pipeline depth (even, so that a stage always belongs to one consumer group).
+// stages = pipeline depth (even, so that a stage always belongs to one consumer group),
+// dim = head dim (128 or 256).
 struct AttnSmem {
-  int nb, batch, stages;
-  __host__ __device__ constexpr AttnSmem(int nb_, int batch_, int stages_) : nb(nb_), batch(batch_), stages(stages_) {}
+  int nb, batch, stages, dim;
+  __host__ __device__ constexpr AttnSmem(int nb_, int batch_, int stages_, int dim_ = kHeadDim)
+      : nb(nb_), batch(batch_), stages(stages_), dim(dim_) {}
   __host__ __device__ constexpr int heads() const { return 8 * nb; }
-  __host__ __device__ constexpr size_t q_slot() const { return (size_t)heads() * kQRowBytes; }
+  __host__ __device__ constexpr size_t q_slot() const { return (size_t)heads() * q_row_bytes(dim); }
   __host__ __device__ constexpr size_t off_q() const { return (size_t)stages * kStageBytes; }
   __host__ __device__ constexpr size_t off_merge_o() const { return off_q() + stages * q_slot(); }
   __host__ __device__ constexpr size_t off_merge_ml() const {
@@ -49,25 +60,29 @@ struct AttnSmem {
 };
 
 constexpr size_t kMaxDynSmem = 232448;  // 227 KB per CTA on sm_100-class GPUs
-constexpr size_t attn_smem_bytes(int batch, int nb, int stages) { return AttnSmem(nb, batch, stages).total(); }
+constexpr size_t attn_smem_bytes(int batch, int nb, int stages, int dim = kHeadDim) {
+  return AttnSmem(nb, batch, stages, dim).total();
+}
 static_assert(AttnSmem(2, kMaxBatch, 4).total() <= kMaxDynSmem, "attention kernel exceeds 227 KB of shared memory");
+static_assert(AttnSmem(2, kMaxBatch, 4, kHeadDimWide).total() <= kMaxDynSmem,
+              "attention kernel (D = 256) exceeds 227 KB of shared memory");
 // 4 stages by default (measured faster than 6 on the GB300: deeper rings slowed the
-// stream); 6 on request when it fits this batch and group width.
+// stream); 6 on request when it fits this batch and group width (D = 128 only).
 constexpr int attn_stages_for(int batch, int nb, int requested) {
   return requested == kMaxStages && attn_smem_bytes(batch, nb, kMaxStages) <= kMaxDynSmem ? kMaxStages : 4;
 }
 
 struct AttnParams {
-  CUtensorMap tm_k;  // [B][Hkv][Lcap][128] bf16, box 64 dims x 64 tokens, 128B swizzle
+  CUtensorMap tm_k;  // [B][Hkv][Lcap][D] bf16, box 64 dims x tile_tokens(D) tokens, 128B swizzle
   CUtensorMap tm_v;
   const __nv_bfloat16* q;
-  long long q_sb, q_sh;  // element strides of q [B][Hq][128]
+  long long q_sb, q_sh;  // element strides of q [B][Hq][D]
   const int* seq_lens;
-  __nv_bfloat16* attn;   // [B][Hq][128] bf16 result
+  __nv_bfloat16* attn;   // [B][Hq][D] bf16 result
   long long a_sb, a_sh;
   float* scores;         // [B][Hq][Lcap] fp32 (scores-only mode)
   long long s_sb, s_sh;
-  float* part_o;         // [slots][gpad][128] unnormalised partial outputs
+  float* part_o;         // [slots][gpad][D] unnormalised partial outputs
   float* part_ml;        // [slots][gpad][2]   (running max in log2 units, sum)
   int* counters;         // [B*Hkv] completion counters (zero between calls)
   int* err;              // device error word
@@ -100,11 +115,14 @@ __host__ __device__ constexpr int proj_stages(int npad) {
   return (4 * kStageBytes) / proj_stage_bytes(npad) < 8 ? (4 * kStageBytes) / proj_stage_bytes(npad) : 8;
 }
 
-// grid = number of persistent CTAs; nb = 1 for G <= 8, 2 for G <= 16; npad = 0 for the
-// attention alone, else the batch padding (16/32/64/128) of the fused projection
-// (a cooperative launch: every CTA must be resident for the grid barrier).
-cudaError_t launch_attention(const AttnParams& p, int grid, int nb, bool scores_only, cudaStream_t stream,
+// grid = number of persistent CTAs; nb = 1 for G <= 8, 2 for G <= 16; dim = head dim
+// (128 or 256); npad = 0 for the attention alone, else the batch padding (16/32/64/128)
+// of the fused projection (a cooperative launch: every CTA must be resident for the
+// grid barrier; D = 128 only).
+cudaError_t launch_attention(const AttnParams& p, int grid, int nb, int dim, bool scores_only, cudaStream_t stream,
                              int npad = 0);
+// The D = 256 instantiations (their own translation unit).
+cudaError_t launch_attention_d256(const AttnParams& p, int grid, int nb, bool scores_only, cudaStream_t stream);
 
 // ------------------------------------------------------- projection: GEMV path
 constexpr int kGemvThreads = 256;

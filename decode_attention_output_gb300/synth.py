@@ -6,10 +6,10 @@ oracle's callers share.
 
 Recipe (every tensor drawn in fp32 from its own generator, then rounded to
 bf16 round-to-nearest-even by ``Tensor.to(torch.bfloat16)``):
-  q        [B, Hq, 128]        ~ N(0, 1)                         seed + 1
-  k_cache  [B, Hkv, Lcap, 128] ~ N(0, 1) * k_mult               seed + 2
-  v_cache  [B, Hkv, Lcap, 128] ~ N(0, 1)                         seed + 3
-  o_weight [Hq*128, N]         ~ N(0, 1 / (Hq*128))              seed + 4
+  q        [B, Hq, D]          ~ N(0, 1)                         seed + 1
+  k_cache  [B, Hkv, Lcap, D]   ~ N(0, 1) * k_mult               seed + 2
+  v_cache  [B, Hkv, Lcap, D]   ~ N(0, 1)                         seed + 3
+  o_weight [Hq*D, N]           ~ N(0, 1 / (Hq*D))                seed + 4
   seq_lens [B] int32: all Lcap, or uniform integers in [lo, hi]  seed + 5 (CPU)
 The caches are contiguous; positions t >= seq_lens[b] are filled like the rest.
 Draws on a CUDA device use that device's generator, so the values differ from a
@@ -23,7 +23,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-HEAD_DIM = 128
+HEAD_DIM = 128  # the default head dim D
 
 
 @dataclass(frozen=True)
@@ -39,6 +39,7 @@ class Workload:
     ragged_hi: int = 0
     k_mult: float = 1.0
     fixed_lens: tuple = field(default=())  # explicit lengths (tests)
+    D: int = HEAD_DIM                      # head dim: 128 or 256
 
     @property
     def G(self) -> int:
@@ -46,14 +47,16 @@ class Workload:
 
     @property
     def scale(self) -> float:
-        return 1.0 / math.sqrt(HEAD_DIM)
+        return 1.0 / math.sqrt(self.D)
 
     @property
     def w_std(self) -> float:
-        return 1.0 / math.sqrt(self.Hq * HEAD_DIM)
+        return 1.0 / math.sqrt(self.Hq * self.D)
 
 
-# The five synthetic decode workloads: GQA decode shapes with hidden = Hq * 128.
+# The synthetic decode workloads: GQA decode shapes (o_weight is [Hq * D, N]). The
+# last one has head dim 256 (QK^T contracting D in two 128-wide halves), with the
+# other sizes of the batch-8 case.
 WORKLOADS = {
     "b1_h32x8_l2k": Workload("b1_h32x8_l2k", B=1, Hq=32, Hkv=8, Lcap=2048, N=4096),
     "b8_h32x8_l8k": Workload("b8_h32x8_l8k", B=8, Hq=32, Hkv=8, Lcap=8192, N=4096),
@@ -61,6 +64,7 @@ WORKLOADS = {
                                     ragged_lo=512, ragged_hi=32768, k_mult=2.0),
     "b64_h64x8_l16k": Workload("b64_h64x8_l16k", B=64, Hq=64, Hkv=8, Lcap=16384, N=8192),
     "b4_h32x8_l128k": Workload("b4_h32x8_l128k", B=4, Hq=32, Hkv=8, Lcap=131072, N=4096),
+    "b8_h32x8_d256_l8k": Workload("b8_h32x8_d256_l8k", B=8, Hq=32, Hkv=8, Lcap=8192, N=4096, D=256),
 }
 ORDER = list(WORKLOADS)
 
@@ -98,10 +102,10 @@ def _randn_bf16(shape, device, seed: int, mult: float = 1.0) -> torch.Tensor:
 def make_inputs(w: Workload, seed: int = 0, device="cpu") -> dict:
     """All inputs of one decode step for workload ``w`` on ``device``."""
     return {
-        "q": _randn_bf16((w.B, w.Hq, HEAD_DIM), device, seed + 1),
-        "k_cache": _randn_bf16((w.B, w.Hkv, w.Lcap, HEAD_DIM), device, seed + 2, w.k_mult),
-        "v_cache": _randn_bf16((w.B, w.Hkv, w.Lcap, HEAD_DIM), device, seed + 3),
-        "o_weight": _randn_bf16((w.Hq * HEAD_DIM, w.N), device, seed + 4, w.w_std),
+        "q": _randn_bf16((w.B, w.Hq, w.D), device, seed + 1),
+        "k_cache": _randn_bf16((w.B, w.Hkv, w.Lcap, w.D), device, seed + 2, w.k_mult),
+        "v_cache": _randn_bf16((w.B, w.Hkv, w.Lcap, w.D), device, seed + 3),
+        "o_weight": _randn_bf16((w.Hq * w.D, w.N), device, seed + 4, w.w_std),
         "seq_lens": seq_lens_for(w, seed).to(device),
         "scale": w.scale,
     }
@@ -111,9 +115,9 @@ def algorithmic_bytes(w: Workload, seq_lens) -> dict:
     """Bytes the step must move at least once: K and V of the valid tokens, W_o,
     q and out (bf16). Returned per part and in total."""
     lens = [int(x) for x in seq_lens]
-    kv = 2 * w.Hkv * HEAD_DIM * 2 * sum(min(max(L, 0), w.Lcap) for L in lens)
-    wo = w.Hq * HEAD_DIM * w.N * 2
-    qo = w.B * w.Hq * HEAD_DIM * 2 + w.B * w.N * 2
+    kv = 2 * w.Hkv * w.D * 2 * sum(min(max(L, 0), w.Lcap) for L in lens)
+    wo = w.Hq * w.D * w.N * 2
+    qo = w.B * w.Hq * w.D * 2 + w.B * w.N * 2
     return {"kv": kv, "w_o": wo, "q_out": qo, "total": kv + wo + qo}
 
 

@@ -102,6 +102,10 @@ BAD_FWD = [
     ("lens_dtype", dict(lens=desc([2], binding.DA_DTYPE_F32)), DTYPE),
     ("head_dim_64", dict(q=desc([2, 8, 64])), SHAPE),
     ("kv_head_dim_64", dict(k=desc([2, 2, 64, 64]), v=desc([2, 2, 64, 64])), SHAPE),
+    ("head_dim_192", dict(q=desc([2, 8, 192]), k=desc([2, 2, 64, 192]), v=desc([2, 2, 64, 192]),
+                          w=desc([8 * 192, 256])), SHAPE),
+    ("q_256_cache_128", dict(q=desc([2, 8, 256]), w=desc([8 * 256, 256])), SHAPE),
+    ("d256_w_rows_for_128", dict(q=desc([2, 8, 256]), k=desc([2, 2, 64, 256]), v=desc([2, 2, 64, 256])), SHAPE),
     ("heads_not_multiple", dict(q=desc([2, 6, 128]), k=desc([2, 4, 64, 128]), v=desc([2, 4, 64, 128]),
                                 w=desc([6 * 128, 256])), SHAPE),
     ("group_32", dict(q=desc([2, 64, 128]), w=desc([64 * 128, 256])), UNSUP),

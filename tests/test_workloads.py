@@ -1,4 +1,4 @@
-"""The five synthetic decode workloads at full size, run exactly as bench.py runs
+"""The synthetic decode workloads at full size, run exactly as bench.py runs
 them (default plan, one decode_attn_fwd call), checked on sampled batch rows the
 oracle recomputes one by one: every attention head and every output column of
 each sampled row, with the same tolerances as the small cases. Properties that
@@ -35,7 +35,7 @@ def test_workload_sampled_rows(orc, name):
     x = synth.make_inputs(w, seed=0, device=DEV)
     out = torch.full((w.B, w.N), float("nan"), dtype=torch.bfloat16, device=DEV)
     da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out, x["scale"])
-    attn = torch.full((w.B, w.Hq, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    attn = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device=DEV)
     da.decode_attn_only(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], attn, x["scale"])
     torch.cuda.synchronize()
     assert da.decode_attn_device_error() == 0
@@ -43,7 +43,7 @@ def test_workload_sampled_rows(orc, name):
     # the whole step agrees with projecting the attention-only result (split-K orders
     # may differ, so within the bf16 tolerance rather than bit for bit)
     out2 = torch.empty_like(out)
-    da.decode_attn_oproj(attn.view(w.B, w.Hq * 128), x["o_weight"], out2)
+    da.decode_attn_oproj(attn.view(w.B, w.Hq * w.D), x["o_weight"], out2)
     torch.cuda.synchronize()
     assert_bf16_close(f64(out), f64(out2), f"{name} fused vs two-launch")
 
