@@ -15,7 +15,9 @@
  * and the shapes of its table "三个 Matmul 的 Shape 特征分析" (QK^T: M = query
  * heads per KV head, K = head_dim = 128, N = kv_len; attn.V: M = heads per KV
  * head, K = kv_len, N = 128; output_proj: M = batch, K = heads * 128,
- * N = hidden).
+ * N = hidden). Head dim 256 is the page's other GQA decode (section "仓库源码
+ * 佐证": QK^T contracts D = 256 in two halves of 128, attn.V has N = D = 256);
+ * every entry point takes D = 128 or D = 256, read from q's last extent.
  *
  * Conventions shared by every entry point
  *  - Every tensor argument is a da_tensor_t descriptor. Its data pointer is a
@@ -77,7 +79,8 @@ typedef enum {
 } da_status_t;
 
 /* Limits checked on the host. */
-#define DA_HEAD_DIM 128  /* D: the only head_dim the kernels implement */
+#define DA_HEAD_DIM 128      /* D: the default head dim */
+#define DA_HEAD_DIM_WIDE 256 /* D: the other head dim the kernels implement */
 #define DA_MAX_GROUP 16  /* G = Hq / Hkv */
 #define DA_MAX_BATCH 1024
 
@@ -86,16 +89,17 @@ typedef enum {
  * Page: "PyPTO 开箱性能调优实战 Decode Attention 多 Matmul 独立 TileShape 配置
  * F-16", section "代码对比" (the three matmuls) and the shape table.
  *
- *   q        [B, Hq, 128]        bf16  the new token's queries
- *   k_cache  [B, Hkv, Lcap, 128] bf16  keys; token t of sequence b is row t
- *   v_cache  [B, Hkv, Lcap, 128] bf16  values, same shape as k_cache
+ *   q        [B, Hq, D]          bf16  the new token's queries, D = 128 or 256
+ *   k_cache  [B, Hkv, Lcap, D]   bf16  keys; token t of sequence b is row t
+ *   v_cache  [B, Hkv, Lcap, D]   bf16  values, same shape as k_cache
  *   seq_lens [B]                 int32 valid tokens per sequence (device)
- *   o_weight [Hq*128, N]         bf16  row-major; row k = h*128 + d
+ *   o_weight [Hq*D, N]           bf16  row-major; row k = h*D + d
  *   out      [B, N]              bf16  written
- *   scale    softmax scale applied to the fp32 scores (usually 1/sqrt(128))
+ *   scale    softmax scale applied to the fp32 scores (usually 1/sqrt(D))
  *
  * Query head h attends with KV head h / (Hq / Hkv) over tokens t < seq_lens[b].
- * Requires Hq % Hkv == 0, Hq / Hkv <= 16, B <= 1024, N % 8 == 0.
+ * Requires Hq % Hkv == 0, Hq / Hkv <= 16, B <= 1024, N % 8 == 0; any other D
+ * returns DA_ERR_SHAPE.
  * Returns DA_OK or a negative da_status_t.
  */
 int decode_attn_fwd(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
@@ -106,7 +110,7 @@ int decode_attn_fwd(const da_tensor_t* q, const da_tensor_t* k_cache, const da_t
  * decode_attn_only -- the attention half: attn_out[b, h, :] =
  * softmax(scale * q[b,h] . K[b, h/G]^T) . V[b, h/G] over t < seq_lens[b],
  * written as bf16 (the page's `attn_output`, DT_BF16).
- *   attn_out [B, Hq, 128] bf16, caller-allocated, any strides obeying the
+ *   attn_out [B, Hq, D] bf16, caller-allocated, any strides obeying the
  *   conventions. Other arguments as decode_attn_fwd.
  */
 int decode_attn_only(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
@@ -127,7 +131,8 @@ int decode_attn_only(const da_tensor_t* q, const da_tensor_t* k_cache, const da_
  * allocating routine is called. The split-KV partials need one slot per
  * (sequence, KV head) pair plus one per persistent CTA: on a 152-SM GB300 with
  * the default grid that allows B*Hkv up to 1738 when Hq/Hkv <= 8 and up to 793
- * when Hq/Hkv <= 16. A larger call returns DA_ERR_SCRATCH and launches nothing.
+ * when Hq/Hkv <= 16 at D = 128; at D = 256 up to 800 and 324. A larger call
+ * returns DA_ERR_SCRATCH and launches nothing.
  *
  * - The first call on a device looks up the array's device address (no
  *   allocation); make that first call before any stream capture.
@@ -177,11 +182,12 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *                   projection reads o_weight from L2 (measured slower on GB300:
  *                   the prefetch competes with the K/V stream)
  *   "attn_stages"   4 (default) or 6: depth of the attention kernel's K/V ring
- *                   (6 only when it fits in shared memory for the batch)
+ *                   (6 only at D = 128 and when it fits in shared memory for the batch)
  *   "fused"         0 (default): decode_attn_fwd runs two launches (attention,
  *                   projection); 1: one persistent cooperative launch (attention,
  *                   a bounded grid barrier, tcgen05 projection) when batch <= 128
- *                   (correct, but measured slower on GB300 so far)
+ *                   (correct, but measured slower on GB300 so far); head dim 128
+ *                   only: at D = 256 decode_attn_fwd always takes two launches
  *   "fused_attn_ctas" attention workers of the fused step (0: about four 64-token
  *                   tiles each, at most one per SM; the other CTAs start on o_weight)
  * Returns DA_OK or DA_ERR_OPTION.
