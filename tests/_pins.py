@@ -127,6 +127,39 @@ def pin_bruteforce_whole_step(orc):
     _close(y, by, 1e-13, "output vs brute force")
 
 
+def pin_bruteforce_whole_step_d256(orc):
+    """Head dim 256 (the page's other GQA decode): oracle == 60-digit brute force."""
+    rng = np.random.default_rng(31)
+    D2 = 256
+    B, Hq, Hkv, Lcap, N = 1, 2, 1, 3, 8
+    q = rand_bits(rng, (B, Hq, D2))
+    k = rand_bits(rng, (B, Hkv, Lcap, D2))
+    v = rand_bits(rng, (B, Hkv, Lcap, D2))
+    w = rand_bits(rng, (Hq * D2, N), std=1 / math.sqrt(Hq * D2))
+    lens = np.array([3], np.int32)
+    scale = 1 / math.sqrt(D2)
+    attn, y = orc.decode(q, k, v, lens, w, scale)
+    ba, by = brute_decode(bits_to_f64(q), bits_to_f64(k), bits_to_f64(v), lens, bits_to_f64(w), scale)
+    _close(attn, ba, 1e-13, "attention (D=256) vs brute force")
+    _close(y, by, 1e-13, "output (D=256) vs brute force")
+
+
+def pin_integer_scores_exact_d256(orc):
+    """Integer q, k at head dim 256: scores equal the int64 matmul over all 256 dims
+    (a contraction that stopped at 128 would differ)."""
+    rng = np.random.default_rng(32)
+    B, Hq, Hkv, Lcap = 1, 4, 2, 5
+    G = Hq // Hkv
+    qi = rng.integers(-4, 5, size=(B, Hq, 256))
+    ki = rng.integers(-4, 5, size=(B, Hkv, Lcap, 256))
+    lens = np.array([5], np.int32)
+    s = orc.scores(to_bf16_bits(qi.astype(np.float32)), to_bf16_bits(ki.astype(np.float32)), lens)
+    for h in range(Hq):
+        ref = ki[0, h // G] @ qi[0, h]
+        assert np.array_equal(s[0, h], ref.astype(np.float64)), f"scores (D=256) h={h}"
+        assert not np.array_equal(ref, ki[0, h // G, :, :128] @ qi[0, h, :128]), "test needs both halves"
+
+
 def pin_bruteforce_group(orc):
     """One group of G = 3 heads over 7 keys, unusual scale: group_attention == brute force."""
     rng = np.random.default_rng(12)
