@@ -21,8 +21,8 @@ DA_DTYPE_BF16, DA_DTYPE_F32, DA_DTYPE_I32 = 1, 2, 3
 _DTYPES = {torch.bfloat16: DA_DTYPE_BF16, torch.float32: DA_DTYPE_F32, torch.int32: DA_DTYPE_I32}
 
 # every symbol declared in include/decode_attn.h
-EXPORTS = ("decode_attn_fwd", "decode_attn_only", "decode_attn_only_noalloc", "decode_attn_scores", "decode_attn_oproj",
-           "decode_attn_set_option", "decode_attn_get_option", "decode_attn_device_error",
+EXPORTS = ("decode_attn_fwd", "decode_attn_only", "decode_attn_only_noalloc", "decode_attn_fwd_paged",
+           "decode_attn_only_paged", "decode_attn_scores", "decode_attn_oproj", "decode_attn_set_option", "decode_attn_get_option", "decode_attn_device_error",
            "decode_attn_release", "decode_attn_status_str")
 
 
@@ -55,6 +55,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             lib.decode_attn_fwd.argtypes = [P, P, P, P, P, P, f32, vp]
             lib.decode_attn_only.argtypes = [P, P, P, P, P, f32, vp]
             lib.decode_attn_only_noalloc.argtypes = [P, P, P, P, P, f32, vp]
+            lib.decode_attn_fwd_paged.argtypes = [P, P, P, P, P, P, P, f32, vp]
+            lib.decode_attn_only_paged.argtypes = [P, P, P, P, P, P, f32, vp]
             lib.decode_attn_scores.argtypes = [P, P, P, P, vp]
             lib.decode_attn_oproj.argtypes = [P, P, P, vp]
             lib.decode_attn_set_option.argtypes = [ctypes.c_char_p, i64]
@@ -119,7 +121,7 @@ def decode_attn_fwd(q, k_cache, v_cache, seq_lens, o_weight, out, scale: float, 
 
 
 def decode_attn_only(q, k_cache, v_cache, seq_lens, attn_out, scale: float, stream=None) -> torch.Tensor:
-    """attn_out[B, Hq, 128] = softmax(scale * q K^T) V (bf16); returns ``attn_out``."""
+    """attn_out[B, Hq, D] = softmax(scale * q K^T) V (bf16); returns ``attn_out``."""
     lib = load()
     ds = [describe(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
     _check("decode_attn_only", lib.decode_attn_only(*[_ref(d) for d in ds], float(scale), _stream(stream)))
@@ -136,6 +138,26 @@ def decode_attn_only_noalloc(q, k_cache, v_cache, seq_lens, attn_out, scale: flo
     ds = [describe(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
     _check("decode_attn_only_noalloc",
            lib.decode_attn_only_noalloc(*[_ref(d) for d in ds], float(scale), _stream(stream)))
+    return attn_out
+
+
+def decode_attn_fwd_paged(q, k_pages, v_pages, block_table, seq_lens, o_weight, out, scale: float,
+                          stream=None) -> torch.Tensor:
+    """decode_attn_fwd over a paged cache: k_pages / v_pages [num_blocks, Hkv, block_size, D],
+    block_table [B, max_blocks] int32; returns ``out``."""
+    lib = load()
+    ds = [describe(x) for x in (q, k_pages, v_pages, block_table, seq_lens, o_weight, out)]
+    _check("decode_attn_fwd_paged", lib.decode_attn_fwd_paged(*[_ref(d) for d in ds], float(scale), _stream(stream)))
+    return out
+
+
+def decode_attn_only_paged(q, k_pages, v_pages, block_table, seq_lens, attn_out, scale: float,
+                           stream=None) -> torch.Tensor:
+    """decode_attn_only over a paged cache (see decode_attn_fwd_paged); returns ``attn_out``."""
+    lib = load()
+    ds = [describe(x) for x in (q, k_pages, v_pages, block_table, seq_lens, attn_out)]
+    _check("decode_attn_only_paged",
+           lib.decode_attn_only_paged(*[_ref(d) for d in ds], float(scale), _stream(stream)))
     return attn_out
 
 

@@ -124,8 +124,9 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 4-D map over a [B][Hkv][Lcap][D] bf16 cache; box = 64 dims x tile_tokens(D) tokens.
-int encode_kv_map(CUtensorMap* map, const da_tensor_t* t) {
+// 4-D map over a [B][Hkv][Lcap][D] bf16 cache (or a [num_blocks][Hkv][block_size][D]
+// page pool); box = 64 dims x box_tokens tokens (0: tile_tokens(D)).
+int encode_kv_map(CUtensorMap* map, const da_tensor_t* t, int box_tokens = 0) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return DA_ERR_CUDA;
   const int64_t B = t->shape[0], H = t->shape[1], L = t->shape[2], D = t->shape[3];
@@ -135,7 +136,7 @@ int encode_kv_map(CUtensorMap* map, const da_tensor_t* t) {
   const int64_t sb = B == 1 ? sh * H : t->stride[0];
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)H, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)st * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)tile_tokens((int)D), 1, 1};
+  cuuint32_t box[4] = {64, (cuuint32_t)(box_tokens > 0 ? box_tokens : tile_tokens((int)D)), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -232,6 +233,62 @@ int check_attention_inputs(const da_tensor_t* q, const da_tensor_t* k, const da_
   s->G = (int)(Hq / Hkv);
   s->Lcap = (int)Lcap;
   s->D = (int)D;
+  return DA_OK;
+}
+
+// A paged cache: k_pages / v_pages [num_blocks][Hkv][block_size][D] bf16 (any strides obeying
+// the conventions), block_table [B][max_blocks] int32 (rows contiguous), seq_lens [B].
+// The logical capacity is max_blocks * block_size.
+struct PagedShape {
+  const int* table;
+  long long table_stride;
+  int block_size, num_blocks;
+};
+
+int check_paged_inputs(const da_tensor_t* q, const da_tensor_t* kp, const da_tensor_t* vp,
+                       const da_tensor_t* table, const da_tensor_t* lens, AttnShape* s, PagedShape* ps) {
+  DA_TRY(check_tensor(q, DA_DTYPE_BF16, 3, kInput16));
+  DA_TRY(check_tensor(kp, DA_DTYPE_BF16, 4, kInput16));
+  DA_TRY(check_tensor(vp, DA_DTYPE_BF16, 4, kInput16));
+  if (!table || !lens) return DA_ERR_NULL;
+  if (table->dtype != DA_DTYPE_I32 || lens->dtype != DA_DTYPE_I32) return DA_ERR_DTYPE;
+  if (table->ndim != 2 || lens->ndim != 1) return DA_ERR_SHAPE;
+  const int64_t B = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+  const int64_t NB = kp->shape[0], Hkv = kp->shape[1], BS = kp->shape[2], MB = table->shape[1];
+  if (D != kHeadDim && D != kHeadDimWide) return DA_ERR_SHAPE;
+  if (kp->shape[3] != D) return DA_ERR_SHAPE;
+  for (int i = 0; i < 4; ++i)
+    if (vp->shape[i] != kp->shape[i]) return DA_ERR_SHAPE;
+  if (table->shape[0] != B || lens->shape[0] != B) return DA_ERR_SHAPE;
+  if (Hq <= 0 || Hkv <= 0 || NB <= 0 || BS <= 0 || MB <= 0) return DA_ERR_SHAPE;
+  if (Hq % Hkv) return DA_ERR_SHAPE;
+  if (!paged_block_ok((int)std::min<int64_t>(BS, 1 << 30), (int)D)) return DA_ERR_UNSUPPORTED;
+  if (Hq / Hkv > kMaxGroup) return DA_ERR_UNSUPPORTED;
+  if (B > DA_MAX_BATCH) return DA_ERR_UNSUPPORTED;
+  if (B * Hkv > (int64_t)kMaxCounters) return DA_ERR_UNSUPPORTED;
+  if (NB >= ((int64_t)1 << 31) || BS > ((int64_t)1 << 20)) return DA_ERR_UNSUPPORTED;
+  const int64_t Lcap = MB * BS;
+  if (MB > ((int64_t)1 << 30) || Lcap > ((int64_t)1 << 30)) return DA_ERR_UNSUPPORTED;
+  const int64_t tt = tile_tokens((int)D);
+  if (B * Hkv * ((Lcap + tt - 1) / tt) >= ((int64_t)1 << 31)) return DA_ERR_UNSUPPORTED;
+  if (B > 0) {
+    if (!lens->data || !table->data) return DA_ERR_NULL;
+    if (B > 1 && lens->stride[0] != 1) return DA_ERR_STRIDE;
+    if (MB > 1 && table->stride[1] != 1) return DA_ERR_STRIDE;
+    if (B > 1 && table->stride[0] < MB) return DA_ERR_STRIDE;
+    if (reinterpret_cast<uintptr_t>(lens->data) % 4 || reinterpret_cast<uintptr_t>(table->data) % 4)
+      return DA_ERR_ALIGN;
+  }
+  s->B = (int)B;
+  s->Hq = (int)Hq;
+  s->Hkv = (int)Hkv;
+  s->G = (int)(Hq / Hkv);
+  s->Lcap = (int)Lcap;
+  s->D = (int)D;
+  ps->table = static_cast<const int*>(table->data);
+  ps->table_stride = B > 1 ? table->stride[0] : MB;
+  ps->block_size = (int)BS;
+  ps->num_blocks = (int)NB;
   return DA_OK;
 }
 
@@ -411,7 +468,7 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
                   const AttnShape& s, const AttnPlan& pl, char* ws, char* scratch, __nv_bfloat16* attn,
                   long long a_sb, long long a_sh, float* scores, long long s_sb, long long s_sh, float scale,
                   cudaStream_t stream, const void* prefetch = nullptr, long long prefetch_bytes = 0,
-                  const FusedArgs* fused = nullptr) {
+                  const FusedArgs* fused = nullptr, const PagedShape* paged = nullptr) {
   AttnParams p;
   memset(&p, 0, sizeof(p));
   if (fused) {
@@ -428,9 +485,16 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
     p.units = fused->plan->units;
   }
 
-  DA_TRY(encode_kv_map(&p.tm_k, k));
-  if (v) DA_TRY(encode_kv_map(&p.tm_v, v));
+  const int box_tokens = paged ? std::min(paged->block_size, tile_tokens(s.D)) : 0;
+  DA_TRY(encode_kv_map(&p.tm_k, k, box_tokens));
+  if (v) DA_TRY(encode_kv_map(&p.tm_v, v, box_tokens));
   else p.tm_v = p.tm_k;
+  if (paged) {
+    p.block_table = paged->table;
+    p.bt_stride = paged->table_stride;
+    p.block_size = paged->block_size;
+    p.num_blocks = paged->num_blocks;
+  }
   p.q = static_cast<const __nv_bfloat16*>(q->data);
   p.q_sb = q->stride[0];
   p.q_sh = q->stride[1];
@@ -456,12 +520,74 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
   p.prefetch = static_cast<const char*>(prefetch);
   p.prefetch_bytes = prefetch ? (prefetch_bytes & ~15ll) : 0;
   const cudaError_t e =
-      launch_attention(p, pl.grid, pl.nb, s.D, scores != nullptr, stream, fused ? fused->plan->npad : 0);
+      paged ? launch_attention_paged(p, pl.grid, pl.nb, s.D, stream)
+            : launch_attention(p, pl.grid, pl.nb, s.D, scores != nullptr, stream, fused ? fused->plan->npad : 0);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
     cudaGetLastError();
     return DA_ERR_UNSUPPORTED;  // the caller falls back to two launches
   }
   return e == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+// decode_attn_only / decode_attn_only_paged after their input checks.
+int only_checked(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t* v, const da_tensor_t* seq_lens,
+                 const da_tensor_t* attn_out, float scale, void* stream, const AttnShape& s,
+                 const PagedShape* paged) {
+  DA_TRY(check_tensor(attn_out, DA_DTYPE_BF16, 3, kOutput));
+  if (attn_out->shape[0] != s.B || attn_out->shape[1] != s.Hq || attn_out->shape[2] != s.D)
+    return DA_ERR_SHAPE;
+  if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
+  if (s.B == 0) return DA_OK;
+  const Options o = options_snapshot();
+  const AttnPlan pl = plan_attention(s, o);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = nullptr;
+  DA_TRY(workspace_get(pl.bytes, st, &ws));
+  return run_attention(q, k, v, seq_lens, s, pl, ws, ws + kHeaderBytes,
+                       static_cast<__nv_bfloat16*>(attn_out->data), attn_out->stride[0], attn_out->stride[1],
+                       nullptr, 0, 0, scale, st, nullptr, 0, nullptr, paged);
+}
+
+// decode_attn_fwd / decode_attn_fwd_paged after their input checks. The fused step is
+// built for a contiguous cache at head dim 128; everything else takes two launches.
+int fwd_checked(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
+                const da_tensor_t* seq_lens, const da_tensor_t* o_weight, const da_tensor_t* out, float scale,
+                void* stream, const AttnShape& s, const PagedShape* paged) {
+  DA_TRY(check_tensor(o_weight, DA_DTYPE_BF16, 2, kInput16));
+  DA_TRY(check_tensor(out, DA_DTYPE_BF16, 2, kOutput));
+  const int64_t K = (int64_t)s.Hq * s.D, N = o_weight->shape[1];
+  if (o_weight->shape[0] != K || out->shape[0] != s.B || out->shape[1] != N) return DA_ERR_SHAPE;
+  if (N <= 0 || N % 8) return DA_ERR_SHAPE;
+  if (N > (1 << 30) || K > (1 << 30)) return DA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
+  if (s.B == 0) return DA_OK;
+  const Options o = options_snapshot();
+  const AttnPlan ap = plan_attention(s, o);
+  const size_t attn_bytes = align_up((size_t)s.B * K * 2, 256);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const FusedPlan fp = paged ? FusedPlan() : plan_fused(s, (int)K, (int)N, ap, o);
+  if (fp.ok) {  // one launch: attention, grid barrier, projection
+    char* ws = nullptr;
+    DA_TRY(workspace_get(ap.bytes + attn_bytes + fp.part_bytes, st, &ws));
+    char* scratch = ws + kHeaderBytes;
+    __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(scratch + ap.bytes);
+    const FusedArgs fa{&fp, o_weight, out, reinterpret_cast<float*>(scratch + ap.bytes + attn_bytes), (int)K, (int)N};
+    const long long w_span = ((long long)(K - 1) * o_weight->stride[0] + N) * 2;
+    const int rc = run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, s.D, nullptr, 0, 0,
+                                 scale, st, o.l2_prefetch ? o_weight->data : nullptr, w_span, &fa);
+    if (rc != DA_ERR_UNSUPPORTED) return rc;  // else: not co-resident here, take two launches
+  }
+  const ProjPlan gp = plan_projection(s.B, (int)K, (int)N, o);
+  char* ws = nullptr;
+  DA_TRY(workspace_get(ap.bytes + attn_bytes + gp.bytes, st, &ws));
+  char* scratch = ws + kHeaderBytes;
+  __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(scratch + ap.bytes);
+  // W_o span: rows 0..K-1 of stride w_sk, the last row N wide
+  const long long w_span = ((long long)(K - 1) * o_weight->stride[0] + N) * 2;
+  DA_TRY(run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, s.D, nullptr, 0, 0, scale,
+                       st, o.l2_prefetch ? o_weight->data : nullptr, w_span, nullptr, paged));
+  return run_projection(attn, K, o_weight, out, s.B, (int)K, (int)N, ws, scratch + ap.bytes + attn_bytes, gp,
+                        o.pdl != 0, st);
 }
 
 }  // namespace
@@ -523,19 +649,16 @@ int decode_attn_only(const da_tensor_t* q, const da_tensor_t* k_cache, const da_
                      const da_tensor_t* seq_lens, const da_tensor_t* attn_out, float scale, void* stream) {
   AttnShape s;
   DA_TRY(check_attention_inputs(q, k_cache, v_cache, seq_lens, true, &s));
-  DA_TRY(check_tensor(attn_out, DA_DTYPE_BF16, 3, kOutput));
-  if (attn_out->shape[0] != s.B || attn_out->shape[1] != s.Hq || attn_out->shape[2] != s.D)
-    return DA_ERR_SHAPE;
-  if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
-  if (s.B == 0) return DA_OK;
-  const Options o = options_snapshot();
-  const AttnPlan pl = plan_attention(s, o);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  char* ws = nullptr;
-  DA_TRY(workspace_get(pl.bytes, st, &ws));
-  return run_attention(q, k_cache, v_cache, seq_lens, s, pl, ws, ws + kHeaderBytes,
-                       static_cast<__nv_bfloat16*>(attn_out->data), attn_out->stride[0], attn_out->stride[1],
-                       nullptr, 0, 0, scale, st);
+  return only_checked(q, k_cache, v_cache, seq_lens, attn_out, scale, stream, s, nullptr);
+}
+
+int decode_attn_only_paged(const da_tensor_t* q, const da_tensor_t* k_pages, const da_tensor_t* v_pages,
+                           const da_tensor_t* block_table, const da_tensor_t* seq_lens, const da_tensor_t* attn_out,
+                           float scale, void* stream) {
+  AttnShape s;
+  PagedShape ps;
+  DA_TRY(check_paged_inputs(q, k_pages, v_pages, block_table, seq_lens, &s, &ps));
+  return only_checked(q, k_pages, v_pages, seq_lens, attn_out, scale, stream, s, &ps);
 }
 
 }  // extern "C"
@@ -638,41 +761,16 @@ int decode_attn_fwd(const da_tensor_t* q, const da_tensor_t* k_cache, const da_t
                     void* stream) {
   AttnShape s;
   DA_TRY(check_attention_inputs(q, k_cache, v_cache, seq_lens, true, &s));
-  DA_TRY(check_tensor(o_weight, DA_DTYPE_BF16, 2, kInput16));
-  DA_TRY(check_tensor(out, DA_DTYPE_BF16, 2, kOutput));
-  const int64_t K = (int64_t)s.Hq * s.D, N = o_weight->shape[1];
-  if (o_weight->shape[0] != K || out->shape[0] != s.B || out->shape[1] != N) return DA_ERR_SHAPE;
-  if (N <= 0 || N % 8) return DA_ERR_SHAPE;
-  if (N > (1 << 30) || K > (1 << 30)) return DA_ERR_UNSUPPORTED;
-  if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
-  if (s.B == 0) return DA_OK;
-  const Options o = options_snapshot();
-  const AttnPlan ap = plan_attention(s, o);
-  const size_t attn_bytes = align_up((size_t)s.B * K * 2, 256);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const FusedPlan fp = plan_fused(s, (int)K, (int)N, ap, o);
-  if (fp.ok) {  // one launch: attention, grid barrier, projection
-    char* ws = nullptr;
-    DA_TRY(workspace_get(ap.bytes + attn_bytes + fp.part_bytes, st, &ws));
-    char* scratch = ws + kHeaderBytes;
-    __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(scratch + ap.bytes);
-    const FusedArgs fa{&fp, o_weight, out, reinterpret_cast<float*>(scratch + ap.bytes + attn_bytes), (int)K, (int)N};
-    const long long w_span = ((long long)(K - 1) * o_weight->stride[0] + N) * 2;
-    const int rc = run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, s.D, nullptr, 0, 0,
-                                 scale, st, o.l2_prefetch ? o_weight->data : nullptr, w_span, &fa);
-    if (rc != DA_ERR_UNSUPPORTED) return rc;  // else: not co-resident here, take two launches
-  }
-  const ProjPlan gp = plan_projection(s.B, (int)K, (int)N, o);
-  char* ws = nullptr;
-  DA_TRY(workspace_get(ap.bytes + attn_bytes + gp.bytes, st, &ws));
-  char* scratch = ws + kHeaderBytes;
-  __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(scratch + ap.bytes);
-  // W_o span: rows 0..K-1 of stride w_sk, the last row N wide
-  const long long w_span = ((long long)(K - 1) * o_weight->stride[0] + N) * 2;
-  DA_TRY(run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, s.D, nullptr, 0, 0, scale,
-                       st, o.l2_prefetch ? o_weight->data : nullptr, w_span));
-  return run_projection(attn, K, o_weight, out, s.B, (int)K, (int)N, ws, scratch + ap.bytes + attn_bytes, gp,
-                        o.pdl != 0, st);
+  return fwd_checked(q, k_cache, v_cache, seq_lens, o_weight, out, scale, stream, s, nullptr);
+}
+
+int decode_attn_fwd_paged(const da_tensor_t* q, const da_tensor_t* k_pages, const da_tensor_t* v_pages,
+                          const da_tensor_t* block_table, const da_tensor_t* seq_lens, const da_tensor_t* o_weight,
+                          const da_tensor_t* out, float scale, void* stream) {
+  AttnShape s;
+  PagedShape ps;
+  DA_TRY(check_paged_inputs(q, k_pages, v_pages, block_table, seq_lens, &s, &ps));
+  return fwd_checked(q, k_pages, v_pages, seq_lens, o_weight, out, scale, stream, s, &ps);
 }
 
 int decode_attn_device_error(void* stream, int32_t* host_code) {

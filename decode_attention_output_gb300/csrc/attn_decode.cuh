@@ -300,11 +300,100 @@ __device__ void fused_epilogue(const AttnParams& p, uint64_t* bars, uint32_t tme
   }
 }
 
-template <int NB, bool SCORES, int S, int NPAD, int DIM>
+// ---------------------------------------------------------------- paged cache
+// Producer of the paged variant (the whole producer warp; lane 0 waits and issues).
+// A tile of kT tokens is cut into boxes of min(block_size, kT) tokens, each read from
+// its own block: box i of the CTA's range (tiles in order, boxes within a tile) lives
+// in block block_table[b][t / block_size]. The warp looks block ids up 32 boxes at a
+// time, one window ahead (lane l holds box 32w + l), so the table's latency stays off
+// the issue path. Boxes that start at or past the sequence's length are not loaded
+// (the consumers mask those tokens), so the table is never read past a sequence's
+// ceil(L / block_size) entries. A block id outside [0, num_blocks) is recorded in the
+// error word and read past the pool's end, which TMA fills with zeros.
+template <int S, int DIM>
+__device__ void paged_producer(const AttnParams& p, uint32_t ring, uint8_t* q_slots, size_t q_slot, uint64_t* bars,
+                               int* flags, const int* prefix, const int* lens, long long start, long long end,
+                               int lane) {
+  constexpr int kT = tile_tokens(DIM), kBox = box_bytes(DIM), kQRow = q_row_bytes(DIM);
+  if (start >= end) return;
+  const int B = p.B, Hkv = p.Hkv, G = p.G, bs = p.block_size;
+  const int sub_tok = bs < kT ? bs : kT;  // tokens per box
+  const int nsub = kT / sub_tok;          // boxes per 64-dim column of a tile
+  const uint32_t sub_bytes = (uint32_t)sub_tok * 128 * (DIM / 64);  // one box row of K (or V)
+  const long long n_box = (end - start) * nsub;
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
+  auto lookup = [&](long long i) -> int {  // block id of box i (0 when the box is not loaded)
+    if (i >= n_box) return 0;
+    const long long x = start + i / nsub;
+    const Cursor c = cursor_at(x, prefix, B, Hkv);
+    const int t = c.j * kT + (int)(i % nsub) * sub_tok;
+    if (t >= lens[c.b]) return 0;
+    int blk = __ldg(p.block_table + (long long)c.b * p.bt_stride + t / bs);
+    if (blk < 0 || blk >= p.num_blocks) {
+      atomicOr(p.err, kErrBlockTable);
+      blk = p.num_blocks;
+    }
+    return blk;
+  };
+  if (lane == 0) {
+    prefetch_tensormap(&p.tm_k);
+    prefetch_tensormap(&p.tm_v);
+  }
+  const uint64_t kv_policy = l2_policy_evict_first();
+  int cur = lookup(lane), nxt = lookup(32 + lane);
+  Cursor c = cursor_at(start, prefix, B, Hkv);
+  long long seg0 = start, i = 0;
+  int it = 0;
+  for (long long x = start; x < end; ++x, ++it) {
+    if (x != start) {
+      cursor_next(c, prefix, B, Hkv);
+      if (c.j == 0) seg0 = x;
+    }
+    const bool with_q = x - seg0 < kGroups;
+    const int stage = it % S;
+    const int t0 = c.j * kT;
+    const int n_load = min(nsub, (lens[c.b] - t0 + sub_tok - 1) / sub_tok);  // >= 1: t0 < L
+    const uint32_t fb = full_bar(stage);
+    const uint32_t kdst = ring + stage * kStageBytes;
+    if (lane == 0) {
+      mbar_wait_bounded(empty_bar(stage), ((it / S) & 1) ^ 1, p.err, kErrWaitEmpty, flags);
+      mbar_arrive_expect_tx(fb, 2 * n_load * sub_bytes + (with_q ? G * DIM * 2 : 0));
+    }
+    __syncwarp();
+    for (int sidx = 0; sidx < nsub; ++sidx, ++i) {
+      if (i > 0 && (i & 31) == 0) {
+        cur = nxt;
+        nxt = lookup(i + 32 + lane);
+      }
+      const int blk = __shfl_sync(0xffffffffu, cur, (int)(i & 31));
+      if (lane == 0 && sidx < n_load) {
+        const int row = (t0 + sidx * sub_tok) % bs;
+#pragma unroll
+        for (int bx = 0; bx < DIM / 64; ++bx) {
+          const uint32_t off = bx * kBox + sidx * sub_tok * 128;
+          tma_load_4d_hint(kdst + off, &p.tm_k, fb, bx * 64, row, c.kvh, blk, kv_policy);
+          tma_load_4d_hint(kdst + kKTileBytes + off, &p.tm_v, fb, bx * 64, row, c.kvh, blk, kv_policy);
+        }
+      }
+    }
+    if (with_q && lane == 0) {
+      const uint32_t qdst = smem_u32(q_slots + stage * q_slot);
+      const __nv_bfloat16* qsrc = p.q + (long long)c.b * p.q_sb + (long long)(c.kvh * G) * p.q_sh;
+      for (int h = 0; h < G; ++h) bulk_load(qdst + h * kQRow, qsrc + (long long)h * p.q_sh, DIM * 2, fb);
+    }
+  }
+  if (lane == 0)  // do not leave with copies in flight
+    for (int k = it > S ? it - S : 0; k < it; ++k)
+      mbar_wait_bounded(full_bar(k % S), (k / S) & 1, p.err, kErrWaitDrain, nullptr, kWaitLimitNs / 10);
+}
+
+template <int NB, bool SCORES, int S, int NPAD, int DIM, bool PAGED = false>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __grid_constant__ AttnParams p) {
   constexpr bool kFused = NPAD > 0;
   constexpr bool kWide = DIM == kHeadDimWide;
   static_assert(DIM == kHeadDim || (kWide && !kFused), "head dim 128, or 256 without the fused step");
+  static_assert(!PAGED || (!kFused && !SCORES), "the paged variant computes attention only");
   constexpr int kT = tile_tokens(DIM);    // tokens per tile
   constexpr int kBox = box_bytes(DIM);    // one 64-dim box of a tile
   constexpr int kQRow = q_row_bytes(DIM);
@@ -395,7 +484,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
 
   if (warp == kGroups * kGroupWarps) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if constexpr (PAGED) {
+      paged_producer<S, DIM>(p, ring, q_slots, kFixed.q_slot(), bars, flags, prefix, lens, start, end, lane);
+    } else if (lane == 0) {
      int it = 0;
      if (start < end) {
       prefetch_tensormap(&p.tm_k);
@@ -795,7 +886,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   }
 }
 
-template <int NB, bool SCORES, int S, int NPAD, int DIM>
+template <int NB, bool SCORES, int S, int NPAD, int DIM, bool PAGED = false>
 cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   // The shared-memory opt-in is a per-device function attribute: set it once per device.
   static int configured[64] = {0};
@@ -804,7 +895,7 @@ cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attn_decode_kernel<NB, SCORES, S, NPAD, DIM>,
+    e = cudaFuncSetAttribute(attn_decode_kernel<NB, SCORES, S, NPAD, DIM, PAGED>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDynSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
@@ -819,7 +910,7 @@ cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = NPAD > 0 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<NB, SCORES, S, NPAD, DIM>, p);
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<NB, SCORES, S, NPAD, DIM, PAGED>, p);
 }
 
 }  // namespace

@@ -106,7 +106,18 @@ struct AttnParams {
   int N, K, kb_per_tile, units;  // units = column tiles x k-blocks of 64
   int attn_workers;      // CTAs that take attention tiles (<= grid); the fused step may leave
                          // some CTAs free to start on W_o at once
+  // Paged cache only: tm_k / tm_v map [num_blocks][Hkv][block_size][D]; token t of sequence b
+  // is row t % block_size of block block_table[b * bt_stride + t / block_size].
+  const int* block_table;
+  long long bt_stride;
+  int block_size, num_blocks;
 };
+
+// Paged caches: a block size the tiles can be cut into, or that holds whole tiles.
+__host__ __device__ constexpr bool paged_block_ok(int block_size, int dim) {
+  return block_size >= 8 && (block_size % tile_tokens(dim) == 0 ||
+                             (tile_tokens(dim) % block_size == 0 && block_size % 8 == 0));
+}
 
 constexpr int kProjWBytes = 2 * 64 * 128;  // one stage of W_o: 128 columns x 64 k-rows
 // Phase-B stages re-cut the attention ring (kStages x kStageBytes) into W_o + X tiles.
@@ -123,6 +134,8 @@ cudaError_t launch_attention(const AttnParams& p, int grid, int nb, int dim, boo
                              int npad = 0);
 // The D = 256 instantiations (their own translation unit).
 cudaError_t launch_attention_d256(const AttnParams& p, int grid, int nb, bool scores_only, cudaStream_t stream);
+// Attention over a paged cache (p.block_table set), D = 128 or 256.
+cudaError_t launch_attention_paged(const AttnParams& p, int grid, int nb, int dim, cudaStream_t stream);
 
 // ------------------------------------------------------- projection: GEMV path
 constexpr int kGemvThreads = 256;

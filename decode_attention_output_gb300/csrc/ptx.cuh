@@ -17,6 +17,7 @@ enum : int {
   kErrWaitMma = 8,       // tensor-core completion never arrived
   kErrTmem = 16,         // TMEM allocation failed
   kErrGridSync = 32,     // the fused step's grid barrier did not complete
+  kErrBlockTable = 64,   // a paged cache's block table named a block outside the pool
 };
 
 // Two seconds: a kernel of this library runs for milliseconds at most.

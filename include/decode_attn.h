@@ -149,6 +149,38 @@ int decode_attn_only_noalloc(const da_tensor_t* q, const da_tensor_t* k_cache, c
                              void* stream);
 
 /*
+ * decode_attn_fwd_paged / decode_attn_only_paged -- decode_attn_fwd / decode_attn_only
+ * over a paged KV cache: the keys and values live in a pool of fixed-size blocks and
+ * a per-sequence block table lists the blocks of each sequence in token order. The
+ * pages have no paged cache; the computation is exactly that of the contiguous entry
+ * points on the cache the table describes,
+ *
+ *   K[b, j, t, :] = k_pages[block_table[b, t / block_size], j, t % block_size, :]
+ *
+ * for t < seq_lens[b] (and the same for V).
+ *   k_pages     [num_blocks, Hkv, block_size, D] bf16  the key pool (device). Any strides
+ *               obeying the conventions, so a pool stored as [num_blocks, block_size,
+ *               Hkv, D] is passed as the view with dims 1 and 2 swapped.
+ *   v_pages     same shape as k_pages (its own strides)
+ *   block_table [B, max_blocks] int32 (device), rows contiguous: entry i of row b is the
+ *               pool block holding tokens [i * block_size, (i + 1) * block_size) of
+ *               sequence b. Only the first ceil(seq_lens[b] / block_size) entries of a
+ *               row are read.
+ *   seq_lens    [B] int32 (device), clamped to [0, max_blocks * block_size]
+ *   q, o_weight, out, attn_out, scale: as decode_attn_fwd / decode_attn_only.
+ * block_size: a multiple of 64 (of 32 at D = 256), or 8, 16 or 32 (8 or 16 at D = 256);
+ * anything else returns DA_ERR_UNSUPPORTED. A table entry outside [0, num_blocks) that
+ * is read sets bit 64 of the device error word (decode_attn_device_error) and that
+ * block reads as zeros. The fused option does not apply: two launches.
+ */
+int decode_attn_fwd_paged(const da_tensor_t* q, const da_tensor_t* k_pages, const da_tensor_t* v_pages,
+                          const da_tensor_t* block_table, const da_tensor_t* seq_lens, const da_tensor_t* o_weight,
+                          const da_tensor_t* out, float scale, void* stream);
+int decode_attn_only_paged(const da_tensor_t* q, const da_tensor_t* k_pages, const da_tensor_t* v_pages,
+                           const da_tensor_t* block_table, const da_tensor_t* seq_lens, const da_tensor_t* attn_out,
+                           float scale, void* stream);
+
+/*
  * decode_attn_scores -- the first contraction alone: the page's `scores_fp32`
  * (q_grouped . k_cache^T, b_trans=True), unscaled, in fp32.
  *   scores [B, Hq, Lcap] fp32: scores[b, h, t] is written for t < seq_lens[b]

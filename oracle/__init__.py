@@ -87,6 +87,8 @@ class Oracle:
         lib.oracle_attention.restype = ctypes.c_int
         lib.oracle_decode.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _dbl, _p, _p]
         lib.oracle_decode.restype = ctypes.c_int
+        lib.oracle_gather_pages.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _i64, _i64, _p, _p]
+        lib.oracle_gather_pages.restype = ctypes.c_int
         self._lib = lib
 
     def num_threads(self) -> int:
@@ -191,6 +193,30 @@ class Oracle:
                                    float(scale), _ptr(attn), _ptr(out)) != 0:
             raise ValueError("oracle_decode rejected its arguments")
         return attn, out
+
+
+    # ---- paged cache -------------------------------------------------------------------
+    def gather_pages(self, pages, table, seq_lens) -> np.ndarray:
+        """pages [num_blocks, Hkv, bs, D] (bf16 bits), table [B, max_blocks] int32 ->
+        the contiguous cache [B, Hkv, max_blocks * bs, D] (bf16 bits) the table describes."""
+        pages = _u16(pages, "pages")
+        table = np.ascontiguousarray(table, dtype=np.int32)
+        seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        nblk, Hkv, bs, D = pages.shape
+        B, mb = table.shape
+        if seq_lens.shape != (B,):
+            raise ValueError("seq_lens must be [B]")
+        cache = np.zeros((B, Hkv, mb * bs, D), np.uint16)
+        if self._lib.oracle_gather_pages(_ptr(pages), nblk, Hkv, bs, D, _ptr(table), B, mb, _ptr(seq_lens),
+                                         _ptr(cache)) != 0:
+            raise ValueError("oracle_gather_pages rejected its arguments")
+        return cache
+
+    def decode_paged(self, q, k_pages, v_pages, table, seq_lens, w, scale: float):
+        """Whole step over a paged cache: the step on the caches the table describes."""
+        k = self.gather_pages(k_pages, table, seq_lens)
+        v = self.gather_pages(v_pages, table, seq_lens)
+        return self.decode(q, k, v, seq_lens, w, scale)
 
 
 _default: Oracle | None = None

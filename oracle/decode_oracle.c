@@ -275,3 +275,37 @@ int oracle_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, const
   if (out) oracle_oproj(attn, w, B, Hq * D, N, out);
   return 0;
 }
+
+/*
+ * oracle_gather_pages -- the contiguous cache that a paged cache describes, for the
+ * library's block-table entry points (the pages describe no paged cache; this is the
+ * plain reading of a block table): for t < seq_lens[b] and every KV head j,
+ *
+ *   cache[b][j][t][:] = pages[table[b][t / bs]][j][t % bs][:]
+ *
+ * A table entry outside [0, num_blocks) gives a zero row (the library flags it and
+ * reads zeros), and rows t >= seq_lens[b] are zero. Only bit patterns are copied.
+ *   pages [num_blocks][Hkv][bs][D], table [B][max_blocks], cache [B][Hkv][max_blocks*bs][D]
+ * Returns 0, or -1 when a length lies outside [0, max_blocks * bs].
+ */
+int oracle_gather_pages(const uint16_t* pages, int64_t num_blocks, int64_t Hkv, int64_t bs, int64_t D,
+                        const int32_t* table, int64_t B, int64_t max_blocks, const int32_t* seq_lens,
+                        uint16_t* cache) {
+  const int64_t Lcap = max_blocks * bs;
+  for (int64_t b = 0; b < B; ++b)
+    if (seq_lens[b] < 0 || seq_lens[b] > Lcap) return -1;
+  memset(cache, 0, (size_t)(B * Hkv * Lcap * D) * sizeof(uint16_t));
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t t = 0; t < seq_lens[b]; ++t) {
+      const int64_t blk = table[b * max_blocks + t / bs];
+      if (blk < 0 || blk >= num_blocks) continue;
+      const int64_t row = t % bs;
+      for (int64_t j = 0; j < Hkv; ++j) {
+        const uint16_t* src = pages + ((blk * Hkv + j) * bs + row) * D;
+        uint16_t* dst = cache + ((b * Hkv + j) * Lcap + t) * D;
+        memcpy(dst, src, (size_t)D * sizeof(uint16_t));
+      }
+    }
+  }
+  return 0;
+}

@@ -441,6 +441,70 @@ def pin_bf16_widening(orc):
     assert np.array_equal(y[0], bits_to_f64(bits)), "bf16 widening"
 
 
+def _scatter_to_pages(rng, cache, bs, spare):
+    """Cuts a contiguous cache [B, Hkv, Lcap, D] into blocks of bs tokens, stores them in
+    a pool at random places (with `spare` extra blocks of noise) and returns (pool, table).
+    Block-granular slicing, the inverse of the oracle's per-token gather."""
+    B, Hkv, Lcap, D = cache.shape
+    mb = Lcap // bs
+    nblk = B * mb + spare
+    pool = rng.integers(0, 1 << 16, size=(nblk, Hkv, bs, D)).astype(np.uint16)
+    perm = rng.permutation(nblk)[: B * mb].reshape(B, mb)
+    for b in range(B):
+        for i in range(mb):
+            pool[perm[b, i]] = cache[b, :, i * bs:(i + 1) * bs, :]
+    return pool, perm.astype(np.int32)
+
+
+def pin_gather_pages_roundtrip(orc):
+    """Scattering a cache into shuffled blocks and gathering it back through the table
+    returns the cache exactly (rows t < seq_len), and zeros past seq_len."""
+    rng = np.random.default_rng(41)
+    for bs, D in ((16, 128), (8, 256), (64, 128)):
+        B, Hkv, mb = 3, 2, 4
+        cache = rng.integers(0, 1 << 16, size=(B, Hkv, mb * bs, D)).astype(np.uint16)
+        pool, table = _scatter_to_pages(rng, cache, bs, spare=5)
+        lens = np.array([mb * bs, 1, bs + 3], np.int32)
+        got = orc.gather_pages(pool, table, lens)
+        for b in range(B):
+            L = lens[b]
+            assert np.array_equal(got[b, :, :L], cache[b, :, :L]), f"gather bs={bs} b={b}"
+            assert np.all(got[b, :, L:] == 0), "rows past seq_len are zero"
+
+
+def pin_gather_pages_reads_only_used_entries(orc):
+    """Table entries past ceil(L / bs) are never used, and an entry outside the pool
+    gives zero rows for its tokens only."""
+    rng = np.random.default_rng(42)
+    bs, D, B, Hkv, mb = 16, 128, 2, 1, 3
+    cache = rng.integers(0, 1 << 16, size=(B, Hkv, mb * bs, D)).astype(np.uint16)
+    pool, table = _scatter_to_pages(rng, cache, bs, spare=0)
+    lens = np.array([20, 48], np.int32)
+    table[0, 2] = 1 << 30  # past ceil(20 / 16) = 2 entries: unused
+    table[1, 1] = -7       # outside the pool: tokens 16..31 of row 1 read as zero
+    got = orc.gather_pages(pool, table, lens)
+    assert np.array_equal(got[0, :, :20], cache[0, :, :20])
+    assert np.array_equal(got[1, :, :16], cache[1, :, :16]) and np.all(got[1, :, 16:32] == 0)
+    assert np.array_equal(got[1, :, 32:48], cache[1, :, 32:48])
+
+
+def pin_paged_decode_equals_contiguous(orc):
+    """The whole step over a paged cache equals the step over the cache it describes."""
+    rng = np.random.default_rng(43)
+    B, Hq, Hkv, bs, mb, N = 2, 4, 2, 16, 3, 16
+    q = rand_bits(rng, (B, Hq, D))
+    k = rand_bits(rng, (B, Hkv, mb * bs, D))
+    v = rand_bits(rng, (B, Hkv, mb * bs, D))
+    w = rand_bits(rng, (Hq * D, N), std=1 / math.sqrt(Hq * D))
+    lens = np.array([48, 17], np.int32)
+    kp, table = _scatter_to_pages(np.random.default_rng(44), k, bs, spare=2)
+    vp, table_v = _scatter_to_pages(np.random.default_rng(44), v, bs, spare=2)
+    assert np.array_equal(table, table_v)
+    a1, y1 = orc.decode_paged(q, kp, vp, table, lens, w, 1 / math.sqrt(D))
+    a0, y0 = orc.decode(q, k, v, lens, w, 1 / math.sqrt(D))
+    assert np.array_equal(a1, a0) and np.array_equal(y1, y0)
+
+
 PINS = [v for kname, v in sorted(globals().items()) if kname.startswith("pin_") and callable(v)]
 
 

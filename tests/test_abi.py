@@ -174,3 +174,61 @@ def test_binding_raises_with_code(lib):
     with pytest.raises(da.DecodeAttnError) as ei:
         da.decode_attn_only(q, k, k, lens, attn, 0.1, stream=0)
     assert ei.value.code == DTYPE
+
+
+# ---------------------------------------------------------- paged-cache entry points
+def paged_args(B=2, Hq=8, Hkv=2, D=128, nblk=10, bs=16, mb=4, N=256, **over):
+    a = dict(q=desc([B, Hq, D]), kp=desc([nblk, Hkv, bs, D]), vp=desc([nblk, Hkv, bs, D]),
+             table=desc([B, mb], binding.DA_DTYPE_I32), lens=desc([B], binding.DA_DTYPE_I32),
+             w=desc([Hq * D, N]), out=desc([B, N]), attn=desc([B, Hq, D]))
+    a.update(over)
+    return a
+
+
+def call_paged(lib, a, scale=0.1):
+    r = lambda d: ctypes.byref(d) if d is not None else None  # noqa: E731
+    rc_fwd = lib.decode_attn_fwd_paged(r(a["q"]), r(a["kp"]), r(a["vp"]), r(a["table"]), r(a["lens"]), r(a["w"]),
+                                       r(a["out"]), ctypes.c_float(scale), None)
+    rc_only = lib.decode_attn_only_paged(r(a["q"]), r(a["kp"]), r(a["vp"]), r(a["table"]), r(a["lens"]),
+                                         r(a["attn"]), ctypes.c_float(scale), None)
+    return rc_fwd, rc_only
+
+
+BAD_PAGED = [
+    ("block_size_24", dict(kp=desc([10, 2, 24, 128]), vp=desc([10, 2, 24, 128])), UNSUP),
+    ("block_size_4", dict(kp=desc([10, 2, 4, 128]), vp=desc([10, 2, 4, 128])), UNSUP),
+    ("block_size_96", dict(kp=desc([10, 2, 96, 128]), vp=desc([10, 2, 96, 128])), UNSUP),
+    ("d256_block_size_48", dict(q=desc([2, 8, 256]), kp=desc([10, 2, 48, 256]), vp=desc([10, 2, 48, 256]),
+                                w=desc([8 * 256, 256]), attn=desc([2, 8, 256])), UNSUP),
+    ("table_dtype", dict(table=desc([2, 4], binding.DA_DTYPE_F32)), DTYPE),
+    ("table_rows", dict(table=desc([3, 4], binding.DA_DTYPE_I32)), SHAPE),
+    ("table_1d", dict(table=desc([8], binding.DA_DTYPE_I32)), SHAPE),
+    ("table_inner_stride", dict(table=desc([2, 4], binding.DA_DTYPE_I32, strides=[8, 2])), STRIDE),
+    ("table_rows_overlap", dict(table=desc([2, 4], binding.DA_DTYPE_I32, strides=[2, 1])), STRIDE),
+    ("table_misaligned", dict(table=desc([2, 4], binding.DA_DTYPE_I32, addr=FAKE + 2)), ALIGN),
+    ("null_table", dict(table=None), NULL),
+    ("v_pages_shape", dict(vp=desc([9, 2, 16, 128])), SHAPE),
+    ("pages_head_dim", dict(kp=desc([10, 2, 16, 256]), vp=desc([10, 2, 16, 256])), SHAPE),
+    ("pages_misaligned", dict(kp=desc([10, 2, 16, 128], addr=FAKE + 8)), ALIGN),
+    ("pages_token_stride_odd", dict(kp=desc([10, 2, 16, 128], strides=[2 * 16 * 132, 16 * 132, 132, 1])),
+     STRIDE),
+    ("group_32", dict(q=desc([2, 64, 128]), w=desc([64 * 128, 256]), attn=desc([2, 64, 128])), UNSUP),
+    ("empty_pool", dict(kp=desc([0, 2, 16, 128]), vp=desc([0, 2, 16, 128])), SHAPE),
+]
+
+
+@cpu_only
+@pytest.mark.parametrize("name,over,code", BAD_PAGED, ids=[c[0] for c in BAD_PAGED])
+def test_paged_rejects(lib, name, over, code):
+    assert call_paged(lib, paged_args(**over)) == (code, code)
+
+
+@cpu_only
+def test_paged_accepts_valid_block_sizes_on_the_host(lib):
+    """Valid shapes pass validation; with B = 0 nothing is launched."""
+    for D, bs in ((128, 8), (128, 16), (128, 32), (128, 64), (128, 192), (256, 8), (256, 16), (256, 32),
+                  (256, 96)):
+        a = paged_args(B=0, D=D, bs=bs)
+        for key in ("q", "table", "lens", "out", "attn"):
+            a[key].data = None
+        assert call_paged(lib, a) == (OK, OK), (D, bs)

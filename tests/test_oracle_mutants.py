@@ -43,6 +43,10 @@ MUTANTS = [
     ("seq_len_ignored", "1, seq_lens[b], D, scale,", "1, Lcap, D, scale,", None),
     ("v_row_offset", "acc += z[t] * bf16_bits_to_double(v[t * v_row_stride + d]);",
      "acc += z[t] * bf16_bits_to_double(v[t * v_row_stride + (d + 1) % D]);", None),
+    ("paged_block_index_modulo", "table[b * max_blocks + t / bs]", "table[b * max_blocks + t % max_blocks]", None),
+    ("paged_row_index_divided", "const int64_t row = t % bs;", "const int64_t row = (t / bs) % bs;", None),
+    ("paged_head_ignored", "pages + ((blk * Hkv + j) * bs + row) * D", "pages + ((blk * Hkv) * bs + row) * D", None),
+    ("paged_table_stride", "table[b * max_blocks + t / bs]", "table[b + t / bs]", None),
 ]
 
 
