@@ -124,8 +124,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 4-D map over a [B][Hkv][Lcap][D] bf16 cache (or a [num_blocks][Hkv][block_size][D]
-// page pool); box = 64 dims x box_tokens tokens (0: tile_tokens(D)).
+// 5-D map over a [B][Hkv][Lcap][D] bf16 cache (or a [num_blocks][Hkv][block_size][D]
+// page pool) with the head dim split in two: {64 dims, token, D/64 dim boxes, head,
+// batch (or block)}. One box = 64 dims x box_tokens tokens x all D/64 dim boxes, which
+// lands in shared memory as D/64 consecutive 64-dim boxes of box_tokens rows (128-byte
+// rows, 128-byte swizzle): one copy per tile and tensor (box_tokens 0: tile_tokens(D)).
 int encode_kv_map(CUtensorMap* map, const da_tensor_t* t, int box_tokens = 0) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return DA_ERR_CUDA;
@@ -134,12 +137,28 @@ int encode_kv_map(CUtensorMap* map, const da_tensor_t* t, int box_tokens = 0) {
   const int64_t st = L == 1 ? D : t->stride[2];
   const int64_t sh = H == 1 ? st * L : t->stride[1];
   const int64_t sb = B == 1 ? sh * H : t->stride[0];
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)H, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)st * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)(box_tokens > 0 ? box_tokens : tile_tokens((int)D)), 1, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, estr,
+  cuuint64_t dims[5] = {64, (cuuint64_t)L, (cuuint64_t)(D / 64), (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[4] = {(cuuint64_t)st * 2, 128, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
+  cuuint32_t box[5] = {64, (cuuint32_t)(box_tokens > 0 ? box_tokens : tile_tokens((int)D)), (cuuint32_t)(D / 64),
+                       1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, t->data, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_UNSUPPORTED;
+}
+
+// Map over a block table seen as one flat int32 array of `entries` (a 2-D map of one
+// row); box = 16 entries.
+int encode_table_map(CUtensorMap* map, const void* base, int64_t entries) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return DA_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)entries, 1};
+  cuuint64_t strides[1] = {(cuuint64_t)align_up((size_t)entries * 4, 16)};
+  cuuint32_t box[2] = {16, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_UNSUPPORTED;
 }
@@ -241,7 +260,7 @@ int check_attention_inputs(const da_tensor_t* q, const da_tensor_t* k, const da_
 // The logical capacity is max_blocks * block_size.
 struct PagedShape {
   const int* table;
-  long long table_stride;
+  long long table_stride, table_entries;  // row stride; flat extent (B-1)*stride + max_blocks
   int block_size, num_blocks;
 };
 
@@ -276,8 +295,9 @@ int check_paged_inputs(const da_tensor_t* q, const da_tensor_t* kp, const da_ten
     if (B > 1 && lens->stride[0] != 1) return DA_ERR_STRIDE;
     if (MB > 1 && table->stride[1] != 1) return DA_ERR_STRIDE;
     if (B > 1 && table->stride[0] < MB) return DA_ERR_STRIDE;
-    if (reinterpret_cast<uintptr_t>(lens->data) % 4 || reinterpret_cast<uintptr_t>(table->data) % 4)
-      return DA_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(lens->data) % 4 || reinterpret_cast<uintptr_t>(table->data) % 16)
+      return DA_ERR_ALIGN;  // the table is read by TMA: 16-byte aligned base
+    if ((B - 1) * table->stride[0] + MB >= ((int64_t)1 << 31)) return DA_ERR_UNSUPPORTED;
   }
   s->B = (int)B;
   s->Hq = (int)Hq;
@@ -287,6 +307,7 @@ int check_paged_inputs(const da_tensor_t* q, const da_tensor_t* kp, const da_ten
   s->D = (int)D;
   ps->table = static_cast<const int*>(table->data);
   ps->table_stride = B > 1 ? table->stride[0] : MB;
+  ps->table_entries = B > 0 ? (B - 1) * ps->table_stride + MB : 0;
   ps->block_size = (int)BS;
   ps->num_blocks = (int)NB;
   return DA_OK;
@@ -494,6 +515,9 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
     p.bt_stride = paged->table_stride;
     p.block_size = paged->block_size;
     p.num_blocks = paged->num_blocks;
+    p.block_shift = 0;
+    while ((1 << p.block_shift) < paged->block_size) ++p.block_shift;
+    DA_TRY(encode_table_map(&p.tm_table, paged->table, paged->table_entries));
   }
   p.q = static_cast<const __nv_bfloat16*>(q->data);
   p.q_sb = q->stride[0];

@@ -301,49 +301,59 @@ __device__ void fused_epilogue(const AttnParams& p, uint64_t* bars, uint32_t tme
 }
 
 // ---------------------------------------------------------------- paged cache
-// Producer of the paged variant (the whole producer warp; lane 0 waits and issues).
-// A tile of kT tokens is cut into boxes of min(block_size, kT) tokens, each read from
-// its own block: box i of the CTA's range (tiles in order, boxes within a tile) lives
-// in block block_table[b][t / block_size]. The warp looks block ids up 32 boxes at a
-// time, one window ahead (lane l holds box 32w + l), so the table's latency stays off
-// the issue path. Boxes that start at or past the sequence's length are not loaded
-// (the consumers mask those tokens), so the table is never read past a sequence's
-// ceil(L / block_size) entries. A block id outside [0, num_blocks) is recorded in the
-// error word and read past the pool's end, which TMA fills with zeros.
+// Producer of the paged variant (one lane, like the contiguous producer). A tile of
+// kT tokens is cut into boxes of min(block_size, kT) tokens (block sizes are powers of
+// two), each read from its own block: box s of tile j of sequence b comes from block
+// block_table[b][(j*kT + s*sub_tok) / block_size]. The block ids travel by TMA too: the 16 table entries
+// from the tile's first one (rounded down to 16 bytes) are loaded kIdTiles tiles
+// ahead into a shared-memory ring, each row completing on its own mbarrier, so no
+// table read sits between a stage becoming free and its copies going out (the stream
+// is bound by bytes in flight). Entries past a sequence's ceil(L / block_size) may be
+// fetched but are never used; boxes that start at or past the sequence's length are
+// not loaded (the consumers mask those tokens). A block id outside [0, num_blocks) is
+// recorded in the error word and read past the pool's end, which TMA fills with zeros.
 template <int S, int DIM>
-__device__ void paged_producer(const AttnParams& p, uint32_t ring, uint8_t* q_slots, size_t q_slot, uint64_t* bars,
-                               int* flags, const int* prefix, const int* lens, long long start, long long end,
-                               int lane) {
-  constexpr int kT = tile_tokens(DIM), kBox = box_bytes(DIM), kQRow = q_row_bytes(DIM);
+__device__ __forceinline__ void paged_producer(const AttnParams& p, uint32_t ring, uint8_t* q_slots, size_t q_slot,
+                                               uint64_t* bars, int* flags, const int* prefix, const int* lens,
+                                               int* ids, long long start, long long end) {
+  // This lane shares its SM sub-partition with two busy consumer warps, so every
+  // instruction per tile costs: block sizes are powers of two (shifts, no divisions),
+  // and all but the copies is done before waiting for the stage.
+  constexpr int kT = tile_tokens(DIM), kQRow = q_row_bytes(DIM);
+  constexpr int kLogT = kT == 64 ? 6 : 5;
+  static_assert((1 << kLogT) == kT, "tile tokens are a power of two");
+  constexpr int PF = AttnSmem::kIdTiles, kRow = AttnSmem::kIdRow, kStride = AttnSmem::kIdStride;
+  static_assert(kStride * 4 % 128 == 0, "ring rows must start 128-byte aligned");
+  static_assert((PF & (PF - 1)) == 0, "ring rows are a power of two");
+  constexpr int kMaxSub = kT / 8;  // boxes per tile at the smallest block size
+  static_assert(kMaxSub + 3 <= kRow, "a tile's ids fit one row after rounding down to 16 bytes");
   if (start >= end) return;
-  const int B = p.B, Hkv = p.Hkv, G = p.G, bs = p.block_size;
-  const int sub_tok = bs < kT ? bs : kT;  // tokens per box
-  const int nsub = kT / sub_tok;          // boxes per 64-dim column of a tile
-  const uint32_t sub_bytes = (uint32_t)sub_tok * 128 * (DIM / 64);  // one box row of K (or V)
-  const long long n_box = (end - start) * nsub;
+  const int B = p.B, Hkv = p.Hkv, G = p.G;
+  const int lbs = p.block_shift;
+  const int lsub = lbs < kLogT ? lbs : kLogT;  // log2 of the tokens per box
+  const int nsub = 1 << (kLogT - lsub);        // boxes per 64-dim column of a tile
+  const uint32_t sub_bytes = (128u * (DIM / 64)) << lsub;  // one box row of K (or V)
+  const unsigned nblk = (unsigned)p.num_blocks;
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
-  auto lookup = [&](long long i) -> int {  // block id of box i (0 when the box is not loaded)
-    if (i >= n_box) return 0;
-    const long long x = start + i / nsub;
-    const Cursor c = cursor_at(x, prefix, B, Hkv);
-    const int t = c.j * kT + (int)(i % nsub) * sub_tok;
-    if (t >= lens[c.b]) return 0;
-    int blk = __ldg(p.block_table + (long long)c.b * p.bt_stride + t / bs);
-    if (blk < 0 || blk >= p.num_blocks) {
-      atomicOr(p.err, kErrBlockTable);
-      blk = p.num_blocks;
-    }
-    return blk;
+  auto id_bar = [&](int k) { return smem_u32(bars + 2 * S + k); };
+  // flat table index of a tile's first entry
+  auto entry = [&](const Cursor& a) { return (long long)a.b * p.bt_stride + ((a.j << kLogT) >> lbs); };
+  auto fetch = [&](const Cursor& a, int slot) {
+    mbar_arrive_expect_tx(id_bar(slot), kRow * 4);
+    tma_load_2d(smem_u32(ids + slot * kStride), &p.tm_table, id_bar(slot), (int)(entry(a) & ~3ll), 0);
   };
-  if (lane == 0) {
-    prefetch_tensormap(&p.tm_k);
-    prefetch_tensormap(&p.tm_v);
-  }
+  prefetch_tensormap(&p.tm_k);
+  prefetch_tensormap(&p.tm_v);
+  prefetch_tensormap(&p.tm_table);
   const uint64_t kv_policy = l2_policy_evict_first();
-  int cur = lookup(lane), nxt = lookup(32 + lane);
+  Cursor ca = cursor_at(start, prefix, B, Hkv);  // the tile whose ids were fetched last
+  for (int k = 0; k < PF && start + k < end; ++k) {
+    if (k > 0) cursor_next(ca, prefix, B, Hkv);
+    fetch(ca, k);
+  }
   Cursor c = cursor_at(start, prefix, B, Hkv);
-  long long seg0 = start, i = 0;
+  long long seg0 = start;
   int it = 0;
   for (long long x = start; x < end; ++x, ++it) {
     if (x != start) {
@@ -352,40 +362,52 @@ __device__ void paged_producer(const AttnParams& p, uint32_t ring, uint8_t* q_sl
     }
     const bool with_q = x - seg0 < kGroups;
     const int stage = it % S;
-    const int t0 = c.j * kT;
-    const int n_load = min(nsub, (lens[c.b] - t0 + sub_tok - 1) / sub_tok);  // >= 1: t0 < L
+    const int t0 = c.j << kLogT;
+    // boxes holding tokens of the sequence (>= 1: t0 < L); the first row in the block:
+    // with bs < kT every box starts a block (t0 % bs == 0), with bs >= kT the tile's one
+    // box starts at t0 % bs
+    const int n_load = min(nsub, (lens[c.b] - t0 + (1 << lsub) - 1) >> lsub);
+    const int row = t0 & ((1 << lbs) - 1);
+    const int slot = it & (PF - 1);
+    mbar_wait_bounded(id_bar(slot), (it / PF) & 1, p.err, kErrWaitFull, flags);
+    const int* idr = ids + slot * kStride + (int)(entry(c) & 3);
+    int blk[kMaxSub];
+#pragma unroll
+    for (int s = 0; s < kMaxSub; ++s) blk[s] = idr[s];  // within the row; checked where used
     const uint32_t fb = full_bar(stage);
     const uint32_t kdst = ring + stage * kStageBytes;
-    if (lane == 0) {
-      mbar_wait_bounded(empty_bar(stage), ((it / S) & 1) ^ 1, p.err, kErrWaitEmpty, flags);
-      mbar_arrive_expect_tx(fb, 2 * n_load * sub_bytes + (with_q ? G * DIM * 2 : 0));
-    }
-    __syncwarp();
-    for (int sidx = 0; sidx < nsub; ++sidx, ++i) {
-      if (i > 0 && (i & 31) == 0) {
-        cur = nxt;
-        nxt = lookup(i + 32 + lane);
-      }
-      const int blk = __shfl_sync(0xffffffffu, cur, (int)(i & 31));
-      if (lane == 0 && sidx < n_load) {
-        const int row = (t0 + sidx * sub_tok) % bs;
+    mbar_wait_bounded(empty_bar(stage), ((it / S) & 1) ^ 1, p.err, kErrWaitEmpty, flags);
+    mbar_arrive_expect_tx(fb, 2 * n_load * sub_bytes + (with_q ? G * DIM * 2 : 0));
 #pragma unroll
-        for (int bx = 0; bx < DIM / 64; ++bx) {
-          const uint32_t off = bx * kBox + sidx * sub_tok * 128;
-          tma_load_4d_hint(kdst + off, &p.tm_k, fb, bx * 64, row, c.kvh, blk, kv_policy);
-          tma_load_4d_hint(kdst + kKTileBytes + off, &p.tm_v, fb, bx * 64, row, c.kvh, blk, kv_policy);
-        }
+    for (int s = 0; s < kMaxSub; ++s) {
+      if (s >= n_load) break;
+      int bk = blk[s];
+      if ((unsigned)bk >= nblk) {
+        atomicOr(p.err, kErrBlockTable);
+        bk = (int)nblk;
       }
+      // one copy per tensor: box s = all D/64 dim boxes of its rows ([box][dim box][rows])
+      const uint32_t off = (uint32_t)(s * 128 * (DIM / 64)) << lsub;
+      tma_load_5d_hint(kdst + off, &p.tm_k, fb, 0, row, 0, c.kvh, bk, kv_policy);
+      tma_load_5d_hint(kdst + kKTileBytes + off, &p.tm_v, fb, 0, row, 0, c.kvh, bk, kv_policy);
     }
-    if (with_q && lane == 0) {
+    if (with_q) {
       const uint32_t qdst = smem_u32(q_slots + stage * q_slot);
       const __nv_bfloat16* qsrc = p.q + (long long)c.b * p.q_sb + (long long)(c.kvh * G) * p.q_sh;
       for (int h = 0; h < G; ++h) bulk_load(qdst + h * kQRow, qsrc + (long long)h * p.q_sh, DIM * 2, fb);
     }
+    // ids of tile x + PF into the row this tile has just read. The row's reads have
+    // completed: their values are operands of the copies issued above, which precede
+    // this refill in program order. (A proxy fence here would also wait for the copies
+    // in flight.)
+    if (x + PF < end) {
+      cursor_next(ca, prefix, B, Hkv);
+      fetch(ca, slot);
+    }
   }
-  if (lane == 0)  // do not leave with copies in flight
-    for (int k = it > S ? it - S : 0; k < it; ++k)
-      mbar_wait_bounded(full_bar(k % S), (k / S) & 1, p.err, kErrWaitDrain, nullptr, kWaitLimitNs / 10);
+  // do not leave with copies in flight (every id row fetched was waited for above)
+  for (int k = it > S ? it - S : 0; k < it; ++k)
+    mbar_wait_bounded(full_bar(k % S), (k / S) & 1, p.err, kErrWaitDrain, nullptr, kWaitLimitNs / 10);
 }
 
 template <int NB, bool SCORES, int S, int NPAD, int DIM, bool PAGED = false>
@@ -395,7 +417,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   static_assert(DIM == kHeadDim || (kWide && !kFused), "head dim 128, or 256 without the fused step");
   static_assert(!PAGED || (!kFused && !SCORES), "the paged variant computes attention only");
   constexpr int kT = tile_tokens(DIM);    // tokens per tile
-  constexpr int kBox = box_bytes(DIM);    // one 64-dim box of a tile
   constexpr int kQRow = q_row_bytes(DIM);
   constexpr int kKs = DIM / 16;           // k-steps of QK^T
   constexpr int kTmemCols = NPAD <= 16 ? 32 : 2 * NPAD;  // two accumulator regions
@@ -425,6 +446,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), kGroupWarps);
+    }
+    if (PAGED) {  // rows of the block-id ring
+      for (int s = 0; s < AttnSmem::kIdTiles; ++s) mbar_init(smem_u32(bars + 2 * S + s), 1);
     }
     if (kFused) {
       for (int s = 0; s < 8; ++s) {
@@ -485,7 +509,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   if (warp == kGroups * kGroupWarps) {
     // ------------------------------------------------------------ producer
     if constexpr (PAGED) {
-      paged_producer<S, DIM>(p, ring, q_slots, kFixed.q_slot(), bars, flags, prefix, lens, start, end, lane);
+      if (lane == 0)
+        paged_producer<S, DIM>(p, ring, q_slots, kFixed.q_slot(), bars, flags, prefix, lens,
+                               reinterpret_cast<int*>(smem + lay.off_ids()), start, end);
     } else if (lane == 0) {
      int it = 0;
      if (start < end) {
@@ -516,14 +542,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
         mbar_arrive_expect_tx(fb, bytes);
         const uint32_t kdst = ring + stage * kStageBytes;
         const int t0 = c.j * kT;
-#pragma unroll
-        for (int bx = 0; bx < DIM / 64; ++bx)
-          tma_load_4d_hint(kdst + bx * kBox, &p.tm_k, fb, bx * 64, t0, c.kvh, c.b, kv_policy);
-        if (!SCORES) {
-#pragma unroll
-          for (int bx = 0; bx < DIM / 64; ++bx)
-            tma_load_4d_hint(kdst + kKTileBytes + bx * kBox, &p.tm_v, fb, bx * 64, t0, c.kvh, c.b, kv_policy);
-        }
+        tma_load_5d_hint(kdst, &p.tm_k, fb, 0, t0, 0, c.kvh, c.b, kv_policy);  // all D/64 boxes at once
+        if (!SCORES) tma_load_5d_hint(kdst + kKTileBytes, &p.tm_v, fb, 0, t0, 0, c.kvh, c.b, kv_policy);
         for (long long todo = min(pf_piece, pf_end - pf_next); todo > 0;) {
           const long long n = min(todo, 32768ll);
           bulk_prefetch_l2(p.prefetch + pf_next, (uint32_t)n, pf_policy);
@@ -573,6 +593,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
     // this warp's first token inside a stage, and (D = 256) its 128-dim half of O
     const int tb = kWide ? (wg >> 1) * 16 : wg * 16;
     const int dh = kWide ? (wg & 1) : 0;
+    // Tile layout in shared memory: [box][dim box][box rows][128 B], one box = the rows
+    // one copy brings (the whole tile, or a paged block smaller than a tile). Byte offset
+    // of a row inside its dim box, and the distance between dim boxes:
+    constexpr int kLogT = kT == 64 ? 6 : 5;
+    const int lbox = PAGED ? min(p.block_shift, kLogT) : kLogT;  // log2 rows per box
+    const uint32_t dbox = 128u << lbox;
+    auto row_off = [&](int r) {
+      return ((uint32_t)((r >> lbox) * (DIM / 64)) << (lbox + 7)) + ((uint32_t)(r & ((1 << lbox) - 1)) << 7);
+    };
+    const uint32_t qk_row = row_off(tb + (lane & 7) + ((lane >> 3) & 1) * 8);  // ldmatrix rows of S^T
+    const uint32_t pv_row = row_off(tb + (lane & 7) + ((lane >> 4) & 1) * 8);  // ldmatrix.trans rows of V
     const float sl2 = p.scale_log2;
     Cursor c;
     if (start < end) c = cursor_at(start, prefix, B, Hkv);
@@ -611,11 +642,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
 #pragma unroll
             for (int i = 0; i < 4; ++i) se[nb][i] = so[nb][i] = 0.f;
           {
-            const int row = tb + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
             for (int ks = 0; ks < kKs; ++ks) {
               const int chunk = 2 * (ks & 3) + (lane >> 4);
-              const uint32_t addr = kbase + (ks >> 2) * kBox + row * 128 + ((chunk ^ (lane & 7)) << 4);
+              const uint32_t addr = kbase + (ks >> 2) * dbox + qk_row + ((chunk ^ (lane & 7)) << 4);
               uint32_t a[4];
               ldsm_x4(addr, a[0], a[1], a[2], a[3]);
 #pragma unroll
@@ -679,11 +709,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
             // ---- O^T[128 dims (of half dh)][8*NB heads] += V_tile^T . P^T
             const uint32_t vbase = kbase + kKTileBytes;
             const int jm = lane >> 3;
-            const int row = tb + (lane & 7) + (jm >> 1) * 8;
 #pragma unroll
             for (int mb = 0; mb < 8; ++mb) {
               const int chunk = 2 * (mb & 3) + (jm & 1);
-              const uint32_t addr = vbase + (dh * 2 + (mb >> 2)) * kBox + row * 128 + ((chunk ^ (lane & 7)) << 4);
+              const uint32_t addr = vbase + (dh * 2 + (mb >> 2)) * dbox + pv_row + ((chunk ^ (lane & 7)) << 4);
               uint32_t a[4];
               ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
               if (vw < 16) {  // rows past the sequence may hold anything; P is 0 there

@@ -56,7 +56,13 @@ struct AttnSmem {
   __host__ __device__ constexpr size_t off_flags() const { return off_bars() + (2 * stages + 18) * 8; }
   __host__ __device__ constexpr size_t off_prefix() const { return off_flags() + 16; }
   __host__ __device__ constexpr size_t off_lens() const { return off_prefix() + (size_t)(batch + 1) * 4; }
-  __host__ __device__ constexpr size_t total() const { return 1024 + off_lens() + (size_t)batch * 4; }
+  // paged caches: kIdTiles rows of 16 block ids (one 64-byte TMA box per tile), rows
+  // 128 bytes apart (a tensor copy's shared-memory destination is 128-byte aligned)
+  __host__ __device__ constexpr size_t off_ids() const { return (off_lens() + (size_t)batch * 4 + 127) & ~(size_t)127; }
+  __host__ __device__ constexpr size_t total() const { return 1024 + off_ids() + kIdTiles * kIdStride * 4; }
+  static constexpr int kIdTiles = 8;
+  static constexpr int kIdRow = 16;     // entries a row receives
+  static constexpr int kIdStride = 32;  // entries between rows (128 bytes)
 };
 
 constexpr size_t kMaxDynSmem = 232448;  // 227 KB per CTA on sm_100-class GPUs
@@ -111,12 +117,14 @@ struct AttnParams {
   const int* block_table;
   long long bt_stride;
   int block_size, num_blocks;
+  int block_shift;       // log2(block_size)
+  CUtensorMap tm_table;  // the table as one flat int32 array (one row), box 16 entries
 };
 
-// Paged caches: a block size the tiles can be cut into, or that holds whole tiles.
+// Paged caches: a power of two from 8 tokens (tiles are cut into blocks, or blocks hold
+// whole tiles; the producer's index arithmetic is shifts and masks).
 __host__ __device__ constexpr bool paged_block_ok(int block_size, int dim) {
-  return block_size >= 8 && (block_size % tile_tokens(dim) == 0 ||
-                             (tile_tokens(dim) % block_size == 0 && block_size % 8 == 0));
+  return block_size >= 8 && block_size <= (1 << 20) && (block_size & (block_size - 1)) == 0 && dim > 0;
 }
 
 constexpr int kProjWBytes = 2 * 64 * 128;  // one stage of W_o: 128 columns x 64 k-rows

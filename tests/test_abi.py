@@ -198,6 +198,8 @@ BAD_PAGED = [
     ("block_size_24", dict(kp=desc([10, 2, 24, 128]), vp=desc([10, 2, 24, 128])), UNSUP),
     ("block_size_4", dict(kp=desc([10, 2, 4, 128]), vp=desc([10, 2, 4, 128])), UNSUP),
     ("block_size_96", dict(kp=desc([10, 2, 96, 128]), vp=desc([10, 2, 96, 128])), UNSUP),
+    ("block_size_192", dict(kp=desc([10, 2, 192, 128]), vp=desc([10, 2, 192, 128])), UNSUP),
+    ("table_not_16_aligned", dict(table=desc([2, 4], binding.DA_DTYPE_I32, addr=FAKE + 4)), ALIGN),
     ("d256_block_size_48", dict(q=desc([2, 8, 256]), kp=desc([10, 2, 48, 256]), vp=desc([10, 2, 48, 256]),
                                 w=desc([8 * 256, 256]), attn=desc([2, 8, 256])), UNSUP),
     ("table_dtype", dict(table=desc([2, 4], binding.DA_DTYPE_F32)), DTYPE),
@@ -226,8 +228,8 @@ def test_paged_rejects(lib, name, over, code):
 @cpu_only
 def test_paged_accepts_valid_block_sizes_on_the_host(lib):
     """Valid shapes pass validation; with B = 0 nothing is launched."""
-    for D, bs in ((128, 8), (128, 16), (128, 32), (128, 64), (128, 192), (256, 8), (256, 16), (256, 32),
-                  (256, 96)):
+    for D, bs in ((128, 8), (128, 16), (128, 32), (128, 64), (128, 4096), (256, 8), (256, 16), (256, 32),
+                  (256, 128)):
         a = paged_args(B=0, D=D, bs=bs)
         for key in ("q", "table", "lens", "out", "attn"):
             a[key].data = None
