@@ -17,12 +17,13 @@ import torch
 
 from . import build as _build
 
-DA_DTYPE_BF16, DA_DTYPE_F32, DA_DTYPE_I32 = 1, 2, 3
-_DTYPES = {torch.bfloat16: DA_DTYPE_BF16, torch.float32: DA_DTYPE_F32, torch.int32: DA_DTYPE_I32}
+DA_DTYPE_BF16, DA_DTYPE_F32, DA_DTYPE_I32, DA_DTYPE_E4M3 = 1, 2, 3, 4
+_DTYPES = {torch.bfloat16: DA_DTYPE_BF16, torch.float32: DA_DTYPE_F32, torch.int32: DA_DTYPE_I32,
+           torch.float8_e4m3fn: DA_DTYPE_E4M3}
 
 # every symbol declared in include/decode_attn.h
 EXPORTS = ("decode_attn_fwd", "decode_attn_only", "decode_attn_only_noalloc", "decode_attn_fwd_paged",
-           "decode_attn_only_paged", "decode_attn_scores", "decode_attn_oproj", "decode_attn_set_option", "decode_attn_get_option", "decode_attn_device_error",
+           "decode_attn_only_paged", "decode_attn_fwd_fp8", "decode_attn_only_fp8", "decode_attn_scores", "decode_attn_oproj", "decode_attn_set_option", "decode_attn_get_option", "decode_attn_device_error",
            "decode_attn_release", "decode_attn_status_str")
 
 
@@ -57,6 +58,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             lib.decode_attn_only_noalloc.argtypes = [P, P, P, P, P, f32, vp]
             lib.decode_attn_fwd_paged.argtypes = [P, P, P, P, P, P, P, f32, vp]
             lib.decode_attn_only_paged.argtypes = [P, P, P, P, P, P, f32, vp]
+            lib.decode_attn_fwd_fp8.argtypes = [P, P, P, P, P, P, f32, f32, f32, vp]
+            lib.decode_attn_only_fp8.argtypes = [P, P, P, P, P, f32, f32, f32, vp]
             lib.decode_attn_scores.argtypes = [P, P, P, P, vp]
             lib.decode_attn_oproj.argtypes = [P, P, P, vp]
             lib.decode_attn_set_option.argtypes = [ctypes.c_char_p, i64]
@@ -158,6 +161,27 @@ def decode_attn_only_paged(q, k_pages, v_pages, block_table, seq_lens, attn_out,
     ds = [describe(x) for x in (q, k_pages, v_pages, block_table, seq_lens, attn_out)]
     _check("decode_attn_only_paged",
            lib.decode_attn_only_paged(*[_ref(d) for d in ds], float(scale), _stream(stream)))
+    return attn_out
+
+
+def decode_attn_fwd_fp8(q, k_cache, v_cache, seq_lens, o_weight, out, scale: float, k_scale: float, v_scale: float,
+                        stream=None) -> torch.Tensor:
+    """decode_attn_fwd over an fp8 cache: k_cache / v_cache torch.float8_e4m3fn, the keys
+    and values being k_cache * k_scale and v_cache * v_scale; returns ``out``."""
+    lib = load()
+    ds = [describe(x) for x in (q, k_cache, v_cache, seq_lens, o_weight, out)]
+    _check("decode_attn_fwd_fp8", lib.decode_attn_fwd_fp8(*[_ref(d) for d in ds], float(scale), float(k_scale),
+                                                          float(v_scale), _stream(stream)))
+    return out
+
+
+def decode_attn_only_fp8(q, k_cache, v_cache, seq_lens, attn_out, scale: float, k_scale: float, v_scale: float,
+                         stream=None) -> torch.Tensor:
+    """decode_attn_only over an fp8 cache (see decode_attn_fwd_fp8); returns ``attn_out``."""
+    lib = load()
+    ds = [describe(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
+    _check("decode_attn_only_fp8", lib.decode_attn_only_fp8(*[_ref(d) for d in ds], float(scale), float(k_scale),
+                                                            float(v_scale), _stream(stream)))
     return attn_out
 
 

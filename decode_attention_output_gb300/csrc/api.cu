@@ -129,20 +129,24 @@ EncodeTiledFn encode_fn() {
 // batch (or block)}. One box = 64 dims x box_tokens tokens x all D/64 dim boxes, which
 // lands in shared memory as D/64 consecutive 64-dim boxes of box_tokens rows (128-byte
 // rows, 128-byte swizzle): one copy per tile and tensor (box_tokens 0: tile_tokens(D)).
+// An fp8 (e4m3) cache is mapped the same way with 128-dim boxes (128-byte rows): at
+// D = 128 a tile is one box of 64 tokens x 128 bytes.
 int encode_kv_map(CUtensorMap* map, const da_tensor_t* t, int box_tokens = 0) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return DA_ERR_CUDA;
   const int64_t B = t->shape[0], H = t->shape[1], L = t->shape[2], D = t->shape[3];
+  const int64_t es = t->dtype == DA_DTYPE_E4M3 ? 1 : 2, inner = 128 / es;  // elements per 128-byte box row
   // a stride of an extent-1 dimension is never used; give it a harmless legal value
   const int64_t st = L == 1 ? D : t->stride[2];
   const int64_t sh = H == 1 ? st * L : t->stride[1];
   const int64_t sb = B == 1 ? sh * H : t->stride[0];
-  cuuint64_t dims[5] = {64, (cuuint64_t)L, (cuuint64_t)(D / 64), (cuuint64_t)H, (cuuint64_t)B};
-  cuuint64_t strides[4] = {(cuuint64_t)st * 2, 128, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
-  cuuint32_t box[5] = {64, (cuuint32_t)(box_tokens > 0 ? box_tokens : tile_tokens((int)D)), (cuuint32_t)(D / 64),
-                       1, 1};
+  cuuint64_t dims[5] = {(cuuint64_t)inner, (cuuint64_t)L, (cuuint64_t)(D / inner), (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[4] = {(cuuint64_t)(st * es), 128, (cuuint64_t)(sh * es), (cuuint64_t)(sb * es)};
+  cuuint32_t box[5] = {(cuuint32_t)inner, (cuuint32_t)(box_tokens > 0 ? box_tokens : tile_tokens((int)D)),
+                       (cuuint32_t)(D / inner), 1, 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, t->data, dims, strides, box, estr,
+  const CUtensorMapDataType type = es == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(map, type, 5, t->data, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_UNSUPPORTED;
@@ -181,7 +185,7 @@ int encode_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
 // --------------------------------------------------------------- validation
 enum Use { kInput16, kOutput };  // inputs feed TMA / 16-byte loads, outputs take scalar stores
 
-int elem_size(int dtype) { return dtype == DA_DTYPE_BF16 ? 2 : 4; }
+int elem_size(int dtype) { return dtype == DA_DTYPE_BF16 ? 2 : (dtype == DA_DTYPE_E4M3 ? 1 : 4); }
 
 int check_tensor(const da_tensor_t* t, int dtype, int ndim, Use use) {
   if (!t) return DA_ERR_NULL;
@@ -199,7 +203,7 @@ int check_tensor(const da_tensor_t* t, int dtype, int ndim, Use use) {
   if (use == kInput16) {
     if (addr % 16) return DA_ERR_ALIGN;
     for (int i = 0; i < ndim - 1; ++i)
-      if (t->shape[i] > 1 && (t->stride[i] <= 0 || t->stride[i] % 8)) return DA_ERR_STRIDE;
+      if (t->shape[i] > 1 && (t->stride[i] <= 0 || (t->stride[i] * elem_size(dtype)) % 16)) return DA_ERR_STRIDE;
   } else {
     if (addr % elem_size(dtype)) return DA_ERR_ALIGN;
     for (int i = 0; i < ndim - 1; ++i)
@@ -219,16 +223,17 @@ struct AttnShape {
 };
 
 int check_attention_inputs(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t* v,
-                           const da_tensor_t* lens, bool need_v, AttnShape* s) {
+                           const da_tensor_t* lens, bool need_v, AttnShape* s, int kv_dtype = DA_DTYPE_BF16) {
   DA_TRY(check_tensor(q, DA_DTYPE_BF16, 3, kInput16));
-  DA_TRY(check_tensor(k, DA_DTYPE_BF16, 4, kInput16));
-  if (need_v) DA_TRY(check_tensor(v, DA_DTYPE_BF16, 4, kInput16));
+  DA_TRY(check_tensor(k, kv_dtype, 4, kInput16));
+  if (need_v) DA_TRY(check_tensor(v, kv_dtype, 4, kInput16));
   if (!lens) return DA_ERR_NULL;
   if (lens->dtype != DA_DTYPE_I32) return DA_ERR_DTYPE;
   if (lens->ndim != 1) return DA_ERR_SHAPE;
   const int64_t B = q->shape[0], Hq = q->shape[1], Hkv = k->shape[1], Lcap = k->shape[2], D = q->shape[2];
   if (k->shape[3] != D) return DA_ERR_SHAPE;
   if (D != kHeadDim && D != kHeadDimWide) return DA_ERR_SHAPE;
+  if (kv_dtype == DA_DTYPE_E4M3 && D != kHeadDim) return DA_ERR_UNSUPPORTED;  // fp8 caches: D = 128
   if (k->shape[0] != B || lens->shape[0] != B) return DA_ERR_SHAPE;
   if (need_v)
     for (int i = 0; i < 4; ++i)
@@ -477,6 +482,11 @@ FusedPlan plan_fused(const AttnShape& s, int K, int N, const AttnPlan& ap, const
   return f;
 }
 
+// Scales of an fp8 (e4m3) cache: K = k_cache * k, V = v_cache * v.
+struct KvScales {
+  float k, v;
+};
+
 struct FusedArgs {
   const FusedPlan* plan;
   const da_tensor_t* w;
@@ -489,7 +499,8 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
                   const AttnShape& s, const AttnPlan& pl, char* ws, char* scratch, __nv_bfloat16* attn,
                   long long a_sb, long long a_sh, float* scores, long long s_sb, long long s_sh, float scale,
                   cudaStream_t stream, const void* prefetch = nullptr, long long prefetch_bytes = 0,
-                  const FusedArgs* fused = nullptr, const PagedShape* paged = nullptr) {
+                  const FusedArgs* fused = nullptr, const PagedShape* paged = nullptr,
+                  const KvScales* kv8 = nullptr) {
   AttnParams p;
   memset(&p, 0, sizeof(p));
   if (fused) {
@@ -538,14 +549,18 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
   p.G = s.G;
   p.Lcap = s.Lcap;
   p.gpad = pl.gpad;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  // scores are scaled in the exp2 domain; an fp8 cache's k_scale folds in there
+  p.scale_log2 = scale * (kv8 ? kv8->k : 1.f) * 1.4426950408889634f;
+  p.k_scale = kv8 ? kv8->k : 1.f;
+  p.v_scale = kv8 ? kv8->v : 1.f;
   p.stages = (int)options_snapshot().attn_stages;
   p.attn_workers = fused ? fused->plan->attn_workers : pl.grid;
   p.prefetch = static_cast<const char*>(prefetch);
   p.prefetch_bytes = prefetch ? (prefetch_bytes & ~15ll) : 0;
   const cudaError_t e =
-      paged ? launch_attention_paged(p, pl.grid, pl.nb, s.D, stream)
-            : launch_attention(p, pl.grid, pl.nb, s.D, scores != nullptr, stream, fused ? fused->plan->npad : 0);
+      kv8     ? launch_attention_fp8(p, pl.grid, pl.nb, stream)
+      : paged ? launch_attention_paged(p, pl.grid, pl.nb, s.D, stream)
+              : launch_attention(p, pl.grid, pl.nb, s.D, scores != nullptr, stream, fused ? fused->plan->npad : 0);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
     cudaGetLastError();
     return DA_ERR_UNSUPPORTED;  // the caller falls back to two launches
@@ -556,7 +571,7 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
 // decode_attn_only / decode_attn_only_paged after their input checks.
 int only_checked(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t* v, const da_tensor_t* seq_lens,
                  const da_tensor_t* attn_out, float scale, void* stream, const AttnShape& s,
-                 const PagedShape* paged) {
+                 const PagedShape* paged, const KvScales* kv8 = nullptr) {
   DA_TRY(check_tensor(attn_out, DA_DTYPE_BF16, 3, kOutput));
   if (attn_out->shape[0] != s.B || attn_out->shape[1] != s.Hq || attn_out->shape[2] != s.D)
     return DA_ERR_SHAPE;
@@ -569,14 +584,14 @@ int only_checked(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t* 
   DA_TRY(workspace_get(pl.bytes, st, &ws));
   return run_attention(q, k, v, seq_lens, s, pl, ws, ws + kHeaderBytes,
                        static_cast<__nv_bfloat16*>(attn_out->data), attn_out->stride[0], attn_out->stride[1],
-                       nullptr, 0, 0, scale, st, nullptr, 0, nullptr, paged);
+                       nullptr, 0, 0, scale, st, nullptr, 0, nullptr, paged, kv8);
 }
 
 // decode_attn_fwd / decode_attn_fwd_paged after their input checks. The fused step is
 // built for a contiguous cache at head dim 128; everything else takes two launches.
 int fwd_checked(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
                 const da_tensor_t* seq_lens, const da_tensor_t* o_weight, const da_tensor_t* out, float scale,
-                void* stream, const AttnShape& s, const PagedShape* paged) {
+                void* stream, const AttnShape& s, const PagedShape* paged, const KvScales* kv8 = nullptr) {
   DA_TRY(check_tensor(o_weight, DA_DTYPE_BF16, 2, kInput16));
   DA_TRY(check_tensor(out, DA_DTYPE_BF16, 2, kOutput));
   const int64_t K = (int64_t)s.Hq * s.D, N = o_weight->shape[1];
@@ -589,7 +604,7 @@ int fwd_checked(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tenso
   const AttnPlan ap = plan_attention(s, o);
   const size_t attn_bytes = align_up((size_t)s.B * K * 2, 256);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const FusedPlan fp = paged ? FusedPlan() : plan_fused(s, (int)K, (int)N, ap, o);
+  const FusedPlan fp = (paged || kv8) ? FusedPlan() : plan_fused(s, (int)K, (int)N, ap, o);
   if (fp.ok) {  // one launch: attention, grid barrier, projection
     char* ws = nullptr;
     DA_TRY(workspace_get(ap.bytes + attn_bytes + fp.part_bytes, st, &ws));
@@ -609,7 +624,7 @@ int fwd_checked(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tenso
   // W_o span: rows 0..K-1 of stride w_sk, the last row N wide
   const long long w_span = ((long long)(K - 1) * o_weight->stride[0] + N) * 2;
   DA_TRY(run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, s.D, nullptr, 0, 0, scale,
-                       st, o.l2_prefetch ? o_weight->data : nullptr, w_span, nullptr, paged));
+                       st, o.l2_prefetch ? o_weight->data : nullptr, w_span, nullptr, paged, kv8));
   return run_projection(attn, K, o_weight, out, s.B, (int)K, (int)N, ws, scratch + ap.bytes + attn_bytes, gp,
                         o.pdl != 0, st);
 }
@@ -786,6 +801,26 @@ int decode_attn_fwd(const da_tensor_t* q, const da_tensor_t* k_cache, const da_t
   AttnShape s;
   DA_TRY(check_attention_inputs(q, k_cache, v_cache, seq_lens, true, &s));
   return fwd_checked(q, k_cache, v_cache, seq_lens, o_weight, out, scale, stream, s, nullptr);
+}
+
+int decode_attn_fwd_fp8(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
+                        const da_tensor_t* seq_lens, const da_tensor_t* o_weight, const da_tensor_t* out, float scale,
+                        float k_scale, float v_scale, void* stream) {
+  AttnShape s;
+  DA_TRY(check_attention_inputs(q, k_cache, v_cache, seq_lens, true, &s, DA_DTYPE_E4M3));
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return DA_ERR_UNSUPPORTED;
+  const KvScales kv{k_scale, v_scale};
+  return fwd_checked(q, k_cache, v_cache, seq_lens, o_weight, out, scale, stream, s, nullptr, &kv);
+}
+
+int decode_attn_only_fp8(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
+                         const da_tensor_t* seq_lens, const da_tensor_t* attn_out, float scale, float k_scale,
+                         float v_scale, void* stream) {
+  AttnShape s;
+  DA_TRY(check_attention_inputs(q, k_cache, v_cache, seq_lens, true, &s, DA_DTYPE_E4M3));
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return DA_ERR_UNSUPPORTED;
+  const KvScales kv{k_scale, v_scale};
+  return only_checked(q, k_cache, v_cache, seq_lens, attn_out, scale, stream, s, nullptr, &kv);
 }
 
 int decode_attn_fwd_paged(const da_tensor_t* q, const da_tensor_t* k_pages, const da_tensor_t* v_pages,

@@ -410,12 +410,17 @@ __device__ __forceinline__ void paged_producer(const AttnParams& p, uint32_t rin
     mbar_wait_bounded(full_bar(k % S), (k / S) & 1, p.err, kErrWaitDrain, nullptr, kWaitLimitNs / 10);
 }
 
-template <int NB, bool SCORES, int S, int NPAD, int DIM, bool PAGED = false>
+template <int NB, bool SCORES, int S, int NPAD, int DIM, bool PAGED = false, bool KV8 = false>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __grid_constant__ AttnParams p) {
   constexpr bool kFused = NPAD > 0;
   constexpr bool kWide = DIM == kHeadDimWide;
   static_assert(DIM == kHeadDim || (kWide && !kFused), "head dim 128, or 256 without the fused step");
   static_assert(!PAGED || (!kFused && !SCORES), "the paged variant computes attention only");
+  static_assert(!KV8 || (DIM == kHeadDim && !kFused && !SCORES && !PAGED),
+                "the fp8-cache variant: head dim 128, attention only, contiguous cache");
+  // Stage: K tile then V tile (bf16: 32 KB; fp8: 64 tokens x 128 B each, 16 KB).
+  constexpr int kSB = KV8 ? kStageBytes8 : kStageBytes;
+  constexpr int kKB = kSB / 2;
   constexpr int kT = tile_tokens(DIM);    // tokens per tile
   constexpr int kQRow = q_row_bytes(DIM);
   constexpr int kKs = DIM / 16;           // k-steps of QK^T
@@ -423,8 +428,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   constexpr int HP = 8 * NB;  // heads per group, padded to the MMA width
   const int B = p.B, Hkv = p.Hkv, G = p.G, Lcap = p.Lcap;
   static_assert(S % kGroups == 0, "a stage must always be consumed by the same group");
-  constexpr AttnSmem kFixed(NB, 0, S, DIM);  // offsets that do not depend on the batch size
-  const AttnSmem lay(NB, B, S, DIM);
+  constexpr AttnSmem kFixed(NB, 0, S, DIM, kSB);  // offsets that do not depend on the batch size
+  const AttnSmem lay(NB, B, S, DIM, kSB);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -537,13 +542,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
         const uint32_t ph = (it / S) & 1;
         mbar_wait_bounded(empty_bar(stage), ph ^ 1, p.err, kErrWaitEmpty, flags);
         const uint32_t fb = full_bar(stage);
-        uint32_t bytes = SCORES ? kKTileBytes : kStageBytes;
+        uint32_t bytes = SCORES ? kKB : kSB;
         if (with_q) bytes += G * DIM * 2;
         mbar_arrive_expect_tx(fb, bytes);
-        const uint32_t kdst = ring + stage * kStageBytes;
+        const uint32_t kdst = ring + stage * kSB;
         const int t0 = c.j * kT;
         tma_load_5d_hint(kdst, &p.tm_k, fb, 0, t0, 0, c.kvh, c.b, kv_policy);  // all D/64 boxes at once
-        if (!SCORES) tma_load_5d_hint(kdst + kKTileBytes, &p.tm_v, fb, 0, t0, 0, c.kvh, c.b, kv_policy);
+        if (!SCORES) tma_load_5d_hint(kdst + kKB, &p.tm_v, fb, 0, t0, 0, c.kvh, c.b, kv_policy);
         for (long long todo = min(pf_piece, pf_end - pf_next); todo > 0;) {
           const long long n = min(todo, 32768ll);
           bulk_prefetch_l2(p.prefetch + pf_next, (uint32_t)n, pf_policy);
@@ -593,6 +598,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
     // this warp's first token inside a stage, and (D = 256) its 128-dim half of O
     const int tb = kWide ? (wg >> 1) * 16 : wg * 16;
     const int dh = kWide ? (wg & 1) : 0;
+    // dims (within an m-tile of 16) of this lane's accumulator rows g and g+8
+    const int d_lo = KV8 ? 2 * g : g, d_hi = KV8 ? 2 * g + 1 : g + 8;
     // Tile layout in shared memory: [box][dim box][box rows][128 B], one box = the rows
     // one copy brings (the whole tile, or a paged block smaller than a tile). Byte offset
     // of a row inside its dim box, and the distance between dim boxes:
@@ -627,21 +634,51 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
           for (int nb = 0; nb < NB; ++nb) {
 #pragma unroll
             for (int ks = 0; ks < kKs; ++ks) {
-              const uint8_t* row = qs + (nb * 8 + g) * kQRow + (ks * 16 + 2 * t) * 2;
-              qf[nb][ks][0] = *reinterpret_cast<const uint32_t*>(row);
-              qf[nb][ks][1] = *reinterpret_cast<const uint32_t*>(row + 16);
+              if constexpr (KV8) {
+                // k-slots 2t, 2t+1, 2t+8, 2t+9 of step ks hold dims 16ks + 4t .. 4t+3 (the
+                // order in which an fp8 K row reaches this lane); q in f16, same order
+                const uint8_t* row = qs + (nb * 8 + g) * kQRow + (ks * 16 + 4 * t) * 2;
+                const uint2 w = *reinterpret_cast<const uint2*>(row);
+                qf[nb][ks][0] = bf16x2_to_f16x2_clamped(w.x);
+                qf[nb][ks][1] = bf16x2_to_f16x2_clamped(w.y);
+              } else {
+                const uint8_t* row = qs + (nb * 8 + g) * kQRow + (ks * 16 + 2 * t) * 2;
+                qf[nb][ks][0] = *reinterpret_cast<const uint32_t*>(row);
+                qf[nb][ks][1] = *reinterpret_cast<const uint32_t*>(row + 16);
+              }
             }
           }
         }
         if (vw > 0) {
-          const uint32_t kbase = ring + stage * kStageBytes;
+          const uint32_t kbase = ring + stage * kSB;
           // ---- S^T[16 tokens][8*NB heads] = K_tile . Q^T  (fp32, unscaled)
           float se[NB][4], so[NB][4];
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
             for (int i = 0; i < 4; ++i) se[nb][i] = so[nb][i] = 0.f;
-          {
+          if constexpr (KV8) {
+            // fp8 K rows are 128 bytes: one ldmatrix.x4 brings two k-steps (rows tb..+7 and
+            // tb+8..+15 of 16-byte chunks 2kk and 2kk+1); a lane holds 4 dims of a row per
+            // matrix, widened to f16 exactly (the k-slot order of the q fragments)
+            const int row = tb + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int kk = 0; kk < kKs / 2; ++kk) {
+              const int chunk = 2 * kk + (lane >> 4);
+              uint32_t m[4];
+              ldsm_x4(kbase + row * 128 + ((chunk ^ (lane & 7)) << 4), m[0], m[1], m[2], m[3]);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t a[4] = {e4m3x2_to_f16x2(m[2 * h]), e4m3x2_to_f16x2(m[2 * h + 1]),
+                                       e4m3x2_to_f16x2(m[2 * h] >> 16), e4m3x2_to_f16x2(m[2 * h + 1] >> 16)};
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                  if (h) mma_f16_16816(so[nb], a, qf[nb][2 * kk + h][0], qf[nb][2 * kk + h][1]);
+                  else mma_f16_16816(se[nb], a, qf[nb][2 * kk + h][0], qf[nb][2 * kk + h][1]);
+                }
+              }
+            }
+          } else {
 #pragma unroll
             for (int ks = 0; ks < kKs; ++ks) {
               const int chunk = 2 * (ks & 3) + (lane >> 4);
@@ -691,11 +728,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
               const float al0 = fast_exp2(m_run[nb][0] - mn0), al1 = fast_exp2(m_run[nb][1] - mn1);
               m_run[nb][0] = mn0;
               m_run[nb][1] = mn1;
-              const uint32_t r0 = pack_bf16x2(fast_exp2(x0 - mn0), fast_exp2(x1 - mn1));  // token g
-              const uint32_t r1 = pack_bf16x2(fast_exp2(x2 - mn0), fast_exp2(x3 - mn1));  // token g+8
-              // the sum uses the bf16-rounded weights that enter P.V
-              l_run[nb][0] = l_run[nb][0] * al0 + (bf16lo_to_f32(r0) + bf16lo_to_f32(r1));
-              l_run[nb][1] = l_run[nb][1] * al1 + (bf16hi_to_f32(r0) + bf16hi_to_f32(r1));
+              // P in the P.V operand type (bf16; f16 with an fp8 cache); the sum uses the rounded
+              // weights that enter P.V
+              uint32_t r0, r1;
+              if constexpr (KV8) {
+                r0 = pack_f16x2(fast_exp2(x0 - mn0), fast_exp2(x1 - mn1));  // token g
+                r1 = pack_f16x2(fast_exp2(x2 - mn0), fast_exp2(x3 - mn1));  // token g+8
+                l_run[nb][0] = l_run[nb][0] * al0 + (f16lo_to_f32(r0) + f16lo_to_f32(r1));
+                l_run[nb][1] = l_run[nb][1] * al1 + (f16hi_to_f32(r0) + f16hi_to_f32(r1));
+              } else {
+                r0 = pack_bf16x2(fast_exp2(x0 - mn0), fast_exp2(x1 - mn1));  // token g
+                r1 = pack_bf16x2(fast_exp2(x2 - mn0), fast_exp2(x3 - mn1));  // token g+8
+                l_run[nb][0] = l_run[nb][0] * al0 + (bf16lo_to_f32(r0) + bf16lo_to_f32(r1));
+                l_run[nb][1] = l_run[nb][1] * al1 + (bf16hi_to_f32(r0) + bf16hi_to_f32(r1));
+              }
 #pragma unroll
               for (int mb = 0; mb < 8; ++mb) {
                 o[mb][nb][0] *= al0;
@@ -707,7 +753,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
               pb[nb][1] = movmatrix_trans(r1);  // P[head g][tokens 2t+8, 2t+9]
             }
             // ---- O^T[128 dims (of half dh)][8*NB heads] += V_tile^T . P^T
-            const uint32_t vbase = kbase + kKTileBytes;
+            const uint32_t vbase = kbase + kKB;
+            if constexpr (KV8) {
+              // fp8 V rows are 128 bytes. ldmatrix.trans of 16-bit pairs hands a lane tokens
+              // 2t, 2t+1 of dims 2g, 2g+1 (one byte each); a byte permute makes (dim 2g: two
+              // tokens) and (dim 2g+1: two tokens), widened to f16 exactly. So the MMA's rows
+              // g and g+8 of m-tile mb are dims 16mb + 2g and 16mb + 2g + 1.
+              const int row = tb + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+              for (int mp = 0; mp < 4; ++mp) {
+                const int chunk = 2 * mp + (lane >> 4);
+                uint32_t m[4];
+                ldsm_x4_trans(vbase + row * 128 + ((chunk ^ (lane & 7)) << 4), m[0], m[1], m[2], m[3]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  uint32_t lo = m[2 * h], hi = m[2 * h + 1];  // tokens 2t, 2t+1 and 2t+8, 2t+9
+                  if (vw < 16) {  // rows past the sequence may hold anything; P is 0 there
+                    lo = mask_tokens(lo, 2 * t, vw);
+                    hi = mask_tokens(hi, 2 * t + 8, vw);
+                  }
+                  const uint32_t pl = __byte_perm(lo, 0, 0x3120), ph = __byte_perm(hi, 0, 0x3120);
+                  const uint32_t a[4] = {e4m3x2_to_f16x2(pl), e4m3x2_to_f16x2(pl >> 16), e4m3x2_to_f16x2(ph),
+                                         e4m3x2_to_f16x2(ph >> 16)};
+#pragma unroll
+                  for (int nb = 0; nb < NB; ++nb) mma_f16_16816(o[2 * mp + h][nb], a, pb[nb][0], pb[nb][1]);
+                }
+              }
+            } else {
             const int jm = lane >> 3;
 #pragma unroll
             for (int mb = 0; mb < 8; ++mb) {
@@ -723,6 +795,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
               }
 #pragma unroll
               for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(o[mb][nb], a, pb[nb][0], pb[nb][1]);
+            }
             }
           }
         }
@@ -748,10 +821,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
             const int h0 = nb * 8 + 2 * t;
 #pragma unroll
             for (int mb = 0; mb < 8; ++mb) {
-              mo[h0 * kMergeRow + mb * 16 + g] = o[mb][nb][0];
-              mo[(h0 + 1) * kMergeRow + mb * 16 + g] = o[mb][nb][1];
-              mo[h0 * kMergeRow + mb * 16 + g + 8] = o[mb][nb][2];
-              mo[(h0 + 1) * kMergeRow + mb * 16 + g + 8] = o[mb][nb][3];
+              mo[h0 * kMergeRow + mb * 16 + d_lo] = o[mb][nb][0];
+              mo[(h0 + 1) * kMergeRow + mb * 16 + d_lo] = o[mb][nb][1];
+              mo[h0 * kMergeRow + mb * 16 + d_hi] = o[mb][nb][2];
+              mo[(h0 + 1) * kMergeRow + mb * 16 + d_hi] = o[mb][nb][3];
             }
             if (g == 0) {
               ml[h0 * 2] = m_run[nb][0];
@@ -777,8 +850,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
               m_run[nb][cc] = mn;
 #pragma unroll
               for (int mb = 0; mb < 8; ++mb) {
-                o[mb][nb][cc] = o[mb][nb][cc] * a_self + mo[h * kMergeRow + mb * 16 + g] * a_part;
-                o[mb][nb][cc + 2] = o[mb][nb][cc + 2] * a_self + mo[h * kMergeRow + mb * 16 + g + 8] * a_part;
+                o[mb][nb][cc] = o[mb][nb][cc] * a_self + mo[h * kMergeRow + mb * 16 + d_lo] * a_part;
+                o[mb][nb][cc + 2] = o[mb][nb][cc + 2] * a_self + mo[h * kMergeRow + mb * 16 + d_hi] * a_part;
               }
             }
           }
@@ -788,10 +861,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
             const int h0 = nb * 8 + 2 * t;
 #pragma unroll
             for (int mb = 0; mb < 8; ++mb) {
-              mo[h0 * kMergeRow + mb * 16 + g] = o[mb][nb][0];
-              mo[(h0 + 1) * kMergeRow + mb * 16 + g] = o[mb][nb][1];
-              mo[h0 * kMergeRow + mb * 16 + g + 8] = o[mb][nb][2];
-              mo[(h0 + 1) * kMergeRow + mb * 16 + g + 8] = o[mb][nb][3];
+              mo[h0 * kMergeRow + mb * 16 + d_lo] = o[mb][nb][0];
+              mo[(h0 + 1) * kMergeRow + mb * 16 + d_lo] = o[mb][nb][1];
+              mo[h0 * kMergeRow + mb * 16 + d_hi] = o[mb][nb][2];
+              mo[(h0 + 1) * kMergeRow + mb * 16 + d_hi] = o[mb][nb][3];
             }
             if (g == 0) {
               ml[h0 * 2] = m_run[nb][0];
@@ -824,6 +897,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
             lsum += f * merge_ml[(w * HP + h) * 2 + 1];
             acc += f * merge_o[(w * HP + h) * kMergeRow + dl];
           }
+          if constexpr (KV8) acc *= p.v_scale;  // V = v_cache * v_scale (linear through every merge)
           if (n_parts == 1) {
             p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
           } else {
@@ -915,7 +989,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   }
 }
 
-template <int NB, bool SCORES, int S, int NPAD, int DIM, bool PAGED = false>
+template <int NB, bool SCORES, int S, int NPAD, int DIM, bool PAGED = false, bool KV8 = false>
 cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   // The shared-memory opt-in is a per-device function attribute: set it once per device.
   static int configured[64] = {0};
@@ -924,7 +998,7 @@ cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attn_decode_kernel<NB, SCORES, S, NPAD, DIM, PAGED>,
+    e = cudaFuncSetAttribute(attn_decode_kernel<NB, SCORES, S, NPAD, DIM, PAGED, KV8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDynSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
@@ -932,14 +1006,14 @@ cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kAttnThreads);
-  cfg.dynamicSmemBytes = attn_smem_bytes(p.B, NB, S, DIM);
+  cfg.dynamicSmemBytes = attn_smem_bytes(p.B, NB, S, DIM, KV8 ? kStageBytes8 : kStageBytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;  // the fused step's grid barrier needs every CTA resident
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = NPAD > 0 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<NB, SCORES, S, NPAD, DIM, PAGED>, p);
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<NB, SCORES, S, NPAD, DIM, PAGED, KV8>, p);
 }
 
 }  // namespace

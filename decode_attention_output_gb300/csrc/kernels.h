@@ -41,12 +41,13 @@ static_assert(tile_tokens(kHeadDimWide) * kHeadDimWide * 2 == kKTileBytes, "K ti
 // stages = pipeline depth (even, so that a stage always belongs to one consumer group),
 // dim = head dim (128 or 256).
 struct AttnSmem {
-  int nb, batch, stages, dim;
-  __host__ __device__ constexpr AttnSmem(int nb_, int batch_, int stages_, int dim_ = kHeadDim)
-      : nb(nb_), batch(batch_), stages(stages_), dim(dim_) {}
+  int nb, batch, stages, dim, stage_bytes;
+  __host__ __device__ constexpr AttnSmem(int nb_, int batch_, int stages_, int dim_ = kHeadDim,
+                                         int stage_bytes_ = kStageBytes)
+      : nb(nb_), batch(batch_), stages(stages_), dim(dim_), stage_bytes(stage_bytes_) {}
   __host__ __device__ constexpr int heads() const { return 8 * nb; }
   __host__ __device__ constexpr size_t q_slot() const { return (size_t)heads() * q_row_bytes(dim); }
-  __host__ __device__ constexpr size_t off_q() const { return (size_t)stages * kStageBytes; }
+  __host__ __device__ constexpr size_t off_q() const { return (size_t)stages * stage_bytes; }
   __host__ __device__ constexpr size_t off_merge_o() const { return off_q() + stages * q_slot(); }
   __host__ __device__ constexpr size_t off_merge_ml() const {
     return off_merge_o() + (size_t)kGroupWarps * heads() * kMergeRow * 4;
@@ -66,9 +67,15 @@ struct AttnSmem {
 };
 
 constexpr size_t kMaxDynSmem = 232448;  // 227 KB per CTA on sm_100-class GPUs
-constexpr size_t attn_smem_bytes(int batch, int nb, int stages, int dim = kHeadDim) {
-  return AttnSmem(nb, batch, stages, dim).total();
+constexpr size_t attn_smem_bytes(int batch, int nb, int stages, int dim = kHeadDim, int stage_bytes = kStageBytes) {
+  return AttnSmem(nb, batch, stages, dim, stage_bytes).total();
 }
+// fp8 (e4m3) caches: a stage holds 64 tokens x 128 dims x 1 byte of K and of V (16 KB),
+// and the ring has twice the stages, so it spans the same 128 KB.
+constexpr int kStageBytes8 = 16384;
+constexpr int kStages8 = 8;
+static_assert(AttnSmem(2, kMaxBatch, kStages8, kHeadDim, kStageBytes8).total() <= kMaxDynSmem,
+              "attention kernel (fp8 cache) exceeds 227 KB of shared memory");
 static_assert(AttnSmem(2, kMaxBatch, 4).total() <= kMaxDynSmem, "attention kernel exceeds 227 KB of shared memory");
 static_assert(AttnSmem(2, kMaxBatch, 4, kHeadDimWide).total() <= kMaxDynSmem,
               "attention kernel (D = 256) exceeds 227 KB of shared memory");
@@ -119,6 +126,8 @@ struct AttnParams {
   int block_size, num_blocks;
   int block_shift;       // log2(block_size)
   CUtensorMap tm_table;  // the table as one flat int32 array (one row), box 16 entries
+  // fp8 (e4m3) caches only: K = k_cache * k_scale, V = v_cache * v_scale
+  float k_scale, v_scale;
 };
 
 // Paged caches: a power of two from 8 tokens (tiles are cut into blocks, or blocks hold
@@ -144,6 +153,8 @@ cudaError_t launch_attention(const AttnParams& p, int grid, int nb, int dim, boo
 cudaError_t launch_attention_d256(const AttnParams& p, int grid, int nb, bool scores_only, cudaStream_t stream);
 // Attention over a paged cache (p.block_table set), D = 128 or 256.
 cudaError_t launch_attention_paged(const AttnParams& p, int grid, int nb, int dim, cudaStream_t stream);
+// Attention over an fp8 (e4m3) cache, D = 128 (p.k_scale, p.v_scale set).
+cudaError_t launch_attention_fp8(const AttnParams& p, int grid, int nb, cudaStream_t stream);
 
 // ------------------------------------------------------- projection: GEMV path
 constexpr int kGemvThreads = 256;

@@ -23,8 +23,9 @@
  *  - Every tensor argument is a da_tensor_t descriptor. Its data pointer is a
  *    DEVICE pointer owned by the caller; the library never frees or keeps it.
  *  - Strides are in elements. The innermost dimension must be contiguous
- *    (stride 1); every other stride must be a multiple of 8 elements and every
- *    base pointer 16-byte aligned (TMA and 16-byte vector loads need it).
+ *    (stride 1); every other stride of an input must be a multiple of 16 bytes
+ *    (8 bf16 elements, 16 e4m3 elements) and every base pointer 16-byte aligned
+ *    (TMA and 16-byte vector loads need it).
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream). Every call only enqueues work on it and returns; nothing is
  *    synchronised, nothing is copied back to the host.
@@ -52,7 +53,7 @@ extern "C" {
 #endif
 
 /* Element types of da_tensor_t.dtype. */
-enum { DA_DTYPE_BF16 = 1, DA_DTYPE_F32 = 2, DA_DTYPE_I32 = 3 };
+enum { DA_DTYPE_BF16 = 1, DA_DTYPE_F32 = 2, DA_DTYPE_I32 = 3, DA_DTYPE_E4M3 = 4 /* fp8 e4m3 (OCP "fn") */ };
 
 /* A strided view of caller-owned device memory (DLPack-like). */
 typedef struct da_tensor {
@@ -181,6 +182,31 @@ int decode_attn_fwd_paged(const da_tensor_t* q, const da_tensor_t* k_pages, cons
 int decode_attn_only_paged(const da_tensor_t* q, const da_tensor_t* k_pages, const da_tensor_t* v_pages,
                            const da_tensor_t* block_table, const da_tensor_t* seq_lens, const da_tensor_t* attn_out,
                            float scale, void* stream);
+
+/*
+ * decode_attn_fwd_fp8 / decode_attn_only_fp8 -- decode_attn_fwd / decode_attn_only over
+ * an fp8 KV cache: k_cache and v_cache hold e4m3 codes (DA_DTYPE_E4M3, the OCP "fn"
+ * format: 4 exponent bits with bias 7, 3 mantissa bits, no infinities), and the keys and
+ * values are
+ *
+ *   K = k_cache * k_scale,   V = v_cache * v_scale       (one float scale per cache)
+ *
+ * The pages have no fp8 cache; the computation is exactly that of the bf16 entry points
+ * on these K and V. The cache bytes halve; q, o_weight and the outputs stay bf16.
+ *   k_cache, v_cache [B, Hkv, Lcap, 128] e4m3; strides multiples of 16 elements (bytes)
+ *   k_scale, v_scale finite floats (DA_ERR_UNSUPPORTED otherwise)
+ *   other arguments as decode_attn_fwd / decode_attn_only
+ * Head dim 128 only (D = 256 returns DA_ERR_UNSUPPORTED); the fused option does not apply.
+ * The kernels widen the codes to f16 (exact) and multiply them with q rounded to f16,
+ * which is exact for |q| <= 65504; larger |q| is clamped to 65504. The softmax weights
+ * enter P.V as f16 (bf16 on the bf16 path).
+ */
+int decode_attn_fwd_fp8(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
+                        const da_tensor_t* seq_lens, const da_tensor_t* o_weight, const da_tensor_t* out, float scale,
+                        float k_scale, float v_scale, void* stream);
+int decode_attn_only_fp8(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
+                         const da_tensor_t* seq_lens, const da_tensor_t* attn_out, float scale, float k_scale,
+                         float v_scale, void* stream);
 
 /*
  * decode_attn_scores -- the first contraction alone: the page's `scores_fp32`

@@ -89,6 +89,8 @@ class Oracle:
         lib.oracle_decode.restype = ctypes.c_int
         lib.oracle_gather_pages.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _i64, _i64, _p, _p]
         lib.oracle_gather_pages.restype = ctypes.c_int
+        lib.oracle_e4m3_to_bf16.argtypes = [_p, _i64, _p]
+        lib.oracle_e4m3_to_bf16.restype = ctypes.c_int64
         self._lib = lib
 
     def num_threads(self) -> int:
@@ -217,6 +219,27 @@ class Oracle:
         k = self.gather_pages(k_pages, table, seq_lens)
         v = self.gather_pages(v_pages, table, seq_lens)
         return self.decode(q, k, v, seq_lens, w, scale)
+
+
+    # ---- fp8 (e4m3) cache ------------------------------------------------------------------
+    def e4m3_to_bf16_bits(self, codes) -> np.ndarray:
+        """e4m3 codes (uint8) -> bf16 bit patterns of the same values (exact)."""
+        codes = np.ascontiguousarray(codes)
+        if codes.dtype != np.uint8:
+            raise TypeError(f"expected uint8 e4m3 codes, got {codes.dtype}")
+        out = np.zeros(codes.shape, np.uint16)
+        self._lib.oracle_e4m3_to_bf16(_ptr(codes), codes.size, _ptr(out))
+        return out
+
+    def decode_fp8(self, q, k_codes, v_codes, seq_lens, w, scale: float, k_scale: float, v_scale: float):
+        """Whole step over an fp8 cache whose keys and values are k_codes * k_scale and
+        v_codes * v_scale. The codes widen exactly to bf16; k_scale multiplies every
+        score (it joins `scale`) and v_scale every attention output (the projection is
+        linear), so the step is the bf16 one on the widened codes, in fp64."""
+        kb = self.e4m3_to_bf16_bits(k_codes)
+        vb = self.e4m3_to_bf16_bits(v_codes)
+        attn, out = self.decode(q, kb, vb, seq_lens, w, float(scale) * float(k_scale))
+        return attn * float(v_scale), out * float(v_scale)
 
 
 _default: Oracle | None = None

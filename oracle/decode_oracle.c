@@ -309,3 +309,31 @@ int oracle_gather_pages(const uint16_t* pages, int64_t num_blocks, int64_t Hkv, 
   }
   return 0;
 }
+
+/*
+ * oracle_e4m3_to_bf16 -- widens fp8 e4m3 codes (the OCP 8-bit format E4M3 "fn": 1 sign
+ * bit, 4 exponent bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN)
+ * to the bf16 bit patterns of the same values, for the library's fp8-cache entry points
+ * (the pages describe no fp8 cache). Every e4m3 value is a bf16 value, so this is exact:
+ *   exponent field 0:      (-1)^s * m * 2^-9            (subnormals and zeros)
+ *   exponent field e > 0:  (-1)^s * (1 + m / 8) * 2^(e - 7)
+ * NaN codes give the bf16 quiet NaN 0x7fc0 (with the sign). Returns the number of NaN codes.
+ */
+int64_t oracle_e4m3_to_bf16(const uint8_t* in, int64_t n, uint16_t* out) {
+  int64_t nans = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const unsigned b = in[i];
+    const unsigned s = b >> 7, e = (b >> 3) & 15u, m = b & 7u;
+    if (e == 15u && m == 7u) {
+      out[i] = (uint16_t)((s << 15) | 0x7fc0u);
+      ++nans;
+      continue;
+    }
+    const double mag = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+    const float f = (float)(s ? -mag : mag);  /* exact: at most 4 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof(u));
+    out[i] = (uint16_t)(u >> 16);  /* exact: the low 16 bits of u are zero */
+  }
+  return nans;
+}

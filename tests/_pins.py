@@ -505,6 +505,57 @@ def pin_paged_decode_equals_contiguous(orc):
     assert np.array_equal(a1, a0) and np.array_equal(y1, y0)
 
 
+def pin_e4m3_known_values(orc):
+    """e4m3 codes whose values the format's definition fixes by hand (bias 7, 3 mantissa
+    bits, subnormals m * 2^-9, S.1111.111 = NaN)."""
+    table = {0x00: 0.0, 0x80: -0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x30: 0.5,
+             0x38: 1.0, 0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x48: 4.0, 0x58: 16.0, 0x7E: 448.0,
+             0xB8: -1.0, 0xFE: -448.0, 0x77: 240.0, 0x70: 128.0}
+    codes = np.array(sorted(table), np.uint8)
+    got = bits_to_f64(orc.e4m3_to_bf16_bits(codes))
+    for c, g in zip(codes, got):
+        want = table[int(c)]
+        assert g == want and math.copysign(1, g) == math.copysign(1, want), f"code {c:#04x}: {g} != {want}"
+    nan = bits_to_f64(orc.e4m3_to_bf16_bits(np.array([0x7F, 0xFF], np.uint8)))
+    assert np.all(np.isnan(nan)), "S.1111.111 is NaN"
+
+
+def pin_e4m3_all_codes_match_library(orc):
+    """All 256 codes widen to the values torch's float8_e4m3fn conversion gives."""
+    import torch
+
+    codes = np.arange(256, dtype=np.uint8)
+    got = bits_to_f64(orc.e4m3_to_bf16_bits(codes))
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan), "NaN codes"
+    assert np.array_equal(got[~nan], ref[~nan]), "e4m3 values"
+
+
+def pin_fp8_decode_bruteforce(orc):
+    """The fp8-cache step (scales folded into the softmax scale and the outputs) equals a
+    60-digit brute force on the dequantized keys and values, k_codes * k_scale and
+    v_codes * v_scale, computed here from the e4m3 definition independently."""
+    import torch
+
+    rng = np.random.default_rng(51)
+    B, Hq, Hkv, Lcap, N = 1, 4, 2, 5, 16
+    q = rand_bits(rng, (B, Hq, D))
+    kc = rng.integers(0, 256, size=(B, Hkv, Lcap, D)).astype(np.uint8)
+    vc = rng.integers(0, 256, size=(B, Hkv, Lcap, D)).astype(np.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0x3A  # no NaN codes in a valid cache
+    vc[(vc & 0x7F) == 0x7F] = 0x41
+    w = rand_bits(rng, (Hq * D, N), std=1 / math.sqrt(Hq * D))
+    lens = np.array([4], np.int32)
+    scale, k_scale, v_scale = 1 / math.sqrt(D), 0.0123, 0.75
+    attn, y = orc.decode_fp8(q, kc, vc, lens, w, scale, k_scale, v_scale)
+    kf = torch.from_numpy(kc).view(torch.float8_e4m3fn).double().numpy() * k_scale
+    vf = torch.from_numpy(vc).view(torch.float8_e4m3fn).double().numpy() * v_scale
+    ba, by = brute_decode(bits_to_f64(q), kf, vf, lens, bits_to_f64(w), scale)
+    _close(attn, ba, 1e-12, "fp8 attention vs brute force")
+    _close(y, by, 1e-12, "fp8 output vs brute force")
+
+
 PINS = [v for kname, v in sorted(globals().items()) if kname.startswith("pin_") and callable(v)]
 
 

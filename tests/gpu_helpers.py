@@ -41,5 +41,29 @@ def oracle_decode(orc, x: dict, rows=None):
         q, k, v, lens = q[idx], k[idx], v[idx], lens[idx]
     lcap = k.shape[2]
     lens_h = lens.cpu().numpy().astype(np.int64).clip(0, lcap).astype(np.int32)
+    if "k_scale" in x:  # fp8 (e4m3) cache
+        return orc.decode_fp8(synth.to_bits(q), synth.to_bits(k), synth.to_bits(v), lens_h,
+                              synth.to_bits(x["o_weight"]), x["scale"], x["k_scale"], x["v_scale"])
     return orc.decode(synth.to_bits(q), synth.to_bits(k), synth.to_bits(v), lens_h, synth.to_bits(x["o_weight"]),
                       x["scale"])
+
+
+def run_fwd(x, out, stream=None):
+    """decode_attn_fwd, or decode_attn_fwd_fp8 for an e4m3 cache."""
+    import decode_attention_output_gb300 as da
+
+    if "k_scale" in x:
+        return da.decode_attn_fwd_fp8(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out,
+                                      x["scale"], x["k_scale"], x["v_scale"], stream=stream)
+    return da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out, x["scale"],
+                              stream=stream)
+
+
+def run_only(x, attn, stream=None):
+    """decode_attn_only, or decode_attn_only_fp8 for an e4m3 cache."""
+    import decode_attention_output_gb300 as da
+
+    if "k_scale" in x:
+        return da.decode_attn_only_fp8(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], attn, x["scale"],
+                                       x["k_scale"], x["v_scale"], stream=stream)
+    return da.decode_attn_only(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], attn, x["scale"], stream=stream)

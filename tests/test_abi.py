@@ -234,3 +234,59 @@ def test_paged_accepts_valid_block_sizes_on_the_host(lib):
         for key in ("q", "table", "lens", "out", "attn"):
             a[key].data = None
         assert call_paged(lib, a) == (OK, OK), (D, bs)
+
+
+# ------------------------------------------------------------- fp8-cache entry points
+E4M3 = binding.DA_DTYPE_E4M3
+
+
+def fp8_args(**over):
+    a = fwd_args(k=desc([2, 2, 64, 128], E4M3), v=desc([2, 2, 64, 128], E4M3))
+    a["attn"] = desc([2, 8, 128])
+    a.update(over)
+    return a
+
+
+def call_fp8(lib, a, scale=0.1, k_scale=0.02, v_scale=0.02):
+    r = lambda d: ctypes.byref(d) if d is not None else None  # noqa: E731
+    f = ctypes.c_float
+    rc_fwd = lib.decode_attn_fwd_fp8(r(a["q"]), r(a["k"]), r(a["v"]), r(a["lens"]), r(a["w"]), r(a["out"]), f(scale),
+                                     f(k_scale), f(v_scale), None)
+    rc_only = lib.decode_attn_only_fp8(r(a["q"]), r(a["k"]), r(a["v"]), r(a["lens"]), r(a["attn"]), f(scale),
+                                       f(k_scale), f(v_scale), None)
+    return rc_fwd, rc_only
+
+
+BAD_FP8 = [
+    ("kv_bf16", dict(k=desc([2, 2, 64, 128]), v=desc([2, 2, 64, 128])), DTYPE),
+    ("v_bf16", dict(v=desc([2, 2, 64, 128])), DTYPE),
+    ("q_fp8", dict(q=desc([2, 8, 128], E4M3)), DTYPE),
+    ("head_dim_256", dict(q=desc([2, 8, 256]), k=desc([2, 2, 64, 256], E4M3), v=desc([2, 2, 64, 256], E4M3),
+                          w=desc([8 * 256, 256]), attn=desc([2, 8, 256])), UNSUP),
+    ("row_stride_136_bytes", dict(k=desc([2, 2, 64, 128], E4M3, strides=[2 * 64 * 136, 64 * 136, 136, 1])), STRIDE),
+    ("k_misaligned", dict(k=desc([2, 2, 64, 128], E4M3, addr=FAKE + 8)), ALIGN),
+    ("v_shape", dict(v=desc([2, 2, 32, 128], E4M3)), SHAPE),
+]
+
+
+@cpu_only
+@pytest.mark.parametrize("name,over,code", BAD_FP8, ids=[c[0] for c in BAD_FP8])
+def test_fp8_rejects(lib, name, over, code):
+    assert call_fp8(lib, fp8_args(**over)) == (code, code)
+
+
+@cpu_only
+def test_fp8_rejects_nonfinite_scales(lib):
+    assert call_fp8(lib, fp8_args(), k_scale=float("inf")) == (UNSUP, UNSUP)
+    assert call_fp8(lib, fp8_args(), v_scale=float("nan")) == (UNSUP, UNSUP)
+
+
+@cpu_only
+def test_fp8_row_stride_of_16_bytes_passes_validation(lib):
+    """A 144-byte row stride (16-byte multiple, not a multiple of 128) is accepted; B = 0."""
+    a = fp8_args(q=desc([0, 8, 128]), k=desc([0, 2, 64, 128], E4M3, strides=[2 * 64 * 144, 64 * 144, 144, 1]),
+                 v=desc([0, 2, 64, 128], E4M3), lens=desc([0], binding.DA_DTYPE_I32), out=desc([0, 256]),
+                 attn=desc([0, 8, 128]))
+    for key in ("q", "k", "v", "lens", "out", "attn"):
+        a[key].data = None
+    assert call_fp8(lib, a) == (OK, OK)

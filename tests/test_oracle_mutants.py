@@ -47,6 +47,10 @@ MUTANTS = [
     ("paged_row_index_divided", "const int64_t row = t % bs;", "const int64_t row = (t / bs) % bs;", None),
     ("paged_head_ignored", "pages + ((blk * Hkv + j) * bs + row) * D", "pages + ((blk * Hkv) * bs + row) * D", None),
     ("paged_table_stride", "table[b * max_blocks + t / bs]", "table[b + t / bs]", None),
+    ("e4m3_bias_8", "ldexp(1.0 + (double)m / 8.0, (int)e - 7)", "ldexp(1.0 + (double)m / 8.0, (int)e - 8)", None),
+    ("e4m3_subnormal_as_normal", "e == 0 ? ldexp((double)m, -9)", "e == 0 ? ldexp(1.0 + (double)m / 8.0, -7)", None),
+    ("e4m3_mantissa_quarters", "(1.0 + (double)m / 8.0, (int)e - 7)", "(1.0 + (double)m / 4.0, (int)e - 7)", None),
+    ("e4m3_sign_dropped", "(float)(s ? -mag : mag)", "(float)(mag)", None),
 ]
 
 

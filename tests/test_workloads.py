@@ -11,7 +11,7 @@ import torch
 
 import decode_attention_output_gb300 as da
 from decode_attention_output_gb300 import synth
-from gpu_helpers import assert_bf16_close, f64, oracle_decode
+from gpu_helpers import assert_bf16_close, f64, oracle_decode, run_fwd, run_only
 
 pytestmark = pytest.mark.gpu
 
@@ -34,9 +34,9 @@ def test_workload_sampled_rows(orc, name):
     w = synth.WORKLOADS[name]
     x = synth.make_inputs(w, seed=0, device=DEV)
     out = torch.full((w.B, w.N), float("nan"), dtype=torch.bfloat16, device=DEV)
-    da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out, x["scale"])
+    run_fwd(x, out)
     attn = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device=DEV)
-    da.decode_attn_only(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], attn, x["scale"])
+    run_only(x, attn)
     torch.cuda.synchronize()
     assert da.decode_attn_device_error() == 0
     assert torch.isfinite(out.float()).all() and torch.isfinite(attn.float()).all()
