@@ -517,7 +517,7 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
     p.units = fused->plan->units;
   }
 
-  const int box_tokens = paged ? std::min(paged->block_size, tile_tokens(s.D)) : 0;
+  const int box_tokens = paged ? std::min(paged->block_size, tile_tokens(s.D)) : (kv8 ? kTileFp8 : 0);
   DA_TRY(encode_kv_map(&p.tm_k, k, box_tokens));
   if (v) DA_TRY(encode_kv_map(&p.tm_v, v, box_tokens));
   else p.tm_v = p.tm_k;

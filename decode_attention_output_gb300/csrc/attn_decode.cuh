@@ -418,10 +418,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   static_assert(!PAGED || (!kFused && !SCORES), "the paged variant computes attention only");
   static_assert(!KV8 || (DIM == kHeadDim && !kFused && !SCORES && !PAGED),
                 "the fp8-cache variant: head dim 128, attention only, contiguous cache");
-  // Stage: K tile then V tile (bf16: 32 KB; fp8: 64 tokens x 128 B each, 16 KB).
-  constexpr int kSB = KV8 ? kStageBytes8 : kStageBytes;
+  // Stage: K tile then V tile, 32 KB (bf16: 64 tokens x 256 B each; fp8: 128 tokens x 128 B).
+  constexpr int kSB = kStageBytes;
   constexpr int kKB = kSB / 2;
-  constexpr int kT = tile_tokens(DIM);    // tokens per tile
+  // tokens per tile (fp8 cache: 128, so that a stage again holds 32 KB)
+  constexpr int kT = KV8 ? kTileFp8 : tile_tokens(DIM);
   constexpr int kQRow = q_row_bytes(DIM);
   constexpr int kKs = DIM / 16;           // k-steps of QK^T
   constexpr int kTmemCols = NPAD <= 16 ? 32 : 2 * NPAD;  // two accumulator regions
@@ -596,14 +597,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
       for (int mb = 0; mb < 8; ++mb) o[mb][nb][0] = o[mb][nb][1] = o[mb][nb][2] = o[mb][nb][3] = 0.f;
     }
     // this warp's first token inside a stage, and (D = 256) its 128-dim half of O
-    const int tb = kWide ? (wg >> 1) * 16 : wg * 16;
+    const int tb = KV8 ? wg * 32 : (kWide ? (wg >> 1) * 16 : wg * 16);
     const int dh = kWide ? (wg & 1) : 0;
     // dims (within an m-tile of 16) of this lane's accumulator rows g and g+8
     const int d_lo = KV8 ? 2 * g : g, d_hi = KV8 ? 2 * g + 1 : g + 8;
     // Tile layout in shared memory: [box][dim box][box rows][128 B], one box = the rows
     // one copy brings (the whole tile, or a paged block smaller than a tile). Byte offset
     // of a row inside its dim box, and the distance between dim boxes:
-    constexpr int kLogT = kT == 64 ? 6 : 5;
+    constexpr int kLogT = kT == 128 ? 7 : (kT == 64 ? 6 : 5);
     const int lbox = PAGED ? min(p.block_shift, kLogT) : kLogT;  // log2 rows per box
     const uint32_t dbox = 128u << lbox;
     auto row_off = [&](int r) {
@@ -624,7 +625,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
       const bool last = (x == end - 1) || (c.j == c.nt - 1);
       if (it % kGroups == grp) {
         const int t0 = c.j * kT;
-        const int vw = min(kT, lens[c.b] - t0) - tb;  // valid tokens of this warp's 16
+        const int vw = min(kT, lens[c.b] - t0) - tb;  // valid tokens of this warp's 16 (fp8: 32)
         const int stage = it % S;
         const uint32_t ph = (it / S) & 1;
         mbar_wait_bounded(full_bar(stage), ph, p.err, kErrWaitFull, flags);
@@ -649,7 +650,122 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
             }
           }
         }
-        if (vw > 0) {
+        if constexpr (KV8) {
+          // fp8 cache: this warp owns 32 tokens (rows tb .. tb+31 of a 128-token tile), two
+          // 16-row halves that share one softmax update. K and V rows are 128 bytes.
+          if (vw > 0) {
+            const uint32_t kbase = ring + stage * kSB;
+            // ---- S^T = K . Q^T per half. One ldmatrix.x4 brings two k-steps (rows +0..7 and
+            // +8..15 of 16-byte chunks 2kk and 2kk+1); a lane holds 4 dims of a row per matrix,
+            // widened to f16 exactly, which is the k-slot order of the q fragments.
+            float sa[2][NB][4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              float se[NB][4], so[NB][4];
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) se[nb][i] = so[nb][i] = 0.f;
+              const int row = tb + 16 * hh + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+              for (int kk = 0; kk < kKs / 2; ++kk) {
+                const int chunk = 2 * kk + (lane >> 4);
+                uint32_t m[4];
+                ldsm_x4(kbase + row * 128 + ((chunk ^ (lane & 7)) << 4), m[0], m[1], m[2], m[3]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const uint32_t a[4] = {e4m3x2_to_f16x2(m[2 * h]), e4m3x2_to_f16x2(m[2 * h + 1]),
+                                         e4m3x2_to_f16x2(m[2 * h] >> 16), e4m3x2_to_f16x2(m[2 * h + 1] >> 16)};
+#pragma unroll
+                  for (int nb = 0; nb < NB; ++nb) {
+                    if (h) mma_f16_16816(so[nb], a, qf[nb][2 * kk + h][0], qf[nb][2 * kk + h][1]);
+                    else mma_f16_16816(se[nb], a, qf[nb][2 * kk + h][0], qf[nb][2 * kk + h][1]);
+                  }
+                }
+              }
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sa[hh][nb][i] = se[nb][i] + so[nb][i];
+            }
+            // ---- online softmax over the 32 tokens (element i of half hh: token
+            // 16hh + g + 8(i>>1), head 8nb + 2t + (i&1)); P rounded to f16 for P.V
+            uint32_t pb[2][NB][2];
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              float xv[2][4];
+              float mx0 = kNegInf, mx1 = kNegInf;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const bool v0 = 16 * hh + g < vw, v1 = 16 * hh + g + 8 < vw;
+                xv[hh][0] = v0 ? sa[hh][nb][0] * sl2 : kNegInf;
+                xv[hh][1] = v0 ? sa[hh][nb][1] * sl2 : kNegInf;
+                xv[hh][2] = v1 ? sa[hh][nb][2] * sl2 : kNegInf;
+                xv[hh][3] = v1 ? sa[hh][nb][3] * sl2 : kNegInf;
+                mx0 = fmaxf(mx0, fmaxf(xv[hh][0], xv[hh][2]));
+                mx1 = fmaxf(mx1, fmaxf(xv[hh][1], xv[hh][3]));
+              }
+#pragma unroll
+              for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+              }
+              const float mn0 = fmaxf(m_run[nb][0], mx0), mn1 = fmaxf(m_run[nb][1], mx1);
+              const float al0 = fast_exp2(m_run[nb][0] - mn0), al1 = fast_exp2(m_run[nb][1] - mn1);
+              m_run[nb][0] = mn0;
+              m_run[nb][1] = mn1;
+              float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t r0 = pack_f16x2(fast_exp2(xv[hh][0] - mn0), fast_exp2(xv[hh][1] - mn1));
+                const uint32_t r1 = pack_f16x2(fast_exp2(xv[hh][2] - mn0), fast_exp2(xv[hh][3] - mn1));
+                ls0 += f16lo_to_f32(r0) + f16lo_to_f32(r1);  // the weights that enter P.V
+                ls1 += f16hi_to_f32(r0) + f16hi_to_f32(r1);
+                pb[hh][nb][0] = movmatrix_trans(r0);  // P[head g][tokens 16hh + 2t, +1]
+                pb[hh][nb][1] = movmatrix_trans(r1);  // P[head g][tokens 16hh + 2t + 8, +9]
+              }
+              l_run[nb][0] = l_run[nb][0] * al0 + ls0;
+              l_run[nb][1] = l_run[nb][1] * al1 + ls1;
+#pragma unroll
+              for (int mb = 0; mb < 8; ++mb) {
+                o[mb][nb][0] *= al0;
+                o[mb][nb][1] *= al1;
+                o[mb][nb][2] *= al0;
+                o[mb][nb][3] *= al1;
+              }
+            }
+            // ---- O^T += V^T . P^T, one k-step per half. ldmatrix.trans of 16-bit pairs hands
+            // a lane tokens 2t, 2t+1 of dims 2g, 2g+1 (a byte each); a byte permute makes
+            // (dim 2g: two tokens) and (dim 2g+1: two tokens), widened to f16 exactly, so the
+            // MMA's rows g and g+8 of m-tile mb are dims 16mb + 2g and 16mb + 2g + 1.
+            const uint32_t vbase = kbase + kKB;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int vwh = vw - 16 * hh;  // valid tokens of this half
+              if (vwh <= 0) break;
+              const int row = tb + 16 * hh + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+              for (int mp = 0; mp < 4; ++mp) {
+                const int chunk = 2 * mp + (lane >> 4);
+                uint32_t m[4];
+                ldsm_x4_trans(vbase + row * 128 + ((chunk ^ (lane & 7)) << 4), m[0], m[1], m[2], m[3]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  uint32_t lo = m[2 * h], hi = m[2 * h + 1];  // tokens 2t, 2t+1 and 2t+8, 2t+9
+                  if (vwh < 16) {  // rows past the sequence may hold anything; P is 0 there
+                    lo = mask_tokens(lo, 2 * t, vwh);
+                    hi = mask_tokens(hi, 2 * t + 8, vwh);
+                  }
+                  const uint32_t pl = __byte_perm(lo, 0, 0x3120), ph = __byte_perm(hi, 0, 0x3120);
+                  const uint32_t a[4] = {e4m3x2_to_f16x2(pl), e4m3x2_to_f16x2(pl >> 16), e4m3x2_to_f16x2(ph),
+                                         e4m3x2_to_f16x2(ph >> 16)};
+#pragma unroll
+                  for (int nb = 0; nb < NB; ++nb) mma_f16_16816(o[2 * mp + h][nb], a, pb[hh][nb][0], pb[hh][nb][1]);
+                }
+              }
+            }
+          }
+        } else if (vw > 0) {
           const uint32_t kbase = ring + stage * kSB;
           // ---- S^T[16 tokens][8*NB heads] = K_tile . Q^T  (fp32, unscaled)
           float se[NB][4], so[NB][4];
@@ -657,28 +773,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
           for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
             for (int i = 0; i < 4; ++i) se[nb][i] = so[nb][i] = 0.f;
-          if constexpr (KV8) {
-            // fp8 K rows are 128 bytes: one ldmatrix.x4 brings two k-steps (rows tb..+7 and
-            // tb+8..+15 of 16-byte chunks 2kk and 2kk+1); a lane holds 4 dims of a row per
-            // matrix, widened to f16 exactly (the k-slot order of the q fragments)
-            const int row = tb + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-            for (int kk = 0; kk < kKs / 2; ++kk) {
-              const int chunk = 2 * kk + (lane >> 4);
-              uint32_t m[4];
-              ldsm_x4(kbase + row * 128 + ((chunk ^ (lane & 7)) << 4), m[0], m[1], m[2], m[3]);
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const uint32_t a[4] = {e4m3x2_to_f16x2(m[2 * h]), e4m3x2_to_f16x2(m[2 * h + 1]),
-                                       e4m3x2_to_f16x2(m[2 * h] >> 16), e4m3x2_to_f16x2(m[2 * h + 1] >> 16)};
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb) {
-                  if (h) mma_f16_16816(so[nb], a, qf[nb][2 * kk + h][0], qf[nb][2 * kk + h][1]);
-                  else mma_f16_16816(se[nb], a, qf[nb][2 * kk + h][0], qf[nb][2 * kk + h][1]);
-                }
-              }
-            }
-          } else {
+          {
 #pragma unroll
             for (int ks = 0; ks < kKs; ++ks) {
               const int chunk = 2 * (ks & 3) + (lane >> 4);
@@ -728,20 +823,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
               const float al0 = fast_exp2(m_run[nb][0] - mn0), al1 = fast_exp2(m_run[nb][1] - mn1);
               m_run[nb][0] = mn0;
               m_run[nb][1] = mn1;
-              // P in the P.V operand type (bf16; f16 with an fp8 cache); the sum uses the rounded
-              // weights that enter P.V
-              uint32_t r0, r1;
-              if constexpr (KV8) {
-                r0 = pack_f16x2(fast_exp2(x0 - mn0), fast_exp2(x1 - mn1));  // token g
-                r1 = pack_f16x2(fast_exp2(x2 - mn0), fast_exp2(x3 - mn1));  // token g+8
-                l_run[nb][0] = l_run[nb][0] * al0 + (f16lo_to_f32(r0) + f16lo_to_f32(r1));
-                l_run[nb][1] = l_run[nb][1] * al1 + (f16hi_to_f32(r0) + f16hi_to_f32(r1));
-              } else {
-                r0 = pack_bf16x2(fast_exp2(x0 - mn0), fast_exp2(x1 - mn1));  // token g
-                r1 = pack_bf16x2(fast_exp2(x2 - mn0), fast_exp2(x3 - mn1));  // token g+8
-                l_run[nb][0] = l_run[nb][0] * al0 + (bf16lo_to_f32(r0) + bf16lo_to_f32(r1));
-                l_run[nb][1] = l_run[nb][1] * al1 + (bf16hi_to_f32(r0) + bf16hi_to_f32(r1));
-              }
+              // the sum uses the bf16-rounded weights that enter P.V
+              const uint32_t r0 = pack_bf16x2(fast_exp2(x0 - mn0), fast_exp2(x1 - mn1));  // token g
+              const uint32_t r1 = pack_bf16x2(fast_exp2(x2 - mn0), fast_exp2(x3 - mn1));  // token g+8
+              l_run[nb][0] = l_run[nb][0] * al0 + (bf16lo_to_f32(r0) + bf16lo_to_f32(r1));
+              l_run[nb][1] = l_run[nb][1] * al1 + (bf16hi_to_f32(r0) + bf16hi_to_f32(r1));
 #pragma unroll
               for (int mb = 0; mb < 8; ++mb) {
                 o[mb][nb][0] *= al0;
@@ -754,32 +840,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
             }
             // ---- O^T[128 dims (of half dh)][8*NB heads] += V_tile^T . P^T
             const uint32_t vbase = kbase + kKB;
-            if constexpr (KV8) {
-              // fp8 V rows are 128 bytes. ldmatrix.trans of 16-bit pairs hands a lane tokens
-              // 2t, 2t+1 of dims 2g, 2g+1 (one byte each); a byte permute makes (dim 2g: two
-              // tokens) and (dim 2g+1: two tokens), widened to f16 exactly. So the MMA's rows
-              // g and g+8 of m-tile mb are dims 16mb + 2g and 16mb + 2g + 1.
-              const int row = tb + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-              for (int mp = 0; mp < 4; ++mp) {
-                const int chunk = 2 * mp + (lane >> 4);
-                uint32_t m[4];
-                ldsm_x4_trans(vbase + row * 128 + ((chunk ^ (lane & 7)) << 4), m[0], m[1], m[2], m[3]);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  uint32_t lo = m[2 * h], hi = m[2 * h + 1];  // tokens 2t, 2t+1 and 2t+8, 2t+9
-                  if (vw < 16) {  // rows past the sequence may hold anything; P is 0 there
-                    lo = mask_tokens(lo, 2 * t, vw);
-                    hi = mask_tokens(hi, 2 * t + 8, vw);
-                  }
-                  const uint32_t pl = __byte_perm(lo, 0, 0x3120), ph = __byte_perm(hi, 0, 0x3120);
-                  const uint32_t a[4] = {e4m3x2_to_f16x2(pl), e4m3x2_to_f16x2(pl >> 16), e4m3x2_to_f16x2(ph),
-                                         e4m3x2_to_f16x2(ph >> 16)};
-#pragma unroll
-                  for (int nb = 0; nb < NB; ++nb) mma_f16_16816(o[2 * mp + h][nb], a, pb[nb][0], pb[nb][1]);
-                }
-              }
-            } else {
             const int jm = lane >> 3;
 #pragma unroll
             for (int mb = 0; mb < 8; ++mb) {
@@ -795,7 +855,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
               }
 #pragma unroll
               for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(o[mb][nb], a, pb[nb][0], pb[nb][1]);
-            }
             }
           }
         }
@@ -1006,7 +1065,7 @@ cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kAttnThreads);
-  cfg.dynamicSmemBytes = attn_smem_bytes(p.B, NB, S, DIM, KV8 ? kStageBytes8 : kStageBytes);
+  cfg.dynamicSmemBytes = attn_smem_bytes(p.B, NB, S, DIM);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;  // the fused step's grid barrier needs every CTA resident

@@ -1,12 +1,12 @@
 // attn_decode_fp8.cu -- instantiations of the attention kernel over an fp8 (e4m3) KV
-// cache: head dim 128, 8-stage ring of 16 KB stages.
+// cache: head dim 128, 128-token tiles in a 4-stage ring of 32 KB stages.
 #include "attn_decode.cuh"
 
 namespace da {
 
 cudaError_t launch_attention_fp8(const AttnParams& p, int grid, int nb, cudaStream_t stream) {
-  return nb == 1 ? launch_one<1, false, kStages8, 0, kHeadDim, false, true>(p, grid, stream)
-                 : launch_one<2, false, kStages8, 0, kHeadDim, false, true>(p, grid, stream);
+  return nb == 1 ? launch_one<1, false, 4, 0, kHeadDim, false, true>(p, grid, stream)
+                 : launch_one<2, false, 4, 0, kHeadDim, false, true>(p, grid, stream);
 }
 
 }  // namespace da

@@ -70,12 +70,9 @@ constexpr size_t kMaxDynSmem = 232448;  // 227 KB per CTA on sm_100-class GPUs
 constexpr size_t attn_smem_bytes(int batch, int nb, int stages, int dim = kHeadDim, int stage_bytes = kStageBytes) {
   return AttnSmem(nb, batch, stages, dim, stage_bytes).total();
 }
-// fp8 (e4m3) caches: a stage holds 64 tokens x 128 dims x 1 byte of K and of V (16 KB),
-// and the ring has twice the stages, so it spans the same 128 KB.
-constexpr int kStageBytes8 = 16384;
-constexpr int kStages8 = 8;
-static_assert(AttnSmem(2, kMaxBatch, kStages8, kHeadDim, kStageBytes8).total() <= kMaxDynSmem,
-              "attention kernel (fp8 cache) exceeds 227 KB of shared memory");
+// fp8 (e4m3) caches: a tile is 128 tokens (128 x 128 dims x 1 byte of K and of V), so a
+// stage holds the same 32 KB and the ring the same 4 stages as for bf16.
+constexpr int kTileFp8 = 128;
 static_assert(AttnSmem(2, kMaxBatch, 4).total() <= kMaxDynSmem, "attention kernel exceeds 227 KB of shared memory");
 static_assert(AttnSmem(2, kMaxBatch, 4, kHeadDimWide).total() <= kMaxDynSmem,
               "attention kernel (D = 256) exceeds 227 KB of shared memory");
