@@ -1,6 +1,7 @@
 // attn_decode.cuh -- persistent split-KV decode attention for sm_103a (the kernel
 // template; attn_decode.cu instantiates head dim 128 and the fused step,
-// attn_decode_d256.cu head dim 256).
+// attn_decode_d256.cu head dim 256, attn_decode_paged.cu the paged cache,
+// attn_decode_fp8.cu the fp8 cache).
 //
 // Computes, for every batch row b and query head h (KV head j = h / G),
 //   S = q . K^T over t < L_b (the page's scores_fp32, fp32),
@@ -10,18 +11,18 @@
 // QK^T and attn.V shapes of its table "三个 Matmul 的 Shape 特征分析".
 //
 // Design (GB300):
-//  * Work unit = one tile (64 tokens at D = 128, 32 at D = 256: 32 KB of K+V
-//    either way) of one (batch, KV-head) sequence. All tiles of
-//    the batch are laid end to end and each persistent CTA takes an equal,
-//    contiguous range of them, so ragged batches stay balanced. A range may end
-//    or start inside a sequence: each CTA emits one partial (m, l, O) per
-//    sequence it touches; the CTA that finishes a sequence last (an atomic
-//    completion counter, no waiting) merges the partials with the log-sum-exp
-//    rule and writes bf16.
-//  * One producer warp streams K and V tiles with 4-D TMA (128-byte swizzle,
-//    two 64-dim boxes per tile) into a 4- or 6-stage shared-memory ring guarded by
-//    mbarriers; q rows arrive by 1-D bulk copy with a sequence's first tiles.
-//    At D = 256 a tile is four 64-dim boxes of 32 tokens.
+//  * Work unit = one tile of one (batch, KV-head) sequence: 32 KB of K+V (64 tokens at
+//    D = 128, 32 at D = 256, 128 with an fp8 cache). All tiles of the batch are laid
+//    end to end and each persistent CTA takes an equal, contiguous range of them, so
+//    ragged batches stay balanced. A range may end or start inside a sequence: each
+//    CTA emits one partial (m, l, O) per sequence it touches; the CTA that finishes a
+//    sequence last (an atomic completion counter, no waiting) merges the partials with
+//    the log-sum-exp rule and writes bf16.
+//  * One producer lane streams K and V tiles with one 5-D TMA copy per tile and tensor
+//    (the head dim split into 128-byte rows of 64-dim boxes, 128-byte swizzle) into a
+//    4-stage shared-memory ring guarded by mbarriers; q rows arrive by 1-D bulk copy
+//    with a sequence's first tiles. A paged cache is read in boxes of
+//    min(block size, tile) tokens, the block ids arriving by TMA a few tiles ahead.
 //  * Two consumer groups of four warps take alternate stages, so two tiles are
 //    in compute at once per SM. Each warp owns 16 tokens of a stage and all G
 //    query heads of the group (every K/V byte is read once). S^T = K . Q^T runs
@@ -38,6 +39,8 @@
 //    tensor pipe is mostly idle, so the duplicate QK^T is cheap) and hence the same
 //    softmax state, and each accumulates one 128-dim half of O. Registers per
 //    thread stay those of D = 128 except the q fragments, which double.
+//  * fp8 (e4m3) cache: a warp owns 32 tokens (two 16-row halves, one softmax update);
+//    codes are widened to f16 in registers (exact) for f16 MMAs, q and P in f16.
 #pragma once
 #include "kernels.h"
 #include "ptx.cuh"
