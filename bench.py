@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 import hashlib
 import json
 import math
@@ -207,6 +208,34 @@ def recorded_traffic(workload: str):
     return ent.get("dram_bytes_per_launch")
 
 
+def fwd_call(da, x, out, stream=None):
+    """One step through the public API: decode_attn_fwd (decode_attn_fwd_fp8 for an e4m3 cache)."""
+    if "k_scale" in x:
+        return da.decode_attn_fwd_fp8(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out,
+                                      x["scale"], x["k_scale"], x["v_scale"], stream=stream)
+    return da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out, x["scale"],
+                              stream=stream)
+
+
+def only_call(da, x, attn, stream=None):
+    """The attention kernel alone: decode_attn_only (decode_attn_only_fp8 for an e4m3 cache)."""
+    if "k_scale" in x:
+        return da.decode_attn_only_fp8(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], attn, x["scale"],
+                                       x["k_scale"], x["v_scale"], stream=stream)
+    return da.decode_attn_only(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], attn, x["scale"], stream=stream)
+
+
+def oracle_call(orc, x, rows, lens):
+    """The oracle's whole step on host copies of batch rows `rows`."""
+    from decode_attention_output_gb300 import synth
+
+    a = (synth.to_bits(x["q"][rows]), synth.to_bits(x["k_cache"][rows]), synth.to_bits(x["v_cache"][rows]), lens,
+         synth.to_bits(x["o_weight"]))
+    if "k_scale" in x:
+        return lambda: orc.decode_fp8(*a, x["scale"], x["k_scale"], x["v_scale"])
+    return lambda: orc.decode(*a, x["scale"])
+
+
 def oracle_baseline(x_host: dict, w, rows, budget_s: float):
     """Times the fp64 oracle on host copies of `rows` batch rows; returns a dict."""
     import numpy as np
@@ -216,16 +245,15 @@ def oracle_baseline(x_host: dict, w, rows, budget_s: float):
 
     orc = oracle.default()
     lens = x_host["seq_lens"][rows].numpy().astype(np.int32)
-    args = (synth.to_bits(x_host["q"][rows]), synth.to_bits(x_host["k_cache"][rows]),
-            synth.to_bits(x_host["v_cache"][rows]), lens, synth.to_bits(x_host["o_weight"]), x_host["scale"])
-    sub = synth.Workload("sample", B=len(rows), Hq=w.Hq, Hkv=w.Hkv, Lcap=w.Lcap, N=w.N)
+    run = oracle_call(orc, x_host, rows, lens)
+    sub = dataclasses.replace(w, name="sample", B=len(rows), fixed_lens=())
     nbytes = synth.algorithmic_bytes(sub, lens)["total"]
-    orc.decode(*args)  # warm-up
+    run()  # warm-up
     times = []
     t_start = time.perf_counter()
     while len(times) < 3 or (time.perf_counter() - t_start < budget_s and len(times) < 1000):
         t0 = time.perf_counter()
-        orc.decode(*args)
+        run()
         times.append(time.perf_counter() - t0)
     sec = statistics.median(times)
     return {"value": nbytes / sec / 1e9, "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
@@ -244,8 +272,7 @@ def run_reference(args, world, rank):
 
     w = synth.WORKLOADS[args.workload]
     rows = [0]
-    sub = synth.Workload(w.name, B=len(rows), Hq=w.Hq, Hkv=w.Hkv, Lcap=w.Lcap, N=w.N, lens=w.lens,
-                         ragged_lo=w.ragged_lo, ragged_hi=w.ragged_hi, k_mult=w.k_mult)
+    sub = dataclasses.replace(w, B=len(rows))
     x = synth.make_inputs(sub, seed=args.seed, device="cpu")
     import numpy as np
 
@@ -253,13 +280,12 @@ def run_reference(args, world, rank):
 
     orc = oracle.default()
     lens = x["seq_lens"].numpy().astype(np.int32)
-    a = (synth.to_bits(x["q"]), synth.to_bits(x["k_cache"]), synth.to_bits(x["v_cache"]), lens,
-         synth.to_bits(x["o_weight"]), x["scale"])
+    run = oracle_call(orc, x, list(range(len(rows))), lens)
     for _ in range(args.warmup):
-        orc.decode(*a)
+        run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        orc.decode(*a)
+        run()
     sec = (time.perf_counter() - t0) / max(1, args.steps)
     nbytes = synth.algorithmic_bytes(sub, lens)["total"]
     val = nbytes / sec / 1e9
@@ -267,7 +293,8 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "us_per_step": sec * 1e6,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name, "sample_rows": rows, "B": w.B, "Hq": w.Hq,
-                                            "Hkv": w.Hkv, "kv_len": w.Lcap, "hidden": w.N},
+                                            "Hkv": w.Hkv, "kv_len": w.Lcap, "hidden": w.N, "head_dim": w.D,
+                                            "kv_cache": w.kv},
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
                              "sample": f"batch row 0 of {w.name} per step (all heads + o_proj of that row)"},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -304,8 +331,7 @@ def run_ours(args, world, rank, local):
 
     def step(i, st=None):
         s = sets[i % n_sets]
-        da.decode_attn_fwd(s["q"], s["k_cache"], s["v_cache"], s["seq_lens"], s["o_weight"], outs[i % n_sets],
-                           s["scale"], stream=st if st is not None else stream)
+        fwd_call(da, s, outs[i % n_sets], stream=st if st is not None else stream)
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -335,14 +361,13 @@ def run_ours(args, world, rank, local):
     sampler_window = (t_wall0, t_wall1)
 
     # ---- dominant kernel (split-KV attention) timed alone, per launch, same inputs and plan
-    attn_bufs = [torch.empty((w.B, w.Hq, 128), dtype=torch.bfloat16, device=dev) for _ in range(n_sets)]
+    attn_bufs = [torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev) for _ in range(n_sets)]
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     torch.cuda.synchronize(dev)
     for i in range(args.steps):
         s = sets[i % n_sets]
         evs[i][0].record(stream)
-        da.decode_attn_only(s["q"], s["k_cache"], s["v_cache"], s["seq_lens"], attn_bufs[i % n_sets], s["scale"],
-                            stream=stream)
+        only_call(da, s, attn_bufs[i % n_sets], stream=stream)
         evs[i][1].record(stream)
     torch.cuda.synchronize(dev)
     attn_ms_eager = statistics.mean(a.elapsed_time(b) for a, b in evs)
@@ -356,8 +381,7 @@ def run_ours(args, world, rank, local):
         with torch.cuda.graph(ga, stream=cap):
             for i in range(args.steps):
                 s = sets[i % n_sets]
-                da.decode_attn_only(s["q"], s["k_cache"], s["v_cache"], s["seq_lens"], attn_bufs[i % n_sets],
-                                    s["scale"], stream=cap)
+                only_call(da, s, attn_bufs[i % n_sets], stream=cap)
         ga.replay()
         torch.cuda.synchronize(dev)
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -408,7 +432,7 @@ def run_ours(args, world, rank, local):
     total_bytes = sum_over_ranks(world, float(nb["total"]))
     value = total_bytes / (step_ms_max * 1e-3) / 1e9
     peak, peak_src = measured_hbm_peak()
-    attn_bytes = nb["kv"] + w.B * w.Hq * 128 * 2 * 2  # K+V of valid tokens + q in + attention out
+    attn_bytes = nb["kv"] + w.B * w.Hq * w.D * 2 * 2  # K+V of valid tokens + q in + attention out
     achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
     traffic = recorded_traffic(w.name)
 
@@ -425,8 +449,7 @@ def run_ours(args, world, rank, local):
         def e2e_step():
             for k in host:
                 dbuf[k].copy_(host[k], non_blocking=True)
-            da.decode_attn_fwd(dbuf["q"], dbuf["k_cache"], dbuf["v_cache"], dbuf["seq_lens"], dbuf["o_weight"],
-                               outs[0], base["scale"], stream=stream)
+            fwd_call(da, {**base, **dbuf}, outs[0], stream=stream)
             out_h.copy_(outs[0], non_blocking=True)
             torch.cuda.current_stream(dev).synchronize()
 
@@ -450,9 +473,10 @@ def run_ours(args, world, rank, local):
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms_max, "us_per_step": step_ms_max * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.kv == "bf16" else "e4m3 cache, f16 MMA",
             "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "kv_len": w.Lcap, "hidden": w.N,
+                       "head_dim": w.D, "kv_cache": w.kv,
                        "seq_lens_sum": int(lens.sum().item()), "bytes_per_step": nb,
                        "l2": f"{n_sets} rotated input sets of {set_bytes / 1e6:.0f} MB (>2x L2 between reuses)",
                        "step_hbm_frac": value / world / peak, "parallelism": f"replicas x{world}",
