@@ -975,45 +975,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
           named_bar_sync(1, kConsumerThreads);  // every thread's partial stores precede the release
           if (tid == 0) flags[1] = (atomic_add_acq_rel_gpu(p.counters + seq, 1) == n_parts - 1);
           named_bar_sync(1, kConsumerThreads);  // ... and the acquire precedes every thread's loads
-          if (flags[1]) {  // every other part has landed: merge them all
-            // (a) one warp per head: the parts' (m, l) come in together (a lane per part),
-            //     and the normalised weights exp2(m_p - M) / sum go to shared memory
-            float* wpart = merge_o;  // free again: [G][n_parts]
-            for (int h = warp; h < G; h += kGroups * kGroupWarps) {
-              float M = kNegInf;
-              for (int pc = lane; pc < n_parts; pc += 32)
-                M = fmaxf(M, __ldcg(p.part_ml + (((long long)first_cta + pc + seq) * p.gpad + h) * 2));
-#pragma unroll
-              for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-              float lsum = 0.f;
-              for (int pc = lane; pc < n_parts; pc += 32) {
-                const float* ml2 = p.part_ml + (((long long)first_cta + pc + seq) * p.gpad + h) * 2;
-                const float f = fast_exp2(__ldcg(ml2) - M);
-                wpart[h * n_parts + pc] = f;
-                lsum += f * __ldcg(ml2 + 1);
-              }
-#pragma unroll
-              for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-              __syncwarp();
-              for (int pc = lane; pc < n_parts; pc += 32) wpart[h * n_parts + pc] /= lsum;
-            }
-            named_bar_sync(1, kConsumerThreads);
-            // (b) O[h][d] = sum_p w_p O_p[h][d]: the loads of eight parts go out together
+          if (flags[1]) {  // every other part has landed: merge them all, in one pass
+            // Thread (h, d) loads the parts' (m, l, O[h][d]) together, eight parts per batch
+            // from clamped (always valid) addresses, masked afterwards, and merges them with
+            // a running maximum: one L2 round trip per eight parts after the counter.
             for (int h = tid / DIM; h < G; h += kHStep) {
-              float acc = 0.f;
-              for (int p0 = 0; p0 < n_parts; p0 += 16) {
-                // clamped (always valid) addresses: sixteen loads in flight, masked afterwards
-                float v[16];
+              float M = kNegInf, lsum = 0.f, acc = 0.f;
+              for (int p0 = 0; p0 < n_parts; p0 += 8) {
+                float mv[8], lv[8], ov[8];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                  const int pc = min(p0 + u, n_parts - 1);
-                  v[u] = __ldcg(p.part_o + (((long long)first_cta + pc + seq) * p.gpad + h) * DIM + d);
+                for (int u = 0; u < 8; ++u) {
+                  const long long slot = (long long)first_cta + min(p0 + u, n_parts - 1) + seq;
+                  const float* ml = p.part_ml + (slot * p.gpad + h) * 2;
+                  mv[u] = __ldcg(ml);
+                  lv[u] = __ldcg(ml + 1);
+                  ov[u] = __ldcg(p.part_o + (slot * p.gpad + h) * DIM + d);
                 }
+                float Mc = M;
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
-                  if (p0 + u < n_parts) acc += wpart[h * n_parts + p0 + u] * v[u];
+                for (int u = 0; u < 8; ++u)
+                  if (p0 + u < n_parts) Mc = fmaxf(Mc, mv[u]);  // every part holds a token: finite
+                const float r = fast_exp2(M - Mc);                // 0 on the first batch
+                lsum *= r;
+                acc *= r;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                  if (p0 + u < n_parts) {
+                    const float f = fast_exp2(mv[u] - Mc);
+                    lsum += f * lv[u];
+                    acc += f * ov[u];
+                  }
+                M = Mc;
               }
-              p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc);
+              p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
             }
             if (tid == 0) p.counters[seq] = 0;  // ready for the next call
           }

@@ -32,9 +32,8 @@ constexpr int kMaxGroup = 16;
 constexpr int kMaxBatch = 1024;
 constexpr int kMergeRow = 132;                 // floats per head row of the merge scratch (128 + pad); at
                                                // D = 256 a warp holds one 128-dim half of the output
-constexpr int kMaxAttnCtas = 512;              // parts per sequence stay <= this: the cross-CTA merge
-                                               // keeps G x parts weights in the 4*8*nb*kMergeRow scratch
-static_assert(kMaxAttnCtas <= kGroupWarps * kMergeRow, "merge weights must fit the merge scratch");
+constexpr int kMaxAttnCtas = 512;              // persistent CTAs of the attention kernel (and so parts
+                                               // per sequence) at most
 static_assert(tile_tokens(kHeadDim) * kHeadDim * 2 == kKTileBytes, "K tile bytes at D = 128");
 static_assert(tile_tokens(kHeadDimWide) * kHeadDimWide * 2 == kKTileBytes, "K tile bytes at D = 256");
 // Shared-memory carve-up of the attention kernel; nb = 8-head blocks (1 or 2),
