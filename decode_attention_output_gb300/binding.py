@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import struct
 import threading
 
 import torch
@@ -51,7 +52,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             if not os.path.exists(path):
                 raise RuntimeError(f"{path} is missing: run decode_attention_output_gb300.build.build() first")
             lib = ctypes.CDLL(path)
-            P = ctypes.POINTER(da_tensor_t)
+            P = ctypes.c_void_p  # a packed da_tensor_t (see _pack), a pointer to one, or NULL
             vp, f32, i64 = ctypes.c_void_p, ctypes.c_float, ctypes.c_int64
             lib.decode_attn_fwd.argtypes = [P, P, P, P, P, P, f32, vp]
             lib.decode_attn_only.argtypes = [P, P, P, P, P, f32, vp]
@@ -80,22 +81,33 @@ def describe(t: torch.Tensor | None) -> da_tensor_t | None:
     """da_tensor_t view of a tensor (no copy)."""
     if t is None:
         return None
-    if t.dtype not in _DTYPES:
+    return da_tensor_t.from_buffer_copy(_pack(t))
+
+
+# da_tensor_t as bytes: data pointer, dtype, ndim, shape[4], stride[4] (little endian,
+# no padding: the C struct has none either). Packing the fields in one call costs a
+# third of filling a ctypes structure field by field, and the calls below are made
+# once per tensor per step.
+_DESC = struct.Struct("<Qii4q4q")
+_PAD = ((0, 0, 0, 0), (0, 0, 0), (0, 0), (0,), ())
+assert _DESC.size == ctypes.sizeof(da_tensor_t)
+
+
+def _pack(t: torch.Tensor) -> bytes:
+    code = _DTYPES.get(t.dtype)
+    if code is None:
         raise TypeError(f"unsupported dtype {t.dtype}")
-    if t.dim() > 4:
+    shape = t.shape
+    n = len(shape)
+    if n > 4:
         raise ValueError("at most 4 dimensions")
-    d = da_tensor_t()
-    d.data = t.data_ptr() if t.numel() else None
-    d.dtype = _DTYPES[t.dtype]
-    d.ndim = t.dim()
-    for i in range(t.dim()):
-        d.shape[i] = t.shape[i]
-        d.stride[i] = t.stride(i)
-    return d
+    pad = _PAD[n]
+    return _DESC.pack(t.data_ptr() if t.numel() else 0, code, n, *shape, *pad, *t.stride(), *pad)
 
 
-def _ref(d):
-    return ctypes.byref(d) if d is not None else None
+def _ref(t):
+    """Argument for a `const da_tensor_t*` parameter: packed bytes, or NULL for None."""
+    return None if t is None else _pack(t)
 
 
 def _stream(stream) -> int | None:
@@ -118,16 +130,16 @@ def status_str(code: int) -> str:
 def decode_attn_fwd(q, k_cache, v_cache, seq_lens, o_weight, out, scale: float, stream=None) -> torch.Tensor:
     """out[B, N] = (softmax(scale * q K^T) V)_flat . o_weight; returns ``out``."""
     lib = load()
-    ds = [describe(x) for x in (q, k_cache, v_cache, seq_lens, o_weight, out)]
-    _check("decode_attn_fwd", lib.decode_attn_fwd(*[_ref(d) for d in ds], float(scale), _stream(stream)))
+    ds = [_ref(x) for x in (q, k_cache, v_cache, seq_lens, o_weight, out)]
+    _check("decode_attn_fwd", lib.decode_attn_fwd(*ds, float(scale), _stream(stream)))
     return out
 
 
 def decode_attn_only(q, k_cache, v_cache, seq_lens, attn_out, scale: float, stream=None) -> torch.Tensor:
     """attn_out[B, Hq, D] = softmax(scale * q K^T) V (bf16); returns ``attn_out``."""
     lib = load()
-    ds = [describe(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
-    _check("decode_attn_only", lib.decode_attn_only(*[_ref(d) for d in ds], float(scale), _stream(stream)))
+    ds = [_ref(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
+    _check("decode_attn_only", lib.decode_attn_only(*ds, float(scale), _stream(stream)))
     return attn_out
 
 
@@ -138,9 +150,9 @@ def decode_attn_only_noalloc(q, k_cache, v_cache, seq_lens, attn_out, scale: flo
     fixed 8 MiB scratch array inside the library; calls that overlap on the GPU race
     on it. Raises DecodeAttnError (DA_ERR_SCRATCH) when a call needs more scratch."""
     lib = load()
-    ds = [describe(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
+    ds = [_ref(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
     _check("decode_attn_only_noalloc",
-           lib.decode_attn_only_noalloc(*[_ref(d) for d in ds], float(scale), _stream(stream)))
+           lib.decode_attn_only_noalloc(*ds, float(scale), _stream(stream)))
     return attn_out
 
 
@@ -149,8 +161,8 @@ def decode_attn_fwd_paged(q, k_pages, v_pages, block_table, seq_lens, o_weight, 
     """decode_attn_fwd over a paged cache: k_pages / v_pages [num_blocks, Hkv, block_size, D],
     block_table [B, max_blocks] int32; returns ``out``."""
     lib = load()
-    ds = [describe(x) for x in (q, k_pages, v_pages, block_table, seq_lens, o_weight, out)]
-    _check("decode_attn_fwd_paged", lib.decode_attn_fwd_paged(*[_ref(d) for d in ds], float(scale), _stream(stream)))
+    ds = [_ref(x) for x in (q, k_pages, v_pages, block_table, seq_lens, o_weight, out)]
+    _check("decode_attn_fwd_paged", lib.decode_attn_fwd_paged(*ds, float(scale), _stream(stream)))
     return out
 
 
@@ -158,9 +170,9 @@ def decode_attn_only_paged(q, k_pages, v_pages, block_table, seq_lens, attn_out,
                            stream=None) -> torch.Tensor:
     """decode_attn_only over a paged cache (see decode_attn_fwd_paged); returns ``attn_out``."""
     lib = load()
-    ds = [describe(x) for x in (q, k_pages, v_pages, block_table, seq_lens, attn_out)]
+    ds = [_ref(x) for x in (q, k_pages, v_pages, block_table, seq_lens, attn_out)]
     _check("decode_attn_only_paged",
-           lib.decode_attn_only_paged(*[_ref(d) for d in ds], float(scale), _stream(stream)))
+           lib.decode_attn_only_paged(*ds, float(scale), _stream(stream)))
     return attn_out
 
 
@@ -169,8 +181,8 @@ def decode_attn_fwd_fp8(q, k_cache, v_cache, seq_lens, o_weight, out, scale: flo
     """decode_attn_fwd over an fp8 cache: k_cache / v_cache torch.float8_e4m3fn, the keys
     and values being k_cache * k_scale and v_cache * v_scale; returns ``out``."""
     lib = load()
-    ds = [describe(x) for x in (q, k_cache, v_cache, seq_lens, o_weight, out)]
-    _check("decode_attn_fwd_fp8", lib.decode_attn_fwd_fp8(*[_ref(d) for d in ds], float(scale), float(k_scale),
+    ds = [_ref(x) for x in (q, k_cache, v_cache, seq_lens, o_weight, out)]
+    _check("decode_attn_fwd_fp8", lib.decode_attn_fwd_fp8(*ds, float(scale), float(k_scale),
                                                           float(v_scale), _stream(stream)))
     return out
 
@@ -179,8 +191,8 @@ def decode_attn_only_fp8(q, k_cache, v_cache, seq_lens, attn_out, scale: float, 
                          stream=None) -> torch.Tensor:
     """decode_attn_only over an fp8 cache (see decode_attn_fwd_fp8); returns ``attn_out``."""
     lib = load()
-    ds = [describe(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
-    _check("decode_attn_only_fp8", lib.decode_attn_only_fp8(*[_ref(d) for d in ds], float(scale), float(k_scale),
+    ds = [_ref(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
+    _check("decode_attn_only_fp8", lib.decode_attn_only_fp8(*ds, float(scale), float(k_scale),
                                                             float(v_scale), _stream(stream)))
     return attn_out
 
@@ -188,16 +200,16 @@ def decode_attn_only_fp8(q, k_cache, v_cache, seq_lens, attn_out, scale: float, 
 def decode_attn_scores(q, k_cache, seq_lens, scores, stream=None) -> torch.Tensor:
     """scores[B, Hq, Lcap] (fp32) = q K^T for t < seq_lens[b]; returns ``scores``."""
     lib = load()
-    ds = [describe(x) for x in (q, k_cache, seq_lens, scores)]
-    _check("decode_attn_scores", lib.decode_attn_scores(*[_ref(d) for d in ds], _stream(stream)))
+    ds = [_ref(x) for x in (q, k_cache, seq_lens, scores)]
+    _check("decode_attn_scores", lib.decode_attn_scores(*ds, _stream(stream)))
     return scores
 
 
 def decode_attn_oproj(attn_flat, o_weight, out, stream=None) -> torch.Tensor:
     """out[B, N] = attn_flat[B, K] . o_weight[K, N] (bf16); returns ``out``."""
     lib = load()
-    ds = [describe(x) for x in (attn_flat, o_weight, out)]
-    _check("decode_attn_oproj", lib.decode_attn_oproj(*[_ref(d) for d in ds], _stream(stream)))
+    ds = [_ref(x) for x in (attn_flat, o_weight, out)]
+    _check("decode_attn_oproj", lib.decode_attn_oproj(*ds, _stream(stream)))
     return out
 
 

@@ -1057,6 +1057,11 @@ cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
     e = cudaFuncSetAttribute(attn_decode_kernel<NB, SCORES, S, NPAD, DIM, PAGED, KV8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDynSmem);
     if (e != cudaSuccess) return e;
+    // All of the SM's unified L1 as shared memory, the carveout of the projection kernel
+    // too, so that three projection CTAs fit on an SM the moment this kernel leaves it.
+    e = cudaFuncSetAttribute(attn_decode_kernel<NB, SCORES, S, NPAD, DIM, PAGED, KV8>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};

@@ -231,7 +231,9 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
 /*
  * Tuning options (process-wide; 0 = automatic). Keys:
  *   "attn_ctas"     CTAs of the persistent attention kernel (0: one per SM; at most 512)
- *   "oproj_path"    0 auto, 1 CUDA-core GEMV, 2 tcgen05 tensor-core GEMM
+ *   "oproj_path"    0 auto (3 for batch <= 16, else 2), 1 CUDA-core GEMV,
+ *                   2 tcgen05 tensor-core GEMM, 3 W streamed beside the attention
+ *                   kernel (batch <= 16; mma.sync)
  *   "oproj_splitk"  split-K factor of the projection (0: auto)
  *   "gemm_min_batch" smallest batch that takes the tensor-core GEMM in auto mode
  *                   (default 4)
