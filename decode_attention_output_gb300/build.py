@@ -21,8 +21,7 @@ LIB_DIR = os.path.join(PKG, "_lib")
 OBJ_DIR = os.path.join(PKG, "_lib", "obj")
 LIB_NAME = "libdecode_attn.so"
 SOURCES = ["api.cu", "attn_decode.cu", "attn_decode_d256.cu", "attn_decode_paged.cu", "attn_decode_fp8.cu",
-           "oproj_gemv.cu", "oproj_umma.cu",
-           "oproj_stream.cu"]
+           "oproj_gemv.cu", "oproj_umma.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               f"-I{INCLUDE}", f"-I{CSRC}"]

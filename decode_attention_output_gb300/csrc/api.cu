@@ -21,7 +21,7 @@ using namespace da;
 // ------------------------------------------------------------------ options
 struct Options {
   int64_t attn_ctas = 0;
-  int64_t oproj_path = 0;  // 0 auto, 1 gemv, 2 tcgen05, 3 streamed beside the attention
+  int64_t oproj_path = 0;  // 0 auto, 1 gemv, 2 tcgen05
   int64_t oproj_splitk = 0;
   int64_t gemm_min_batch = 4;  // measured crossover: GEMV ahead at B <= 2, even at 4, GEMM ahead from 8
   int64_t pdl = 1;
@@ -29,9 +29,8 @@ struct Options {
   int64_t attn_stages = 4;  // attention pipeline depth, 4 or 6 (6 measured slower)
   int64_t fused = 0;        // decode_attn_fwd as one persistent launch (measured slower so far: off)
   int64_t fused_attn_ctas = 0;  // attention workers of the fused step (0: about 4 tiles each)
-  int64_t oproj_prefetch = 1;   // streamed projection: the first CTAs pull later CTAs' W into L2
-  int64_t oproj_per_sm = 3;     // streamed projection: CTAs that fit on one SM (ring size)
-  int64_t oproj_bufs = 0;       // streamed projection: ring buffers (0: as many as fit)
+  int64_t oproj_prefetch = 0;   // tcgen05 projection behind the attention: pull the rest of each
+                                // CTA's W slice into L2 before waiting (measured no faster: off)
 };
 std::mutex g_mu;
 Options g_opt;
@@ -327,12 +326,21 @@ struct AttnPlan {
   size_t part_o_off, part_ml_off, bytes;
 };
 
-AttnPlan plan_attention(const AttnShape& s, const Options& o) {
+// Persistent CTAs of the attention kernel: one per SM, or fewer for small problems, about
+// four tiles each counted from the cache capacity (an upper bound of the device-side
+// lengths): at batch 1, kv_len 2048 (256 tiles) 64 CTAs took 9.1 us against 10.1 us for 152
+// (fewer parts per sequence to merge, the same bytes in flight). `tile_tok` = tokens per
+// tile of the variant (64 at D = 128, 32 at D = 256, 128 for an fp8 cache). The fused
+// step keeps one CTA per SM: its projection phase runs on every CTA.
+AttnPlan plan_attention(const AttnShape& s, const Options& o, int tile_tok = 0, bool fused = false) {
   AttnPlan pl;
   const int sms = std::max(1, sm_count());
+  if (tile_tok <= 0) tile_tok = tile_tokens(s.D);
+  const long long tiles = (long long)s.B * s.Hkv * ((s.Lcap + tile_tok - 1) / tile_tok);
+  const int auto_grid = fused ? sms : (int)std::max<long long>(1, std::min<long long>(sms, (tiles + 3) / 4));
   // at most kMaxAttnCtas workers: a sequence then has at most that many parts, whose merge
   // weights fit the kernel's merge scratch
-  pl.grid = std::min(o.attn_ctas > 0 ? (int)o.attn_ctas : sms, kMaxAttnCtas);
+  pl.grid = std::min(o.attn_ctas > 0 ? (int)o.attn_ctas : auto_grid, kMaxAttnCtas);
   pl.nb = s.G <= 8 ? 1 : 2;
   pl.gpad = 8 * pl.nb;
   const size_t slots = (size_t)pl.grid + (size_t)s.B * s.Hkv;
@@ -387,91 +395,6 @@ int run_gemv(const __nv_bfloat16* x, long long x_sb, const da_tensor_t* w, const
   return launch_gemv(gp, pl.bt, pdl, stream) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
-// Shared memory an SM has left for one more CTA beside a CTA that uses `other` bytes
-// (0 when that is not enough for anything).
-size_t smem_beside(size_t other) {
-  static int per_sm[kMaxDevices] = {0}, reserved[kMaxDevices] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-  if (per_sm[dev] == 0) {
-    int a = 0, r = 0;
-    if (cudaDeviceGetAttribute(&a, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&r, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
-      return 0;
-    per_sm[dev] = a;
-    reserved[dev] = r;
-  }
-  const size_t used = other + 2 * (size_t)reserved[dev];
-  return (size_t)per_sm[dev] > used ? (size_t)per_sm[dev] - used : 0;
-}
-
-// The streamed projection: a first wave of one CTA per SM with nbuf units each (all in
-// its ring before it waits for the attention), then a second wave splitting the
-// remaining units; every CTA is small enough that oproj_per_sm (3) fit on an SM.
-struct StreamPlan {
-  bool ok = false;
-  int nt = 1, grid = 0;
-  StreamParams sp;
-  size_t bytes = 0;
-};
-
-StreamPlan plan_stream(int B, int K, int N, const Options& o) {
-  StreamPlan pl;
-  memset(&pl.sp, 0, sizeof(pl.sp));
-  if (B < 1 || B > kStreamMaxBatch) return pl;
-  pl.nt = B <= 8 ? 1 : 2;
-  const int ncb = (N + kStreamCols - 1) / kStreamCols, nkc = (K + kStreamRows - 1) / kStreamRows;
-  const long long units = (long long)ncb * nkc;
-  if (units >= (1ll << 30) || ncb > (int)kMaxCounters) return pl;
-  const int sms = std::max(1, sm_count());
-  const size_t per = (size_t)std::max<int64_t>(1, o.oproj_per_sm);
-  const size_t avail = smem_beside(0) / per > 1024 ? smem_beside(0) / per - 1024 : 0;
-  const size_t xunit = (size_t)8 * pl.nt * kStreamXPitch * 2;
-  for (int nbuf = o.oproj_bufs > 0 ? (int)o.oproj_bufs : 6; nbuf >= 2; --nbuf) {
-    const size_t base = stream_smem_bytes(pl.nt, nbuf, 0);
-    if (base + nbuf * xunit > avail) continue;
-    const long long umax_fit = (long long)((avail - base) / xunit);
-    const long long wave1 = std::min<long long>(sms, (units + nbuf - 1) / nbuf);
-    const long long rest = std::max<long long>(0, units - wave1 * nbuf);
-    long long n2 = 0, umax = nbuf;
-    if (rest > 0) {
-      n2 = std::min<long long>(rest, 2ll * sms);
-      if ((rest + n2 - 1) / n2 > umax_fit) n2 = std::min<long long>(rest, (rest + umax_fit - 1) / umax_fit);
-      umax = std::max<long long>(nbuf, (rest + n2 - 1) / n2);
-    }
-    if (wave1 + n2 >= (1ll << 31) || umax > umax_fit) continue;
-    pl.sp.nkc = nkc;
-    pl.sp.units = (int)units;
-    pl.sp.nbuf = nbuf;
-    pl.sp.umax = (int)umax;
-    pl.sp.wave1 = (int)wave1;
-    pl.sp.prefetch = o.oproj_prefetch ? 1 : 0;
-    pl.grid = (int)(wave1 + n2);
-    pl.bytes = align_up((size_t)(pl.grid + ncb) * B * kStreamCols * 4, 256);
-    pl.ok = true;
-    return pl;
-  }
-  return pl;
-}
-
-int run_stream(const __nv_bfloat16* x, long long x_sb, const da_tensor_t* w, const da_tensor_t* out, int B, int K,
-               int N, char* ws, char* scratch, const StreamPlan& pl, bool pdl, cudaStream_t stream) {
-  StreamParams sp = pl.sp;
-  DA_TRY(encode_2d_map(&sp.tm_w, w->data, K, N, w->stride[0], kStreamRows));
-  sp.x = x;
-  sp.x_sb = x_sb;
-  sp.y = static_cast<__nv_bfloat16*>(out->data);
-  sp.y_sb = out->stride[0];
-  sp.part = reinterpret_cast<float*>(scratch);
-  sp.counters = reinterpret_cast<int*>(ws + kGemvCntOff);
-  sp.err = reinterpret_cast<int*>(ws + kErrOff);
-  sp.B = B;
-  sp.K = K;
-  sp.N = N;
-  sp.prefetch = pdl ? sp.prefetch : 0;  // only behind the attention kernel
-  return launch_stream(sp, pl.nt, pl.grid, pdl, stream) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
-}
-
 struct UmmaPlan {
   int npad, ksplit;
   size_t bytes;
@@ -510,32 +433,23 @@ int run_umma(const void* x, long long x_sb, const da_tensor_t* w, const da_tenso
   up.K = K;
   up.N = N;
   up.ksplit = pl.ksplit;
+  up.prefetch = pdl && options_snapshot().oproj_prefetch ? 1 : 0;
   return launch_umma(up, pl.npad, pdl, stream) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
-// The projection step: picks the streamed kernel (batch <= 16), the tcgen05 GEMM
-// (larger batches) or, on request ("oproj_path"), the CUDA-core GEMV, and says how much
-// scratch it needs. `beside` = shared memory the preceding attention kernel leaves on
-// an SM (0: the projection runs alone).
+// The projection step: picks the tcgen05 GEMM or the CUDA-core GEMV by batch size (or
+// the "oproj_path" option) and says how much scratch it needs.
 struct ProjPlan {
-  int path;  // 1 gemv, 2 tcgen05, 3 streamed
+  bool gemm;
   GemvPlan gv;
   UmmaPlan um;
-  StreamPlan st;
   size_t bytes;
 };
 
 ProjPlan plan_projection(int B, int K, int N, const Options& o) {
   ProjPlan pl;
-  pl.path = (int)o.oproj_path;
-  if (pl.path == 0) pl.path = B >= o.gemm_min_batch ? 2 : 1;
-  if (pl.path == 3) {
-    pl.st = plan_stream(B, K, N, o);
-    if (!pl.st.ok) pl.path = 2;
-  }
-  if (pl.path == 3) {
-    pl.bytes = pl.st.bytes;
-  } else if (pl.path == 2) {
+  pl.gemm = o.oproj_path == 2 || (o.oproj_path == 0 && B >= o.gemm_min_batch);
+  if (pl.gemm) {
     pl.um = plan_umma(B, K, N, o);
     pl.bytes = pl.um.bytes;
   } else {
@@ -547,8 +461,7 @@ ProjPlan plan_projection(int B, int K, int N, const Options& o) {
 
 int run_projection(const __nv_bfloat16* x, long long x_sb, const da_tensor_t* w, const da_tensor_t* out, int B,
                    int K, int N, char* ws, char* scratch, const ProjPlan& pl, bool pdl, cudaStream_t stream) {
-  if (pl.path == 3) return run_stream(x, x_sb, w, out, B, K, N, ws, scratch, pl.st, pdl, stream);
-  if (pl.path == 2) return run_umma(x, x_sb, w, out, B, K, N, ws, scratch, pl.um, pdl, stream);
+  if (pl.gemm) return run_umma(x, x_sb, w, out, B, K, N, ws, scratch, pl.um, pdl, stream);
   return run_gemv(x, x_sb, w, out, B, K, N, ws, scratch, pl.gv, pdl, stream);
 }
 
@@ -677,7 +590,7 @@ int only_checked(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t* 
   if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
   if (s.B == 0) return DA_OK;
   const Options o = options_snapshot();
-  const AttnPlan pl = plan_attention(s, o);
+  const AttnPlan pl = plan_attention(s, o, kv8 ? kTileFp8 : 0);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = nullptr;
   DA_TRY(workspace_get(pl.bytes, st, &ws));
@@ -700,18 +613,19 @@ int fwd_checked(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tenso
   if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
   if (s.B == 0) return DA_OK;
   const Options o = options_snapshot();
-  const AttnPlan ap = plan_attention(s, o);
+  const AttnPlan ap = plan_attention(s, o, kv8 ? kTileFp8 : 0);
   const size_t attn_bytes = align_up((size_t)s.B * K * 2, 256);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const FusedPlan fp = (paged || kv8) ? FusedPlan() : plan_fused(s, (int)K, (int)N, ap, o);
+  const AttnPlan fap = plan_attention(s, o, 0, true);
+  const FusedPlan fp = (paged || kv8) ? FusedPlan() : plan_fused(s, (int)K, (int)N, fap, o);
   if (fp.ok) {  // one launch: attention, grid barrier, projection
     char* ws = nullptr;
-    DA_TRY(workspace_get(ap.bytes + attn_bytes + fp.part_bytes, st, &ws));
+    DA_TRY(workspace_get(fap.bytes + attn_bytes + fp.part_bytes, st, &ws));
     char* scratch = ws + kHeaderBytes;
-    __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(scratch + ap.bytes);
-    const FusedArgs fa{&fp, o_weight, out, reinterpret_cast<float*>(scratch + ap.bytes + attn_bytes), (int)K, (int)N};
+    __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(scratch + fap.bytes);
+    const FusedArgs fa{&fp, o_weight, out, reinterpret_cast<float*>(scratch + fap.bytes + attn_bytes), (int)K, (int)N};
     const long long w_span = ((long long)(K - 1) * o_weight->stride[0] + N) * 2;
-    const int rc = run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, s.D, nullptr, 0, 0,
+    const int rc = run_attention(q, k_cache, v_cache, seq_lens, s, fap, ws, scratch, attn, K, s.D, nullptr, 0, 0,
                                  scale, st, o.l2_prefetch ? o_weight->data : nullptr, w_span, &fa);
     if (rc != DA_ERR_UNSUPPORTED) return rc;  // else: not co-resident here, take two launches
   }
@@ -755,7 +669,7 @@ int decode_attn_set_option(const char* key, int64_t value) {
   if (!key) return DA_ERR_OPTION;
   std::lock_guard<std::mutex> lk(g_mu);
   if (!strcmp(key, "attn_ctas") && value >= 0 && value <= kMaxAttnCtas) g_opt.attn_ctas = value;
-  else if (!strcmp(key, "oproj_path") && value >= 0 && value <= 3) g_opt.oproj_path = value;
+  else if (!strcmp(key, "oproj_path") && value >= 0 && value <= 2) g_opt.oproj_path = value;
   else if (!strcmp(key, "oproj_splitk") && value >= 0 && value <= 4096) g_opt.oproj_splitk = value;
   else if (!strcmp(key, "gemm_min_batch") && value >= 1) g_opt.gemm_min_batch = value;
   else if (!strcmp(key, "pdl") && (value == 0 || value == 1)) g_opt.pdl = value;
@@ -764,8 +678,6 @@ int decode_attn_set_option(const char* key, int64_t value) {
   else if (!strcmp(key, "fused") && (value == 0 || value == 1)) g_opt.fused = value;
   else if (!strcmp(key, "fused_attn_ctas") && value >= 0 && value <= kMaxAttnCtas) g_opt.fused_attn_ctas = value;
   else if (!strcmp(key, "oproj_prefetch") && (value == 0 || value == 1)) g_opt.oproj_prefetch = value;
-  else if (!strcmp(key, "oproj_per_sm") && value >= 1 && value <= 4) g_opt.oproj_per_sm = value;
-  else if (!strcmp(key, "oproj_bufs") && value >= 0 && value <= 12) g_opt.oproj_bufs = value;
   else return DA_ERR_OPTION;
   return DA_OK;
 }
@@ -783,8 +695,6 @@ int decode_attn_get_option(const char* key, int64_t* value) {
   else if (!strcmp(key, "fused")) *value = g_opt.fused;
   else if (!strcmp(key, "fused_attn_ctas")) *value = g_opt.fused_attn_ctas;
   else if (!strcmp(key, "oproj_prefetch")) *value = g_opt.oproj_prefetch;
-  else if (!strcmp(key, "oproj_per_sm")) *value = g_opt.oproj_per_sm;
-  else if (!strcmp(key, "oproj_bufs")) *value = g_opt.oproj_bufs;
   else return DA_ERR_OPTION;
   return DA_OK;
 }

@@ -174,37 +174,6 @@ cudaError_t launch_gemv(const GemvParams& p, int bt, bool pdl, cudaStream_t stre
 size_t gemv_smem_bytes(int bt, int kc);
 
 
-// ---------------------------- projection: W streamed by TMA beside the attention kernel
-// Batches up to 16. The kernel is small enough to be resident next to the attention
-// kernel (programmatic dependent launch), so its W reads overlap the attention.
-constexpr int kStreamThreads = 128;   // four warps, 16 columns of a unit each
-constexpr int kStreamCols = 64;       // columns per unit (one 128-byte row of a TMA box)
-constexpr int kStreamRows = 128;      // k-rows per unit
-constexpr int kStreamUnitBytes = kStreamCols * kStreamRows * 2;  // 16 KB
-constexpr int kStreamXPitch = kStreamRows + 8;  // bf16 per x row of a unit in shared memory
-                                                // (+16 B: conflict-free B-fragment loads)
-constexpr int kStreamMaxBatch = 16;
-
-struct StreamParams {
-  CUtensorMap tm_w;   // W [K][N] bf16 row-major: box 64 columns x 128 rows, 128B swizzle
-  const __nv_bfloat16* x;  // [B][K], rows 16-byte aligned
-  long long x_sb;
-  __nv_bfloat16* y;   // [B][N]
-  long long y_sb;
-  float* part;        // [grid + column blocks][B][64] fp32 partials
-  int* counters;      // [column blocks], zero between calls
-  int* err;
-  int B, K, N;
-  int nkc, units;     // 128-row k-chunks per column block; 64-column blocks x nkc
-  int nbuf, umax;     // ring buffers; units of one CTA at most (its x buffer)
-  int wave1;          // first-wave CTAs (nbuf units each); the rest split the remainder
-  int prefetch;       // 1: the first wave pulls the second wave's units into L2 before waiting
-};
-
-size_t stream_smem_bytes(int nt, int nbuf, int umax);
-// nt = ceil(B / 8) (1 or 2); grid = wave1 + second-wave CTAs.
-cudaError_t launch_stream(const StreamParams& p, int nt, int grid, bool pdl, cudaStream_t stream);
-
 // ------------------------------------------- projection: tcgen05 tensor-core path
 constexpr int kUmmaThreads = 128;  // warp 0: TMA producer, warp 1: MMA issuer, all four: epilogue
 constexpr int kUmmaBM = 128;       // hidden columns per tile (the MMA's M, swap-AB)
@@ -219,6 +188,7 @@ struct UmmaParams {
   int* counters;     // [batch chunks][column tiles]
   int* err;
   int B, K, N, ksplit;
+  int prefetch;      // 1: pull the k-blocks past the first ring fill into L2 before the PDL wait
 };
 
 size_t umma_smem_bytes(int npad);

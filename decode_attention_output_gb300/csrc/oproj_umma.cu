@@ -87,6 +87,13 @@ __global__ void __launch_bounds__(kUmmaThreads, 2) oproj_umma_kernel(const __gri
         tma_load_2d(a, &p.tm_w, full_bar(it), n0, k0);
         tma_load_2d(a + kUmmaBK * 128, &p.tm_w, full_bar(it), n0 + 64, k0);
       }
+      // ... and pull the rest of this CTA's W slice into L2, so that the refills after
+      // the wait come from L2 while the attention kernel's last CTAs still run.
+      if (p.prefetch)
+        for (int it = pre; it < nk; ++it) {
+          tma_prefetch_2d(&p.tm_w, n0, (kb0 + it) * kUmmaBK);
+          tma_prefetch_2d(&p.tm_w, n0 + 64, (kb0 + it) * kUmmaBK);
+        }
       pdl_wait_primary();
       for (int it = 0; it < pre; ++it)
         tma_load_2d(ring + it * C::kStage + C::kABytes, &p.tm_x, full_bar(it), (kb0 + it) * kUmmaBK, b0);

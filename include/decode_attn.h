@@ -230,10 +230,10 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
 
 /*
  * Tuning options (process-wide; 0 = automatic). Keys:
- *   "attn_ctas"     CTAs of the persistent attention kernel (0: one per SM; at most 512)
- *   "oproj_path"    0 auto (3 for batch <= 16, else 2), 1 CUDA-core GEMV,
- *                   2 tcgen05 tensor-core GEMM, 3 W streamed beside the attention
- *                   kernel (batch <= 16; mma.sync)
+ *   "attn_ctas"     CTAs of the persistent attention kernel (0: one per SM, fewer for
+ *                   small problems: about four tiles each by the cache capacity;
+ *                   at most 512)
+ *   "oproj_path"    0 auto, 1 CUDA-core GEMV, 2 tcgen05 tensor-core GEMM
  *   "oproj_splitk"  split-K factor of the projection (0: auto)
  *   "gemm_min_batch" smallest batch that takes the tensor-core GEMM in auto mode
  *                   (default 4)
@@ -252,6 +252,10 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *                   only: at D = 256 decode_attn_fwd always takes two launches
  *   "fused_attn_ctas" attention workers of the fused step (0: about four 64-token
  *                   tiles each, at most one per SM; the other CTAs start on o_weight)
+ *   "oproj_prefetch" 0 (default) or 1: in decode_attn_fwd each tcgen05 projection CTA
+ *                   pulls the part of its o_weight slice that its ring does not hold
+ *                   into L2 before it waits for the attention kernel (measured no
+ *                   faster on GB300)
  * Returns DA_OK or DA_ERR_OPTION.
  */
 int decode_attn_set_option(const char* key, int64_t value);
