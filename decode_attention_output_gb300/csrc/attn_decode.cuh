@@ -451,6 +451,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
 
+  if (warp == kGroups * kGroupWarps && lane == 0) {
+    // The producer's tensor maps first: their fetch then overlaps the set-up below (the
+    // sequence lengths' load) instead of delaying the first copy.
+    prefetch_tensormap(&p.tm_k);
+    if (!SCORES) prefetch_tensormap(&p.tm_v);
+    if (PAGED) prefetch_tensormap(&p.tm_table);
+    if (kFused) {
+      prefetch_tensormap(&p.tm_w);
+      prefetch_tensormap(&p.tm_x);
+    }
+  }
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
@@ -512,8 +523,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   // P workers share the T tiles; with P <= T every range is non-empty, so the CTAs
   // cta_of(first tile) .. cta_of(last tile) of a sequence all hold a part of it.
   const int P = T > 0 ? (int)min((long long)min((int)gridDim.x, p.attn_workers), T) : 1;
-  const long long start = (T > 0 && cta < P) ? (long long)cta * T / P : 0;
-  const long long end = (T > 0 && cta < P) ? (long long)(cta + 1) * T / P : 0;
+  // floor(c * T / P) = c * (T / P) + floor(c * (T % P) / P) in 32-bit arithmetic (T < 2^31,
+  // c <= P <= 512): no 64-bit division on the way to the first copy
+  const unsigned Tq = (unsigned)T / (unsigned)P, Tr = (unsigned)T % (unsigned)P;
+  auto split = [&](int c) { return (long long)c * Tq + (long long)(((unsigned)c * Tr) / (unsigned)P); };
+  const long long start = (T > 0 && cta < P) ? split(cta) : 0;
+  const long long end = (T > 0 && cta < P) ? split(cta + 1) : 0;
 
   if (warp == kGroups * kGroupWarps) {
     // ------------------------------------------------------------ producer
@@ -529,11 +544,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
       const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read exactly once
       // This CTA's share of the prefetch region, in 4 KB-aligned pieces, one per tile.
       const uint64_t pf_policy = l2_policy_evict_last();
-      const long long pf_per_cta = ((p.prefetch_bytes + P - 1) / P + 4095) & ~4095ll;
-      const long long pf_begin = min((long long)cta * pf_per_cta, p.prefetch_bytes);
-      const long long pf_end = min(pf_begin + pf_per_cta, p.prefetch_bytes);
-      const long long pf_piece = ((pf_end - pf_begin + (end - start) - 1) / (end - start) + 4095) & ~4095ll;
-      long long pf_next = pf_begin;
+      long long pf_next = 0, pf_end = 0, pf_piece = 0;
+      if (p.prefetch_bytes > 0) {
+        const long long pf_per_cta = ((p.prefetch_bytes + P - 1) / P + 4095) & ~4095ll;
+        pf_next = min((long long)cta * pf_per_cta, p.prefetch_bytes);
+        pf_end = min(pf_next + pf_per_cta, p.prefetch_bytes);
+        pf_piece = ((pf_end - pf_next + (end - start) - 1) / (end - start) + 4095) & ~4095ll;
+      }
       Cursor c = cursor_at(start, prefix, B, Hkv);
       long long seg0 = start;
       for (long long x = start; x < end; ++x, ++it) {
@@ -976,38 +993,50 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
           if (tid == 0) flags[1] = (atomic_add_acq_rel_gpu(p.counters + seq, 1) == n_parts - 1);
           named_bar_sync(1, kConsumerThreads);  // ... and the acquire precedes every thread's loads
           if (flags[1]) {  // every other part has landed: merge them all, in one pass
-            // Thread (h, d) loads the parts' (m, l, O[h][d]) together, eight parts per batch
-            // from clamped (always valid) addresses, masked afterwards, and merges them with
-            // a running maximum: one L2 round trip per eight parts after the counter.
-            for (int h = tid / DIM; h < G; h += kHStep) {
-              float M = kNegInf, lsum = 0.f, acc = 0.f;
+            // Thread (h, d) loads the parts' (m, l, O[h][d]) for two of its heads together,
+            // eight parts per batch from clamped (always valid) addresses, masked afterwards,
+            // and merges them with a running maximum: one L2 round trip per eight parts and
+            // head pair after the counter (a thread holds G / (256 / D) heads: two at G = 4).
+            for (int h = tid / DIM; h < G; h += 2 * kHStep) {
+              const int hs[2] = {h, h + kHStep < G ? h + kHStep : h};
+              float M[2] = {kNegInf, kNegInf}, lsum[2] = {0.f, 0.f}, acc[2] = {0.f, 0.f};
               for (int p0 = 0; p0 < n_parts; p0 += 8) {
-                float mv[8], lv[8], ov[8];
+                float mv[2][8], lv[2][8], ov[2][8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                   const long long slot = (long long)first_cta + min(p0 + u, n_parts - 1) + seq;
-                  const float* ml = p.part_ml + (slot * p.gpad + h) * 2;
-                  mv[u] = __ldcg(ml);
-                  lv[u] = __ldcg(ml + 1);
-                  ov[u] = __ldcg(p.part_o + (slot * p.gpad + h) * DIM + d);
-                }
-                float Mc = M;
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                  if (p0 + u < n_parts) Mc = fmaxf(Mc, mv[u]);  // every part holds a token: finite
-                const float r = fast_exp2(M - Mc);                // 0 on the first batch
-                lsum *= r;
-                acc *= r;
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                  if (p0 + u < n_parts) {
-                    const float f = fast_exp2(mv[u] - Mc);
-                    lsum += f * lv[u];
-                    acc += f * ov[u];
+                  for (int k = 0; k < 2; ++k) {
+                    const float* ml = p.part_ml + (slot * p.gpad + hs[k]) * 2;
+                    mv[k][u] = __ldcg(ml);
+                    lv[k][u] = __ldcg(ml + 1);
+                    ov[k][u] = __ldcg(p.part_o + (slot * p.gpad + hs[k]) * DIM + d);
                   }
-                M = Mc;
+                }
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  float Mc = M[k];
+#pragma unroll
+                  for (int u = 0; u < 8; ++u)
+                    if (p0 + u < n_parts) Mc = fmaxf(Mc, mv[k][u]);  // every part holds a token: finite
+                  const float r = fast_exp2(M[k] - Mc);              // 0 on the first batch
+                  lsum[k] *= r;
+                  acc[k] *= r;
+#pragma unroll
+                  for (int u = 0; u < 8; ++u)
+                    if (p0 + u < n_parts) {
+                      const float f = fast_exp2(mv[k][u] - Mc);
+                      lsum[k] += f * lv[k][u];
+                      acc[k] += f * ov[k][u];
+                    }
+                  M[k] = Mc;
+                }
               }
-              p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
+#pragma unroll
+              for (int k = 0; k < 2; ++k)
+                if (k == 0 || hs[1] != h)
+                  p.attn[(long long)b * p.a_sb + (long long)(kvh * G + hs[k]) * p.a_sh + d] =
+                      __float2bfloat16_rn(acc[k] / lsum[k]);
             }
             if (tid == 0) p.counters[seq] = 0;  // ready for the next call
           }

@@ -54,6 +54,11 @@ __global__ void __launch_bounds__(kUmmaThreads, 2) oproj_umma_kernel(const __gri
   const int nk = (int)((long long)(ks + 1) * nkb / p.ksplit) - kb0;  // >= 1: the host keeps ksplit <= nkb
 
   if (warp == 0) {
+    if (lane == 0) {  // fetch the tensor maps while TMEM and the barriers are set up
+      prefetch_tensormap(&p.tm_w);
+      prefetch_tensormap(&p.tm_x);
+    }
+    __syncwarp();
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
