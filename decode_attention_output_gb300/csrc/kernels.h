@@ -189,7 +189,9 @@ struct UmmaParams {
   int* err;
   int B, K, N, ksplit;
   int prefetch;      // 1: pull the k-blocks past the first ring fill into L2 before the PDL wait
+  int cluster;       // 1: the ksplit slices of a column tile are one cluster (ksplit <= 8)
 };
+constexpr int kMaxClusterSplit = 8;  // portable cluster size
 
 size_t umma_smem_bytes(int npad);
 // grid = (ceil(N / 128), ksplit, ceil(B / npad)); npad in {16, 32, 64, 128}.

@@ -13,8 +13,9 @@
 // byte offset = 1024 between groups of eight k-rows). x is K-major (canonical
 // 128-byte swizzled rows). One thread issues tcgen05.mma, tcgen05.commit frees
 // each stage, and the four warps read the fp32 accumulator out of TMEM.
-// Split-K partials are summed in a fixed order by the CTA that completes a
-// column tile last (atomic counter, no waiting).
+// The split-K slices of a column tile form a thread-block cluster and sum their fp32
+// tiles through distributed shared memory in a fixed order (more than eight slices, on
+// request only: through global partials and the CTA that completes the tile last).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -31,6 +32,7 @@ struct UmmaCfg {
   static constexpr int kTmemCols = NPAD < 32 ? 32 : NPAD;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + (2 * kStages + 1) * 8 + 16;
   static_assert(kSmem <= 113 * 1024, "two CTAs per SM");
+  static_assert((size_t)kStages * kStage >= (size_t)NPAD * kUmmaBM * 4, "the fp32 tile fits the ring");
 };
 
 template <int NPAD>
@@ -158,6 +160,32 @@ __global__ void __launch_bounds__(kUmmaThreads, 2) oproj_umma_kernel(const __gri
 #pragma unroll
     for (int b = 0; b < NPAD; ++b)
       if (n_ok && b0 + b < p.B) p.y[(long long)(b0 + b) * p.y_sb + n] = __float2bfloat16_rn(acc[b]);
+  } else if (p.cluster) {
+    // The k-slices of this column tile are one cluster: their fp32 tiles meet in
+    // distributed shared memory, red[b][m] in the ring (free: every MMA has completed,
+    // so every stage was consumed). CTA r of the cluster sums its share of the outputs
+    // over the slices in slice order (deterministic) and writes bf16.
+    float* red = reinterpret_cast<float*>(smem);
+#pragma unroll
+    for (int b = 0; b < NPAD; ++b) red[b * kUmmaBM + warp * 32 + lane] = acc[b];
+    cluster_sync();  // every slice's tile is in its CTA's shared memory
+    const int rank = (int)cluster_ctarank();
+    const int nb_valid = p.B - b0 < NPAD ? p.B - b0 : NPAD;
+    const int total = nb_valid * kUmmaBM, chunk = (total + p.ksplit - 1) / p.ksplit;
+    const int o_end = min(total, (rank + 1) * chunk);
+    const uint32_t red_u32 = smem_u32(red);
+    for (int o = rank * chunk + tid; o < o_end; o += kUmmaThreads) {
+      float v[kMaxClusterSplit];
+#pragma unroll
+      for (int q = 0; q < kMaxClusterSplit; ++q)
+        v[q] = ld_cluster_f32(cluster_map(red_u32 + 4u * o, (uint32_t)min(q, p.ksplit - 1)));
+      float sum = 0.f;
+#pragma unroll
+      for (int q = 0; q < kMaxClusterSplit; ++q) sum += q < p.ksplit ? v[q] : 0.f;
+      const int b = o / kUmmaBM, nn = n0 + o % kUmmaBM;
+      if (nn < p.N) p.y[(long long)(b0 + b) * p.y_sb + nn] = __float2bfloat16_rn(sum);
+    }
+    cluster_sync();  // no CTA leaves while another still reads its shared memory
   } else {
 #pragma unroll
     for (int b = 0; b < NPAD; ++b)
@@ -221,11 +249,15 @@ cudaError_t launch_npad(const UmmaParams& p, bool pdl, cudaStream_t stream) {
   cfg.blockDim = dim3(kUmmaThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;  // the k-slices of a column tile
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = p.cluster ? p.ksplit : 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, oproj_umma_kernel<NPAD>, p);
 }
 

@@ -234,9 +234,13 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *                   small problems: about four tiles each by the cache capacity;
  *                   at most 512)
  *   "oproj_path"    0 auto, 1 CUDA-core GEMV, 2 tcgen05 tensor-core GEMM
- *   "oproj_splitk"  split-K factor of the projection (0: auto)
+ *   "oproj_splitk"  split-K factor of the projection (0: auto, two CTAs per SM, at
+ *                   most 8)
+ *   "oproj_cluster" 1 (default): the split-K slices of a tcgen05 column tile form a
+ *                   thread-block cluster and reduce in distributed shared memory
+ *                   (split-K <= 8); 0: through global partials and an atomic counter
  *   "gemm_min_batch" smallest batch that takes the tensor-core GEMM in auto mode
- *                   (default 4)
+ *                   (default 1: every batch; the GEMV measured slower on GB300)
  *   "pdl"           1 (default): launch the projection with programmatic
  *                   dependent launch so it overlaps the attention kernel's tail
  *   "l2_prefetch"   0 (default) or 1: in decode_attn_fwd the attention kernel
