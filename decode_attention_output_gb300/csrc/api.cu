@@ -413,7 +413,12 @@ UmmaPlan plan_umma(int B, int K, int N, const Options& o) {
   int ks = (int)o.oproj_splitk;
   // two CTAs per SM, at most eight slices (a cluster): batch 8 step 53.0 -> 51.0 us against one
   // per SM; the long-context workloads within 1 % either way
-  if (ks <= 0) ks = std::min(kMaxClusterSplit, std::max(1, 2 * sms / std::max(1, mtiles * bchunks)));
+  // With K > 4096 (more than 64 k-blocks) four slices measured faster (head dim 256, K = 8192:
+  // step 100.5 -> 97.2 us).
+  if (ks <= 0) {
+    ks = std::min(kMaxClusterSplit, std::max(1, 2 * sms / std::max(1, mtiles * bchunks)));
+    if (nkb > 64) ks = std::min(ks, 4);
+  }
   pl.ksplit = std::max(1, std::min(ks, nkb));
   // up to eight slices reduce in a cluster; more (on request) through global partials
   pl.cluster = pl.ksplit > 1 && pl.ksplit <= kMaxClusterSplit && o.oproj_cluster;
