@@ -447,6 +447,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   int* flags = reinterpret_cast<int*>(smem + kFixed.off_flags());            // [0] abort, [1] last CTA
   int* prefix = reinterpret_cast<int*>(smem + lay.off_prefix());             // [B + 1]
   int* lens = reinterpret_cast<int*>(smem + lay.off_lens());                 // [B], clamped
+  float* cpart_o = reinterpret_cast<float*>(smem + lay.off_cpart());         // [HP][DIM] (cluster mode)
+  float* cpart_ml = cpart_o + HP * DIM;                                       // [HP][2]
   const uint32_t ring = smem_u32(smem);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
@@ -481,6 +483,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
     flags[0] = 0;
     flags[1] = 0;
     flags[2] = 0;
+    for (int h = 0; h < HP; ++h) {  // cluster mode: a CTA without tiles holds an empty state
+      cpart_ml[2 * h] = kNegInf;
+      cpart_ml[2 * h + 1] = 0.f;
+    }
     fence_barrier_init();
   }
   if (kFused && warp == 0) {  // TMEM for the projection accumulators (one CTA per SM)
@@ -527,8 +533,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   // c <= P <= 512): no 64-bit division on the way to the first copy
   const unsigned Tq = (unsigned)T / (unsigned)P, Tr = (unsigned)T % (unsigned)P;
   auto split = [&](int c) { return (long long)c * Tq + (long long)(((unsigned)c * Tr) / (unsigned)P); };
-  const long long start = (T > 0 && cta < P) ? split(cta) : 0;
-  const long long end = (T > 0 && cta < P) ? split(cta + 1) : 0;
+  long long start = (T > 0 && cta < P) ? split(cta) : 0;
+  long long end = (T > 0 && cta < P) ? split(cta + 1) : 0;
+  const int cs = p.cluster;  // > 1: cluster mode (one sequence per cluster)
+  if (cs > 1) {
+    const int sq = cta / cs, r = cta - sq * cs, bq = sq / Hkv, kq = sq - bq * Hkv;
+    const int nt = (prefix[bq + 1] - prefix[bq]) / Hkv;  // < 2^24 tiles: r * nt fits 32 bits
+    const long long F = prefix[bq] + (long long)kq * nt;
+    start = F + (r * nt) / cs;
+    end = F + ((r + 1) * nt) / cs;
+  }
 
   if (warp == kGroups * kGroupWarps) {
     // ------------------------------------------------------------ producer
@@ -597,7 +611,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
     const int wg = warp % kGroupWarps;   // warp in group
     // merge/output mapping: thread -> (first head tid / DIM, dim tid % DIM), heads step kHStep
     constexpr int kHStep = kConsumerThreads / DIM;
-    if (!SCORES) {  // empty sequences produce zero rows
+    if (!SCORES && cs <= 1) {  // empty sequences produce zero rows (cluster mode: in its merge)
       for (int s = cta; s < B * Hkv; s += gridDim.x) {
         const int b = s / Hkv;
         if (lens[b] != 0) continue;
@@ -959,8 +973,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
         //     two of half d / 128 (warps w0 and w0 + 2, whose partners hold the same softmax
         //     state for the same tokens): thread -> (head, dim)
         const long long F = prefix[b] + (long long)kvh * c.nt;  // first tile of this sequence
-        const int first_cta = cta_of(F, T, P), last_cta = cta_of(F + c.nt - 1, T, P);
-        const int n_parts = last_cta - first_cta + 1;
+        const int first_cta = cs > 1 ? 0 : cta_of(F, T, P), last_cta = cs > 1 ? 0 : cta_of(F + c.nt - 1, T, P);
+        const int n_parts = cs > 1 ? cs : last_cta - first_cta + 1;
         constexpr int kHold = kWide ? kGroupWarps / 2 : kGroupWarps;  // warps holding a dim
         constexpr int kWStep = kGroupWarps / kHold;
         const int d = tid % DIM, dl = d & 127, w0 = kWide ? (d >> 7) : 0;
@@ -977,7 +991,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
             acc += f * merge_o[(w * HP + h) * kMergeRow + dl];
           }
           if constexpr (KV8) acc *= p.v_scale;  // V = v_cache * v_scale (linear through every merge)
-          if (n_parts == 1) {
+          if (cs > 1) {  // cluster mode: the state waits in shared memory for the cluster merge
+            cpart_o[h * DIM + d] = acc;
+            if (d == 0) {
+              cpart_ml[2 * h] = M;
+              cpart_ml[2 * h + 1] = lsum;
+            }
+          } else if (n_parts == 1) {
             p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
           } else {
             const long long slot = (long long)cta + seq;
@@ -988,7 +1008,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
             }
           }
         }
-        if (n_parts > 1) {
+        if (cs <= 1 && n_parts > 1) {
           named_bar_sync(1, kConsumerThreads);  // every thread's partial stores precede the release
           if (tid == 0) flags[1] = (atomic_add_acq_rel_gpu(p.counters + seq, 1) == n_parts - 1);
           named_bar_sync(1, kConsumerThreads);  // ... and the acquire precedes every thread's loads
@@ -1068,6 +1088,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   }
   __syncwarp();
   __syncthreads();
+  if (!SCORES && cs > 1) {
+    // Cluster mode: the cluster's CTAs hold the partial states of one sequence; CTA r merges
+    // its share of the (head, dim) outputs over the cluster's CTAs in rank order, reading
+    // their shared memory (distributed shared memory: no global partials, no counter, no
+    // L2 round trip). A CTA without tiles holds m = -inf and is skipped.
+    cluster_sync();  // every CTA's state is in its shared memory
+    const int sq = cta / cs, r = cta - sq * cs, bq = sq / Hkv, kq = sq - bq * Hkv;
+    const int items = G * DIM, chunk = (items + cs - 1) / cs;
+    const int i_end = min(items, (r + 1) * chunk);
+    const uint32_t o_base = smem_u32(cpart_o), ml_base = smem_u32(cpart_ml);
+    for (int item = r * chunk + tid; item < i_end; item += kAttnThreads) {
+      const int h = item / DIM, d = item - h * DIM;
+      float mv[kMaxAttnCluster], lv[kMaxAttnCluster], ov[kMaxAttnCluster];
+#pragma unroll
+      for (int q = 0; q < kMaxAttnCluster; ++q) {  // all loads in flight together
+        const uint32_t rank = (uint32_t)min(q, cs - 1);
+        mv[q] = ld_cluster_f32(cluster_map(ml_base + 8u * h, rank));
+        lv[q] = ld_cluster_f32(cluster_map(ml_base + 8u * h + 4u, rank));
+        ov[q] = ld_cluster_f32(cluster_map(o_base + 4u * (uint32_t)(h * DIM + d), rank));
+      }
+      float M = kNegInf;
+#pragma unroll
+      for (int q = 0; q < kMaxAttnCluster; ++q)
+        if (q < cs) M = fmaxf(M, mv[q]);
+      float lsum = 0.f, acc = 0.f;
+#pragma unroll
+      for (int q = 0; q < kMaxAttnCluster; ++q)
+        if (q < cs && mv[q] != kNegInf) {
+          const float f = fast_exp2(mv[q] - M);
+          lsum += f * lv[q];
+          acc += f * ov[q];
+        }
+      // an empty sequence (no CTA holds a token) gives a zero row
+      p.attn[(long long)bq * p.a_sb + (long long)(kq * G + h) * p.a_sh + d] =
+          __float2bfloat16_rn(lsum > 0.f ? acc / lsum : 0.f);
+    }
+    cluster_sync();  // no CTA leaves while another still reads its shared memory
+  }
   if (kFused && warp == 0) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
@@ -1099,10 +1157,17 @@ cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   cfg.dynamicSmemBytes = attn_smem_bytes(p.B, NB, S, DIM);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // the fused step's grid barrier needs every CTA resident
-  attr[0].val.cooperative = 1;
+  if (NPAD > 0) {
+    attr[0].id = cudaLaunchAttributeCooperative;  // the fused step's grid barrier needs every CTA resident
+    attr[0].val.cooperative = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeClusterDimension;  // cluster mode: one sequence per cluster
+    attr[0].val.clusterDim.x = p.cluster > 1 ? p.cluster : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = NPAD > 0 ? 1 : 0;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, attn_decode_kernel<NB, SCORES, S, NPAD, DIM, PAGED, KV8>, p);
 }
 

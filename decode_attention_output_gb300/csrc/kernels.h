@@ -59,7 +59,10 @@ struct AttnSmem {
   // paged caches: kIdTiles rows of 16 block ids (one 64-byte TMA box per tile), rows
   // 128 bytes apart (a tensor copy's shared-memory destination is 128-byte aligned)
   __host__ __device__ constexpr size_t off_ids() const { return (off_lens() + (size_t)batch * 4 + 127) & ~(size_t)127; }
-  __host__ __device__ constexpr size_t total() const { return 1024 + off_ids() + kIdTiles * kIdStride * 4; }
+  // cluster mode: this CTA's merged state of its sequence, read by the cluster's other CTAs:
+  // O [heads][dim] then (m, l) [heads][2]
+  __host__ __device__ constexpr size_t off_cpart() const { return off_ids() + kIdTiles * kIdStride * 4; }
+  __host__ __device__ constexpr size_t total() const { return 1024 + off_cpart() + (size_t)heads() * (dim + 2) * 4; }
   static constexpr int kIdTiles = 8;
   static constexpr int kIdRow = 16;     // entries a row receives
   static constexpr int kIdStride = 32;  // entries between rows (128 bytes)
@@ -124,7 +127,12 @@ struct AttnParams {
   CUtensorMap tm_table;  // the table as one flat int32 array (one row), box 16 entries
   // fp8 (e4m3) caches only: K = k_cache * k_scale, V = v_cache * v_scale
   float k_scale, v_scale;
+  // Cluster mode (> 1): the grid is B * Hkv clusters of `cluster` CTAs, cluster s = sequence
+  // (b, kvh) = (s / Hkv, s % Hkv); CTA r of it takes tiles [r nt / cluster, (r + 1) nt / cluster)
+  // of the sequence's nt tiles and the partial states merge in distributed shared memory.
+  int cluster;
 };
+constexpr int kMaxAttnCluster = 8;  // portable cluster size
 
 // Paged caches: a power of two from 8 tokens (tiles are cut into blocks, or blocks hold
 // whole tiles; the producer's index arithmetic is shifts and masks).

@@ -76,6 +76,37 @@ def test_decode_matches_oracle(orc, w):
     assert_bf16_close(f64(out), ref_out, f"{w.name} output")
 
 
+CLUSTER_CASES = [c for c in CASES if c.name in ("g4_ragged", "zero_len", "all_zero_len", "tiny", "one_tile",
+                                                 "tile_plus_one", "g16", "g3")] + [
+    W("b1_l2k", 1, 32, 8, 2048, 512, (2048,)),
+    W("b2_ragged_short", 2, 32, 8, 700, 256, (700, 5)),
+    W("b1_g8_d", 1, 64, 8, 1500, 256, (1333,)),
+]
+
+
+@pytest.mark.parametrize("w", CLUSTER_CASES, ids=[c.name for c in CLUSTER_CASES])
+def test_cluster_mode_matches_flat_and_oracle(orc, w):
+    """Small problems run one thread-block cluster per sequence and merge the CTAs' states in
+    distributed shared memory; the flat grid merges through global partials. Both against the
+    oracle, and against each other within the bf16 rounding of the merge order."""
+    res = {}
+    for mode in (1, 0):
+        old = da.decode_attn_get_option("attn_cluster")
+        da.decode_attn_set_option("attn_cluster", mode)
+        try:
+            res[mode] = _run(w, seed=21)
+        finally:
+            da.decode_attn_set_option("attn_cluster", old)
+    x = res[1][0]
+    ref_attn, ref_out = oracle_decode(orc, x)
+    for mode, (_, attn, out) in res.items():
+        assert_bf16_close(f64(attn), ref_attn, f"{w.name} attention, cluster mode {mode}")
+        assert_bf16_close(f64(out), ref_out, f"{w.name} output, cluster mode {mode}")
+    diff = (res[1][1].float() - res[0][1].float()).abs()
+    tol = 2.0 ** -7 * res[0][1].float().abs() + 1e-3  # the two merges round differently
+    assert torch.all(diff <= tol), f"{w.name}: cluster and flat modes differ by {diff.max().item():.3e}"
+
+
 @pytest.mark.parametrize("ctas", [1, 2, 7, 300])
 def test_cta_count_does_not_change_the_result(orc, ctas):
     """Split-KV over any number of persistent CTAs (1 = no split at all, 300 = more
