@@ -242,6 +242,11 @@ cudaError_t launch_npad(const UmmaParams& p, bool pdl, cudaStream_t stream) {
   if (!configured[dev]) {
     e = cudaFuncSetAttribute(oproj_umma_kernel<NPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
+    // all of the unified L1 as shared memory: two CTAs per SM (a smaller carveout fits one,
+    // and the clusters that do not fit wait for a second wave)
+    e = cudaFuncSetAttribute(oproj_umma_kernel<NPAD>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
@@ -270,6 +275,33 @@ size_t umma_smem_bytes(int npad) {
     case 64: return UmmaCfg<64>::kSmem;
     default: return UmmaCfg<128>::kSmem;
   }
+}
+
+// Clusters of `cluster` CTAs of the npad instance that can be resident at once (0 on error).
+int umma_max_active_clusters(int npad, int cluster) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = cluster;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(kUmmaThreads);
+  cfg.gridDim = dim3(1, cluster, 1);
+  int n = 0;
+  cudaError_t e;
+  switch (npad) {
+    case 16: cfg.dynamicSmemBytes = UmmaCfg<16>::kSmem; e = cudaOccupancyMaxActiveClusters(&n, oproj_umma_kernel<16>, &cfg); break;
+    case 32: cfg.dynamicSmemBytes = UmmaCfg<32>::kSmem; e = cudaOccupancyMaxActiveClusters(&n, oproj_umma_kernel<32>, &cfg); break;
+    case 64: cfg.dynamicSmemBytes = UmmaCfg<64>::kSmem; e = cudaOccupancyMaxActiveClusters(&n, oproj_umma_kernel<64>, &cfg); break;
+    default: cfg.dynamicSmemBytes = UmmaCfg<128>::kSmem; e = cudaOccupancyMaxActiveClusters(&n, oproj_umma_kernel<128>, &cfg); break;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 cudaError_t launch_umma(const UmmaParams& p, int npad, bool pdl, cudaStream_t stream) {
