@@ -56,6 +56,25 @@ def test_options_roundtrip(lib):
     da.decode_attn_set_option("attn_ctas", 7)
     assert da.decode_attn_get_option("attn_ctas") == 7
     da.decode_attn_set_option("attn_ctas", old)
+
+
+# every documented option, its default and a value that must be refused
+OPTION_DEFAULTS = {"attn_ctas": 0, "oproj_path": 0, "oproj_splitk": 0, "gemm_min_batch": 1, "pdl": 1,
+                   "l2_prefetch": 0, "attn_stages": 4, "fused": 0, "fused_attn_ctas": 0, "oproj_prefetch": 0,
+                   "oproj_cluster": 1, "attn_cluster": 1}
+OPTION_BAD = {"attn_ctas": 513, "oproj_path": 3, "pdl": 2, "l2_prefetch": -1, "attn_stages": 5, "fused": 2,
+              "oproj_prefetch": 2, "oproj_cluster": 2, "attn_cluster": -1, "gemm_min_batch": 0}
+
+
+@pytest.mark.parametrize("key", sorted(OPTION_DEFAULTS))
+def test_option_defaults_and_range(lib, key):
+    assert da.decode_attn_get_option(key) == OPTION_DEFAULTS[key]
+    if key in OPTION_BAD:
+        with pytest.raises(da.DecodeAttnError):
+            da.decode_attn_set_option(key, OPTION_BAD[key])
+        assert da.decode_attn_get_option(key) == OPTION_DEFAULTS[key]
+    da.decode_attn_set_option(key, OPTION_DEFAULTS[key])
+    assert da.decode_attn_get_option(key) == OPTION_DEFAULTS[key]
     with pytest.raises(da.DecodeAttnError):
         da.decode_attn_set_option("no_such_option", 1)
     with pytest.raises(da.DecodeAttnError):
