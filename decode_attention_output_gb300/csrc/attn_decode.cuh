@@ -1000,11 +1000,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
           } else if (n_parts == 1) {
             p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
           } else {
+            // evict-last: a part written early in the launch (a range's first segment) must
+            // still be in L2 when the sequence's last CTA merges it, after the K/V stream
+            const uint64_t keep = l2_policy_evict_last();
             const long long slot = (long long)cta + seq;
-            p.part_o[(slot * p.gpad + h) * DIM + d] = acc;
+            st_global_hint(p.part_o + (slot * p.gpad + h) * DIM + d, acc, keep);
             if (d == 0) {
-              p.part_ml[(slot * p.gpad + h) * 2] = M;
-              p.part_ml[(slot * p.gpad + h) * 2 + 1] = lsum;
+              st_global_hint(p.part_ml + (slot * p.gpad + h) * 2, M, keep);
+              st_global_hint(p.part_ml + (slot * p.gpad + h) * 2 + 1, lsum, keep);
             }
           }
         }

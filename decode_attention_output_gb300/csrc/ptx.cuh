@@ -134,6 +134,11 @@ __device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Global store with an L2 cache-policy hint.
+__device__ __forceinline__ void st_global_hint(float* ptr, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(policy) : "memory");
+}
+
 // Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes % 16 == 0).
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes, uint64_t policy) {
   asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(policy)
