@@ -107,6 +107,23 @@ def test_cluster_mode_matches_flat_and_oracle(orc, w):
     assert torch.all(diff <= tol), f"{w.name}: cluster and flat modes differ by {diff.max().item():.3e}"
 
 
+MAX_CASES = [
+    W("max_batch_g16", 1024, 16, 1, 70, 128, tuple(int(x) for x in np.random.default_rng(11).integers(0, 71, 1024))),
+    W("max_batch_g2", 1024, 8, 4, 40, 136, tuple(int(x) for x in np.random.default_rng(12).integers(0, 41, 1024))),
+]
+
+
+@pytest.mark.parametrize("w", MAX_CASES, ids=[c.name for c in MAX_CASES])
+def test_maximum_batch_matches_oracle(orc, w):
+    """The largest batch the entry points accept (1024), with the widest GQA group (16) and
+    with 4096 (batch, KV head) sequences; ragged lengths with empty sequences; the
+    projection pads the batch to 128 rows in 8 chunks."""
+    x, attn, out = _run(w, seed=5)
+    ref_attn, ref_out = oracle_decode(orc, x)
+    assert_bf16_close(f64(attn), ref_attn, f"{w.name} attention")
+    assert_bf16_close(f64(out), ref_out, f"{w.name} output")
+
+
 @pytest.mark.parametrize("ctas", [1, 2, 7, 300])
 def test_cta_count_does_not_change_the_result(orc, ctas):
     """Split-KV over any number of persistent CTAs (1 = no split at all, 300 = more
