@@ -204,6 +204,5 @@ constexpr int kMaxClusterSplit = 8;  // portable cluster size
 size_t umma_smem_bytes(int npad);
 // grid = (ceil(N / 128), ksplit, ceil(B / npad)); npad in {16, 32, 64, 128}.
 cudaError_t launch_umma(const UmmaParams& p, int npad, bool pdl, cudaStream_t stream);
-int umma_max_active_clusters(int npad, int cluster);
 
 }  // namespace da

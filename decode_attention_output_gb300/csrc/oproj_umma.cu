@@ -277,33 +277,6 @@ size_t umma_smem_bytes(int npad) {
   }
 }
 
-// Clusters of `cluster` CTAs of the npad instance that can be resident at once (0 on error).
-int umma_max_active_clusters(int npad, int cluster) {
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = cluster;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cfg.blockDim = dim3(kUmmaThreads);
-  cfg.gridDim = dim3(1, cluster, 1);
-  int n = 0;
-  cudaError_t e;
-  switch (npad) {
-    case 16: cfg.dynamicSmemBytes = UmmaCfg<16>::kSmem; e = cudaOccupancyMaxActiveClusters(&n, oproj_umma_kernel<16>, &cfg); break;
-    case 32: cfg.dynamicSmemBytes = UmmaCfg<32>::kSmem; e = cudaOccupancyMaxActiveClusters(&n, oproj_umma_kernel<32>, &cfg); break;
-    case 64: cfg.dynamicSmemBytes = UmmaCfg<64>::kSmem; e = cudaOccupancyMaxActiveClusters(&n, oproj_umma_kernel<64>, &cfg); break;
-    default: cfg.dynamicSmemBytes = UmmaCfg<128>::kSmem; e = cudaOccupancyMaxActiveClusters(&n, oproj_umma_kernel<128>, &cfg); break;
-  }
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
-}
-
 cudaError_t launch_umma(const UmmaParams& p, int npad, bool pdl, cudaStream_t stream) {
   switch (npad) {
     case 16: return launch_npad<16>(p, pdl, stream);
