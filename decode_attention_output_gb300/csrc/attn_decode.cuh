@@ -496,6 +496,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
   // Padded head rows of the q slots stay zero for the whole kernel.
   for (int i = tid; i < (int)(S * kFixed.q_slot() / 16); i += kAttnThreads)
     reinterpret_cast<uint4*>(q_slots)[i] = make_uint4(0, 0, 0, 0);
+  // Launched with programmatic dependent launch, this grid may start while the previous
+  // kernel in the stream drains; nothing above touched global memory, and nothing below
+  // does before the previous kernel has completed and its writes are visible.
+  pdl_wait_primary();
   if (warp == 1) {  // clamped lengths, and tiles per batch row scanned into prefix
     int carry = 0;
     for (int base = 0; base < B; base += 32) {
@@ -1159,7 +1163,7 @@ cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = attn_smem_bytes(p.B, NB, S, DIM);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   if (NPAD > 0) {
     attr[0].id = cudaLaunchAttributeCooperative;  // the fused step's grid barrier needs every CTA resident
     attr[0].val.cooperative = 1;
@@ -1169,8 +1173,11 @@ cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
   }
+  // early launch behind the previous kernel (the kernel waits before any global access)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = (NPAD == 0 && p.pdl) ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, attn_decode_kernel<NB, SCORES, S, NPAD, DIM, PAGED, KV8>, p);
 }
 

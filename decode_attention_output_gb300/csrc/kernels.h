@@ -131,6 +131,7 @@ struct AttnParams {
   // (b, kvh) = (s / Hkv, s % Hkv); CTA r of it takes tiles [r nt / cluster, (r + 1) nt / cluster)
   // of the sequence's nt tiles and the partial states merge in distributed shared memory.
   int cluster;
+  int pdl;  // 1: launched with programmatic dependent launch (waits before any global access)
 };
 constexpr int kMaxAttnCluster = 8;  // portable cluster size
 

@@ -249,6 +249,10 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *                   (default 1: every batch; the GEMV measured slower on GB300)
  *   "pdl"           1 (default): launch the projection with programmatic
  *                   dependent launch so it overlaps the attention kernel's tail
+ *   "attn_pdl"      1 (default): launch the attention kernel with programmatic
+ *                   dependent launch too; it waits for the previous kernel in the
+ *                   stream to complete before its first global-memory access (every
+ *                   input is read after that), so only its start-up overlaps
  *   "l2_prefetch"   0 (default) or 1: in decode_attn_fwd the attention kernel
  *                   pulls o_weight into L2 while it streams K/V, so that the
  *                   projection reads o_weight from L2 (measured slower on GB300:
