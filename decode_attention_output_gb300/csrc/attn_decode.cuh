@@ -318,7 +318,7 @@ __device__ void fused_epilogue(const AttnParams& p, uint64_t* bars, uint32_t tme
 template <int S, int DIM>
 __device__ __forceinline__ void paged_producer(const AttnParams& p, uint32_t ring, uint8_t* q_slots, size_t q_slot,
                                                uint64_t* bars, int* flags, const int* prefix, const int* lens,
-                                               int* ids, long long start, long long end) {
+                                               int* ids, long long start, long long end, int role) {
   // This lane shares its SM sub-partition with two busy consumer warps, so every
   // instruction per tile costs: block sizes are powers of two (shifts, no divisions),
   // and all but the copies is done before waiting for the stage.
@@ -350,10 +350,15 @@ __device__ __forceinline__ void paged_producer(const AttnParams& p, uint32_t rin
   prefetch_tensormap(&p.tm_v);
   prefetch_tensormap(&p.tm_table);
   const uint64_t kv_policy = l2_policy_evict_first();
+  // Two producers (one per consumer group) share the work: this one issues the tiles whose
+  // index in the range has parity `role`, i.e. the stages of group `role` and the block-id
+  // ring rows of the same parity (S and PF are even), and walks the same cursor to skip the
+  // others.
+  static_assert(S % 2 == 0 && PF % 2 == 0, "stages and id rows split by parity");
   Cursor ca = cursor_at(start, prefix, B, Hkv);  // the tile whose ids were fetched last
   for (int k = 0; k < PF && start + k < end; ++k) {
     if (k > 0) cursor_next(ca, prefix, B, Hkv);
-    fetch(ca, k);
+    if ((k & 1) == role) fetch(ca, k);
   }
   Cursor c = cursor_at(start, prefix, B, Hkv);
   long long seg0 = start;
@@ -362,6 +367,10 @@ __device__ __forceinline__ void paged_producer(const AttnParams& p, uint32_t rin
     if (x != start) {
       cursor_next(c, prefix, B, Hkv);
       if (c.j == 0) seg0 = x;
+    }
+    if ((it & 1) != role) {  // the other producer's tile: keep the id cursor in step
+      if (x + PF < end) cursor_next(ca, prefix, B, Hkv);
+      continue;
     }
     const bool with_q = x - seg0 < kGroups;
     const int stage = it % S;
@@ -410,11 +419,12 @@ __device__ __forceinline__ void paged_producer(const AttnParams& p, uint32_t rin
   }
   // do not leave with copies in flight (every id row fetched was waited for above)
   for (int k = it > S ? it - S : 0; k < it; ++k)
-    mbar_wait_bounded(full_bar(k % S), (k / S) & 1, p.err, kErrWaitDrain, nullptr, kWaitLimitNs / 10);
+    if ((k & 1) == role) mbar_wait_bounded(full_bar(k % S), (k / S) & 1, p.err, kErrWaitDrain, nullptr, kWaitLimitNs / 10);
 }
 
 template <int NB, bool SCORES, int S, int NPAD, int DIM, bool PAGED = false, bool KV8 = false>
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(attn_threads(PAGED), 1) attn_decode_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int kThreads = attn_threads(PAGED);
   constexpr bool kFused = NPAD > 0;
   constexpr bool kWide = DIM == kHeadDimWide;
   static_assert(DIM == kHeadDim || (kWide && !kFused), "head dim 128, or 256 without the fused step");
@@ -494,7 +504,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
     tmem_relinquish();
   }
   // Padded head rows of the q slots stay zero for the whole kernel.
-  for (int i = tid; i < (int)(S * kFixed.q_slot() / 16); i += kAttnThreads)
+  for (int i = tid; i < (int)(S * kFixed.q_slot() / 16); i += kThreads)
     reinterpret_cast<uint4*>(q_slots)[i] = make_uint4(0, 0, 0, 0);
   // Launched with programmatic dependent launch, this grid may start while the previous
   // kernel in the stream drains; nothing above touched global memory, and nothing below
@@ -548,12 +558,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
     end = F + ((r + 1) * nt) / cs;
   }
 
-  if (warp == kGroups * kGroupWarps) {
-    // ------------------------------------------------------------ producer
+  if (warp >= kGroups * kGroupWarps) {
+    // ------------------------------------------------------------ producer(s)
     if constexpr (PAGED) {
       if (lane == 0)
         paged_producer<S, DIM>(p, ring, q_slots, kFixed.q_slot(), bars, flags, prefix, lens,
-                               reinterpret_cast<int*>(smem + lay.off_ids()), start, end);
+                               reinterpret_cast<int*>(smem + lay.off_ids()), start, end,
+                               warp - kGroups * kGroupWarps);
     } else if (lane == 0) {
      int it = 0;
      if (start < end) {
@@ -1105,7 +1116,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_decode_kernel(const __gr
     const int items = G * DIM, chunk = (items + cs - 1) / cs;
     const int i_end = min(items, (r + 1) * chunk);
     const uint32_t o_base = smem_u32(cpart_o), ml_base = smem_u32(cpart_ml);
-    for (int item = r * chunk + tid; item < i_end; item += kAttnThreads) {
+    for (int item = r * chunk + tid; item < i_end; item += kThreads) {
       const int h = item / DIM, d = item - h * DIM;
       float mv[kMaxAttnCluster], lv[kMaxAttnCluster], ov[kMaxAttnCluster];
 #pragma unroll
@@ -1160,7 +1171,7 @@ cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kAttnThreads);
+  cfg.blockDim = dim3(attn_threads(PAGED));
   cfg.dynamicSmemBytes = attn_smem_bytes(p.B, NB, S, DIM);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];

@@ -22,6 +22,9 @@ constexpr int kGroupWarps = 4;                 // consumer warps per group; each
 constexpr int kGroups = 2;                     // consumer groups take alternate stages
 constexpr int kConsumerThreads = kGroups * kGroupWarps * 32;
 constexpr int kAttnThreads = kConsumerThreads + 32;  // + one TMA producer warp
+// A paged cache gets one producer warp per consumer group: small blocks mean several copies
+// per tile, and one lane's issue rate set the pace.
+__host__ __device__ constexpr int attn_threads(bool paged) { return kConsumerThreads + (paged ? 64 : 32); }
 constexpr int kMaxStages = 6;                  // even stage counts: stage s always belongs to group s % 2
 constexpr int kKTileBytes = 16384;             // K tile: tile_tokens(D) x D x bf16 (both head dims)
 constexpr int kStageBytes = 2 * kKTileBytes;   // K tile + V tile
