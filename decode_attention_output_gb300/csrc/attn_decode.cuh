@@ -423,8 +423,10 @@ __device__ __forceinline__ void paged_producer(const AttnParams& p, uint32_t rin
 }
 
 template <int NB, bool SCORES, int S, int NPAD, int DIM, bool PAGED = false, bool KV8 = false>
-__global__ void __launch_bounds__(attn_threads(PAGED), 1) attn_decode_kernel(const __grid_constant__ AttnParams p) {
-  constexpr int kThreads = attn_threads(PAGED);
+__global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, SCORES)), 1)
+    attn_decode_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int kProducers = attn_producers(PAGED, NPAD > 0, SCORES);
+  constexpr int kThreads = attn_threads(kProducers);
   constexpr bool kFused = NPAD > 0;
   constexpr bool kWide = DIM == kHeadDimWide;
   static_assert(DIM == kHeadDim || (kWide && !kFused), "head dim 128, or 256 without the fused step");
@@ -566,6 +568,7 @@ __global__ void __launch_bounds__(attn_threads(PAGED), 1) attn_decode_kernel(con
                                reinterpret_cast<int*>(smem + lay.off_ids()), start, end,
                                warp - kGroups * kGroupWarps);
     } else if (lane == 0) {
+     const int role = warp - kGroups * kGroupWarps;  // with two producers: tiles of parity `role`
      int it = 0;
      if (start < end) {
       prefetch_tensormap(&p.tm_k);
@@ -579,6 +582,10 @@ __global__ void __launch_bounds__(attn_threads(PAGED), 1) attn_decode_kernel(con
         pf_next = min((long long)cta * pf_per_cta, p.prefetch_bytes);
         pf_end = min(pf_next + pf_per_cta, p.prefetch_bytes);
         pf_piece = ((pf_end - pf_next + (end - start) - 1) / (end - start) + 4095) & ~4095ll;
+        if (kProducers == 2) {  // the first producer alone pulls the region, per pair of tiles
+          if (role) pf_end = pf_next;
+          else pf_piece *= 2;
+        }
       }
       Cursor c = cursor_at(start, prefix, B, Hkv);
       long long seg0 = start;
@@ -587,6 +594,7 @@ __global__ void __launch_bounds__(attn_threads(PAGED), 1) attn_decode_kernel(con
           cursor_next(c, prefix, B, Hkv);
           if (c.j == 0) seg0 = x;
         }
+        if (kProducers == 2 && (it & 1) != role) continue;  // the other producer's tile
         const bool with_q = x - seg0 < kGroups;  // each group's first tile of the segment
         const int stage = it % S;
         const uint32_t ph = (it / S) & 1;
@@ -615,8 +623,9 @@ __global__ void __launch_bounds__(attn_threads(PAGED), 1) attn_decode_kernel(con
       // step's consumers wait for these copies before the CTA can end, so it skips this).
       if (!kFused)
       for (int k = it > S ? it - S : 0; k < it; ++k)
-        mbar_wait_bounded(full_bar(k % S), (k / S) & 1, p.err, kErrWaitDrain, nullptr,
-                          kWaitLimitNs / 10);
+        if (kProducers == 1 || (k & 1) == role)
+          mbar_wait_bounded(full_bar(k % S), (k / S) & 1, p.err, kErrWaitDrain, nullptr,
+                            kWaitLimitNs / 10);
      }
      if constexpr (kFused) fused_producer<NPAD, S>(p, ring, bars, it, flags);
     }
@@ -1171,7 +1180,7 @@ cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(attn_threads(PAGED));
+  cfg.blockDim = dim3(attn_threads(attn_producers(PAGED, NPAD > 0, SCORES)));
   cfg.dynamicSmemBytes = attn_smem_bytes(p.B, NB, S, DIM);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];

@@ -22,9 +22,14 @@ constexpr int kGroupWarps = 4;                 // consumer warps per group; each
 constexpr int kGroups = 2;                     // consumer groups take alternate stages
 constexpr int kConsumerThreads = kGroups * kGroupWarps * 32;
 constexpr int kAttnThreads = kConsumerThreads + 32;  // + one TMA producer warp
-// A paged cache gets one producer warp per consumer group: small blocks mean several copies
-// per tile, and one lane's issue rate set the pace.
-__host__ __device__ constexpr int attn_threads(bool paged) { return kConsumerThreads + (paged ? 64 : 32); }
+// Producer warps of the attention kernel: one per consumer group (each issues the tiles of
+// its group's stages) for a paged cache, where small blocks mean several copies per tile and
+// one lane's issue rate set the pace; for a contiguous cache when kContigTwoProducers.
+constexpr bool kContigTwoProducers = true;
+__host__ __device__ constexpr int attn_producers(bool paged, bool fused, bool scores) {
+  return paged || (kContigTwoProducers && !fused && !scores) ? 2 : 1;
+}
+__host__ __device__ constexpr int attn_threads(int producers) { return kConsumerThreads + 32 * producers; }
 constexpr int kMaxStages = 6;                  // even stage counts: stage s always belongs to group s % 2
 constexpr int kKTileBytes = 16384;             // K tile: tile_tokens(D) x D x bf16 (both head dims)
 constexpr int kStageBytes = 2 * kKTileBytes;   // K tile + V tile
