@@ -536,9 +536,11 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
   __syncthreads();
   if (kFused) tc_fence_after_sync();
   const uint32_t tmem = kFused ? (uint32_t)flags[3] : 0u;
-  // The projection kernel (launched with programmatic dependent launch) may now be
-  // scheduled; it waits for this grid's completion before it reads our output.
-  pdl_launch_dependents();
+  // The next kernel in the stream (launched with programmatic dependent launch) may now
+  // be scheduled; it waits for this grid's completion before it reads our output. When
+  // the projection follows, the trigger comes near the end of the CTA's tiles instead
+  // (below), so that its W_o loads do not queue in front of this grid's K/V stream.
+  if (p.trigger_at <= 0) pdl_launch_dependents();
 
   const long long T = prefix[B];
   const int cta = blockIdx.x;
@@ -920,6 +922,8 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
         if (lane == 0) mbar_arrive(empty_bar(stage));
       }
 
+      if (p.trigger_at > 0 && tid == 0 && x == (end - p.trigger_at > start ? end - p.trigger_at : start))
+        pdl_launch_dependents();
       if (!SCORES && last) {
         // ---------------------------------------- finish this sequence segment
         const int b = c.b, kvh = c.kvh, seq = b * Hkv + kvh;

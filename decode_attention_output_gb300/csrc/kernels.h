@@ -140,6 +140,9 @@ struct AttnParams {
   // of the sequence's nt tiles and the partial states merge in distributed shared memory.
   int cluster;
   int pdl;  // 1: launched with programmatic dependent launch (waits before any global access)
+  // > 0: each CTA lets the next kernel launch when it reaches the tile this many before the
+  // end of its range; 0: right after set-up
+  int trigger_at;
 };
 constexpr int kMaxAttnCluster = 8;  // portable cluster size
 

@@ -253,6 +253,12 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *                   dependent launch too; it waits for the previous kernel in the
  *                   stream to complete before its first global-memory access (every
  *                   input is read after that), so only its start-up overlaps
+ *   "attn_trigger"  3 (default): in decode_attn_fwd each attention CTA lets the
+ *                   projection kernel launch when it reaches the tile this many
+ *                   before the end of its range, so that the projection's early
+ *                   o_weight loads overlap the attention's last tiles and merges
+ *                   rather than queue in front of its K/V stream; 0: right after
+ *                   the attention's set-up. Timing only: results are identical.
  *   "l2_prefetch"   0 (default) or 1: in decode_attn_fwd the attention kernel
  *                   pulls o_weight into L2 while it streams K/V, so that the
  *                   projection reads o_weight from L2 (measured slower on GB300:

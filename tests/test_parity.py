@@ -124,6 +124,35 @@ def test_maximum_batch_matches_oracle(orc, w):
     assert_bf16_close(f64(out), ref_out, f"{w.name} output")
 
 
+TRIGGER_CASES = [
+    W("b1_l2k", 1, 32, 8, 2048, 512, (2048,)),
+    W("trig_ragged", 3, 8, 2, 300, 256, (300, 1, 129)),
+    W("trig_zero_len", 3, 8, 2, 130, 256, (0, 130, 65)),
+]
+
+
+@pytest.mark.parametrize("w", TRIGGER_CASES, ids=[c.name for c in TRIGGER_CASES])
+@pytest.mark.parametrize("ctas", [0, 1, 7])
+def test_projection_trigger_point_does_not_change_the_result(orc, w, ctas):
+    """decode_attn_fwd lets the projection kernel launch a few tiles before each attention
+    CTA's end (option attn_trigger); the projection still waits for the whole attention grid,
+    so every trigger point (at set-up, one tile before the end, three, and more than any CTA
+    holds) gives the same bits, equal to the oracle within tolerance."""
+    outs = {}
+    old = da.decode_attn_get_option("attn_trigger")
+    try:
+        for trig in (0, 1, 3, 1000):
+            da.decode_attn_set_option("attn_trigger", trig)
+            x, _, out = _run(w, seed=31, ctas=ctas)
+            outs[trig] = out
+    finally:
+        da.decode_attn_set_option("attn_trigger", old)
+    for trig, out in outs.items():
+        assert torch.equal(out, outs[0]), f"{w.name}: trigger point {trig} changed the output"
+    _, ref_out = oracle_decode(orc, x)
+    assert_bf16_close(f64(outs[3]), ref_out, f"{w.name} output")
+
+
 @pytest.mark.parametrize("ctas", [1, 2, 7, 300])
 def test_cta_count_does_not_change_the_result(orc, ctas):
     """Split-KV over any number of persistent CTAs (1 = no split at all, 300 = more

@@ -156,3 +156,18 @@ def test_fp8_repeated_calls_are_deterministic():
     x = synth.make_inputs(w, seed=37, device=DEV)
     runs = [run_fp8(w, x)[1] for _ in range(3)]
     assert torch.equal(runs[0], runs[1]) and torch.equal(runs[1], runs[2])
+
+
+def test_fp8_trigger_point_does_not_change_the_result():
+    """The projection's launch point (option attn_trigger) is timing only on the fp8 path too."""
+    w = W("f8_trig", 2, 32, 8, 1024, 512, (1024, 77))
+    x = synth.make_inputs(w, seed=23, device=DEV)
+    old = da.decode_attn_get_option("attn_trigger")
+    outs = []
+    try:
+        for trig in (0, 3):
+            da.decode_attn_set_option("attn_trigger", trig)
+            outs.append(run_fp8(w, x)[1])
+    finally:
+        da.decode_attn_set_option("attn_trigger", old)
+    assert torch.equal(outs[0], outs[1])

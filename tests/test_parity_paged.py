@@ -176,3 +176,22 @@ def test_paged_empty_batch_is_a_noop():
     attn = torch.empty((0, 8, 128), dtype=torch.bfloat16, device=DEV)
     da.decode_attn_only_paged(q, kp, kp, table, lens, attn, 0.1)
     torch.cuda.synchronize()
+
+
+def test_paged_trigger_point_does_not_change_the_result():
+    """The projection's launch point (option attn_trigger) is timing only on the paged path too."""
+    w = W("p_trig_bs16", 2, 32, 8, 1024, 512, (1024, 77))
+    x = synth.make_inputs(w, seed=23, device=DEV)
+    kp, table = scatter(x["k_cache"], 16, seed=2)
+    vp, _ = scatter(x["v_cache"], 16, seed=2)
+    old = da.decode_attn_get_option("attn_trigger")
+    outs = []
+    try:
+        for trig in (0, 3):
+            da.decode_attn_set_option("attn_trigger", trig)
+            outs.append(_paged(w, x, kp, vp, table)[1])
+    finally:
+        da.decode_attn_set_option("attn_trigger", old)
+    torch.cuda.synchronize()
+    assert da.decode_attn_device_error() == 0
+    assert torch.equal(outs[0], outs[1])
