@@ -31,7 +31,7 @@ struct Options {
   int64_t fused = 0;        // decode_attn_fwd as one persistent launch (measured slower so far: off)
   int64_t fused_attn_ctas = 0;  // attention workers of the fused step (0: about 4 tiles each)
   int64_t oproj_cluster = 1;    // tcgen05 projection: split-K slices reduce in a cluster
-  int64_t attn_cluster = 1;     // small problems: one cluster per sequence, merged on chip
+  int64_t attn_cluster = 1;     // attention in thread-block clusters with on-chip merges
   int64_t attn_pdl = 1;         // attention launched with programmatic dependent launch (eager
                                 // batch-8 step 54.5 -> 52.2 us: its CTAs start as the previous kernel drains)
   int64_t oproj_prefetch = 0;   // tcgen05 projection behind the attention: pull the rest of each
@@ -345,8 +345,33 @@ struct AttnPlan {
 // `clustered`: cluster mode may be used (the attention-only entry points: with the projection
 // kernel's CTAs streaming W beside it, the cluster-placed attention streams slower and the
 // batch-1 step measured 16.9 against 16.3 us; alone it is 8.0 against 9.1 us).
+// Where the cluster mode may be used: nowhere, only above about four tiles per SM, or at
+// any size.
+enum class ClusterUse { kNever, kLarge, kAny };
+
+ClusterUse cluster_use_only(const Options& o) {  // the attention-only entry points
+  return o.attn_cluster ? ClusterUse::kAny : ClusterUse::kNever;
+}
+// decode_attn_fwd: at batch 1 the flat grid gave the faster step (15.0 vs 15.7 us)
+ClusterUse cluster_use_fwd(const Options& o) { return o.attn_cluster ? ClusterUse::kLarge : ClusterUse::kNever; }
+
+// Clusters of cs attention CTAs resident at once on the current device (cached).
+int max_active_clusters(int cs) {
+  static std::mutex mu;
+  static int cache[kMaxDevices][kMaxAttnCluster + 1];
+  static bool known[kMaxDevices][kMaxAttnCluster + 1];
+  int dev = 0;
+  if (cs < 2 || cs > kMaxAttnCluster || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!known[dev][cs]) {
+    cache[dev][cs] = attn_max_active_clusters(cs);
+    known[dev][cs] = true;
+  }
+  return cache[dev][cs];
+}
+
 AttnPlan plan_attention(const AttnShape& s, const Options& o, int tile_tok = 0, bool fused = false,
-                        bool clustered = false) {
+                        ClusterUse clustered = ClusterUse::kNever) {
   AttnPlan pl;
   const int sms = std::max(1, sm_count());
   if (tile_tok <= 0) tile_tok = tile_tokens(s.D);
@@ -356,16 +381,28 @@ AttnPlan plan_attention(const AttnShape& s, const Options& o, int tile_tok = 0, 
   // at most kMaxAttnCtas workers: a sequence then has at most that many parts, whose merge
   // weights fit the kernel's merge scratch
   pl.grid = std::min(o.attn_ctas > 0 ? (int)o.attn_ctas : auto_grid, kMaxAttnCtas);
-  // Cluster mode for small problems (at most about four tiles per SM by capacity, room for a
-  // cluster of two or more per sequence): one cluster of up to eight CTAs per sequence, at
-  // least two tiles each, merging in distributed shared memory instead of through L2.
+  // Cluster mode where there is room for a cluster of cs >= 2 CTAs per sequence (at most 8,
+  // at least two tiles each by capacity), as many clusters as are resident at once up to
+  // the flat grid's size. The kernel gives each sequence cs CTAs of one cluster when the
+  // lengths are equal, so that every sequence merges in distributed shared memory instead
+  // of through L2 (batch 8: step 52.9 -> 50.9 us, head dim 256 97.2 -> 95.1 us); with
+  // unequal lengths it splits the tiles over the whole grid as the flat mode does (a fixed
+  // cs CTAs per sequence would leave the longest sequence to set the pace), and only the
+  // sequences whose parts fall in one cluster merge on chip.
   pl.cluster = 0;
   pl.flat_grid = pl.grid;
-  if (!fused && clustered && o.attn_cluster && o.attn_ctas == 0 && tiles <= 4ll * sms && 2 * seqs <= sms) {
+  const bool small = tiles <= 4ll * sms;
+  const bool cluster_ok = (clustered == ClusterUse::kAny || (clustered == ClusterUse::kLarge && !small)) &&
+                          attn_smem_bytes(s.B, s.G <= 8 ? 1 : 2, 4, s.D, kStageBytes, true) <= kMaxDynSmem;
+  if (!fused && cluster_ok && o.attn_ctas == 0 && 2 * seqs <= sms) {
     const long long cs = std::min<long long>({(long long)kMaxAttnCluster, sms / seqs, (tiles_seq + 1) / 2});
     if (cs >= 2) {
-      pl.cluster = (int)cs;
-      pl.grid = (int)(seqs * cs);
+      const long long want = std::max<long long>(seqs, (pl.grid + cs - 1) / cs);  // clusters
+      const long long n = std::min<long long>(want, max_active_clusters((int)cs));
+      if (n >= seqs) {
+        pl.cluster = (int)cs;
+        pl.grid = (int)(n * cs);
+      }
     }
   }
   pl.nb = s.G <= 8 ? 1 : 2;
@@ -638,7 +675,7 @@ int only_checked(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t* 
   if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
   if (s.B == 0) return DA_OK;
   const Options o = options_snapshot();
-  const AttnPlan pl = plan_attention(s, o, kv8 ? kTileFp8 : 0, false, true);
+  const AttnPlan pl = plan_attention(s, o, kv8 ? kTileFp8 : 0, false, cluster_use_only(o));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = nullptr;
   DA_TRY(workspace_get(pl.bytes, st, &ws));
@@ -661,7 +698,7 @@ int fwd_checked(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tenso
   if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
   if (s.B == 0) return DA_OK;
   const Options o = options_snapshot();
-  const AttnPlan ap = plan_attention(s, o, kv8 ? kTileFp8 : 0);
+  const AttnPlan ap = plan_attention(s, o, kv8 ? kTileFp8 : 0, false, cluster_use_fwd(o));
   const size_t attn_bytes = align_up((size_t)s.B * K * 2, 256);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const AttnPlan fap = plan_attention(s, o, 0, true);
@@ -819,7 +856,7 @@ int decode_attn_only_noalloc(const da_tensor_t* q, const da_tensor_t* k_cache, c
   if (!std::isfinite(scale)) return DA_ERR_UNSUPPORTED;
   if (s.B == 0) return DA_OK;
   const Options o = options_snapshot();
-  const AttnPlan pl = plan_attention(s, o, 0, false, true);
+  const AttnPlan pl = plan_attention(s, o, 0, false, cluster_use_only(o));
   if (kHeaderBytes + pl.bytes > kNoAllocScratchBytes) return DA_ERR_SCRATCH;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* base = nullptr;

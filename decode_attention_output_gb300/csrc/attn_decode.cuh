@@ -459,8 +459,9 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
   int* flags = reinterpret_cast<int*>(smem + kFixed.off_flags());            // [0] abort, [1] last CTA
   int* prefix = reinterpret_cast<int*>(smem + lay.off_prefix());             // [B + 1]
   int* lens = reinterpret_cast<int*>(smem + lay.off_lens());                 // [B], clamped
-  float* cpart_o = reinterpret_cast<float*>(smem + lay.off_cpart());         // [HP][DIM] (cluster mode)
-  float* cpart_ml = cpart_o + HP * DIM;                                       // [HP][2]
+  float* cpart_o = reinterpret_cast<float*>(smem + lay.off_cpart());         // [2][HP][DIM] (cluster mode)
+  float* cpart_ml = cpart_o + 2 * HP * DIM;                                   // [2][HP][2]
+  int* duty = reinterpret_cast<int*>(cpart_ml + 2 * HP * 2);  // [2][4] merges to share, [8] equal lengths
   const uint32_t ring = smem_u32(smem);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
@@ -495,9 +496,9 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
     flags[0] = 0;
     flags[1] = 0;
     flags[2] = 0;
-    for (int h = 0; h < HP; ++h) {  // cluster mode: a CTA without tiles holds an empty state
-      cpart_ml[2 * h] = kNegInf;
-      cpart_ml[2 * h + 1] = 0.f;
+    if (p.cluster > 1) {  // (the region exists in cluster launches only)
+      duty[2] = 0;  // no sequence of this CTA merges on chip (yet)
+      duty[6] = 0;
     }
     fence_barrier_init();
   }
@@ -513,7 +514,8 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
   // does before the previous kernel has completed and its writes are visible.
   pdl_wait_primary();
   if (warp == 1) {  // clamped lengths, and tiles per batch row scanned into prefix
-    int carry = 0;
+    int carry = 0, v0 = 0;
+    bool unequal = false;  // do the rows differ in tile count?
     for (int base = 0; base < B; base += 32) {
       const int b = base + lane;
       int v = 0;
@@ -522,6 +524,8 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
         lens[b] = L;
         v = ((L + kT - 1) / kT) * Hkv;
       }
+      if (base == 0) v0 = __shfl_sync(0xffffffffu, v, 0);
+      unequal |= __any_sync(0xffffffffu, b < B && v != v0);
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int n = __shfl_up_sync(0xffffffffu, v, off);
@@ -530,7 +534,10 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
       if (b < B) prefix[b + 1] = carry + v;
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
-    if (lane == 0) prefix[0] = 0;
+    if (lane == 0) {
+      prefix[0] = 0;
+      if (p.cluster > 1) duty[8] = unequal ? 0 : 1;
+    }
   }
   if (kFused) tc_fence_before_sync();
   __syncthreads();
@@ -544,23 +551,26 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
 
   const long long T = prefix[B];
   const int cta = blockIdx.x;
+  // > 1: cluster mode: the grid comes in clusters of `cs` consecutive CTAs. With equal
+  // lengths the tiles go to B * Hkv * cs workers, cs per sequence, so that the parts of
+  // every sequence lie in one cluster and merge on chip (the grid's other CTAs leave at
+  // once); otherwise to every CTA of the grid.
+  const int cs = p.cluster;
+  // With unequal lengths the cluster CTAs work as the flat grid does, without on-chip
+  // merges and without the cluster barriers at the end, which would hold every CTA of a
+  // cluster until its slowest one is done (the same flag in every CTA).
+  const bool chip = cs > 1 && duty[8];
+  int workers = min((int)gridDim.x, p.attn_workers);
+  if (chip) workers = min(workers, B * Hkv * cs);
   // P workers share the T tiles; with P <= T every range is non-empty, so the CTAs
   // cta_of(first tile) .. cta_of(last tile) of a sequence all hold a part of it.
-  const int P = T > 0 ? (int)min((long long)min((int)gridDim.x, p.attn_workers), T) : 1;
+  const int P = T > 0 ? (int)min((long long)workers, T) : 1;
   // floor(c * T / P) = c * (T / P) + floor(c * (T % P) / P) in 32-bit arithmetic (T < 2^31,
   // c <= P <= 512): no 64-bit division on the way to the first copy
   const unsigned Tq = (unsigned)T / (unsigned)P, Tr = (unsigned)T % (unsigned)P;
   auto split = [&](int c) { return (long long)c * Tq + (long long)(((unsigned)c * Tr) / (unsigned)P); };
   long long start = (T > 0 && cta < P) ? split(cta) : 0;
   long long end = (T > 0 && cta < P) ? split(cta + 1) : 0;
-  const int cs = p.cluster;  // > 1: cluster mode (one sequence per cluster)
-  if (cs > 1) {
-    const int sq = cta / cs, r = cta - sq * cs, bq = sq / Hkv, kq = sq - bq * Hkv;
-    const int nt = (prefix[bq + 1] - prefix[bq]) / Hkv;  // < 2^24 tiles: r * nt fits 32 bits
-    const long long F = prefix[bq] + (long long)kq * nt;
-    start = F + (r * nt) / cs;
-    end = F + ((r + 1) * nt) / cs;
-  }
 
   if (warp >= kGroups * kGroupWarps) {
     // ------------------------------------------------------------ producer(s)
@@ -637,7 +647,7 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
     const int wg = warp % kGroupWarps;   // warp in group
     // merge/output mapping: thread -> (first head tid / DIM, dim tid % DIM), heads step kHStep
     constexpr int kHStep = kConsumerThreads / DIM;
-    if (!SCORES && cs <= 1) {  // empty sequences produce zero rows (cluster mode: in its merge)
+    if (!SCORES) {  // empty sequences produce zero rows
       for (int s = cta; s < B * Hkv; s += gridDim.x) {
         const int b = s / Hkv;
         if (lens[b] != 0) continue;
@@ -1001,8 +1011,20 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
         //     two of half d / 128 (warps w0 and w0 + 2, whose partners hold the same softmax
         //     state for the same tokens): thread -> (head, dim)
         const long long F = prefix[b] + (long long)kvh * c.nt;  // first tile of this sequence
-        const int first_cta = cs > 1 ? 0 : cta_of(F, T, P), last_cta = cs > 1 ? 0 : cta_of(F + c.nt - 1, T, P);
-        const int n_parts = cs > 1 ? cs : last_cta - first_cta + 1;
+        const int first_cta = cta_of(F, T, P), last_cta = cta_of(F + c.nt - 1, T, P);
+        const int n_parts = last_cta - first_cta + 1;
+        // Cluster mode: a sequence whose parts all lie in this CTA's cluster leaves its state
+        // in shared memory (slot 0 if it is this CTA's first segment, else slot 1) for the
+        // on-chip merge after the loop.
+        const bool on_chip = chip && n_parts > 1 && first_cta / cs == last_cta / cs;
+        const int cslot = seg0 == start ? 0 : 1;
+        if (on_chip && tid == 0) {  // this CTA merges its share of the sequence's outputs
+          int* dt = duty + 4 * cslot;
+          dt[0] = seq;
+          dt[1] = first_cta;
+          dt[2] = n_parts;
+          dt[3] = F == split(first_cta) ? 0 : 1;  // the slot the first part sits in
+        }
         constexpr int kHold = kWide ? kGroupWarps / 2 : kGroupWarps;  // warps holding a dim
         constexpr int kWStep = kGroupWarps / kHold;
         const int d = tid % DIM, dl = d & 127, w0 = kWide ? (d >> 7) : 0;
@@ -1019,11 +1041,11 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
             acc += f * merge_o[(w * HP + h) * kMergeRow + dl];
           }
           if constexpr (KV8) acc *= p.v_scale;  // V = v_cache * v_scale (linear through every merge)
-          if (cs > 1) {  // cluster mode: the state waits in shared memory for the cluster merge
-            cpart_o[h * DIM + d] = acc;
+          if (on_chip) {
+            cpart_o[(cslot * HP + h) * DIM + d] = acc;
             if (d == 0) {
-              cpart_ml[2 * h] = M;
-              cpart_ml[2 * h + 1] = lsum;
+              cpart_ml[(cslot * HP + h) * 2] = M;
+              cpart_ml[(cslot * HP + h) * 2 + 1] = lsum;
             }
           } else if (n_parts == 1) {
             p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
@@ -1039,7 +1061,7 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
             }
           }
         }
-        if (cs <= 1 && n_parts > 1) {
+        if (!on_chip && n_parts > 1) {
           named_bar_sync(1, kConsumerThreads);  // every thread's partial stores precede the release
           if (tid == 0) flags[1] = (atomic_add_acq_rel_gpu(p.counters + seq, 1) == n_parts - 1);
           named_bar_sync(1, kConsumerThreads);  // ... and the acquire precedes every thread's loads
@@ -1119,41 +1141,47 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
   }
   __syncwarp();
   __syncthreads();
-  if (!SCORES && cs > 1) {
-    // Cluster mode: the cluster's CTAs hold the partial states of one sequence; CTA r merges
-    // its share of the (head, dim) outputs over the cluster's CTAs in rank order, reading
-    // their shared memory (distributed shared memory: no global partials, no counter, no
-    // L2 round trip). A CTA without tiles holds m = -inf and is skipped.
-    cluster_sync();  // every CTA's state is in its shared memory
-    const int sq = cta / cs, r = cta - sq * cs, bq = sq / Hkv, kq = sq - bq * Hkv;
-    const int items = G * DIM, chunk = (items + cs - 1) / cs;
-    const int i_end = min(items, (r + 1) * chunk);
+  if (!SCORES && chip) {
+    // Cluster mode: every sequence whose parts lie in this cluster is merged here. Each CTA
+    // holding a part merges its share of the (head, dim) outputs over all the parts, in
+    // CTA order, reading their shared memory (distributed shared memory: no global
+    // partials, no counter, no L2 round trip).
+    cluster_sync();  // every CTA's states are in its shared memory
     const uint32_t o_base = smem_u32(cpart_o), ml_base = smem_u32(cpart_ml);
-    for (int item = r * chunk + tid; item < i_end; item += kThreads) {
-      const int h = item / DIM, d = item - h * DIM;
-      float mv[kMaxAttnCluster], lv[kMaxAttnCluster], ov[kMaxAttnCluster];
+    for (int k = 0; k < 2; ++k) {
+      const int np = duty[4 * k + 2];
+      if (np == 0) continue;
+      const int sq = duty[4 * k], f = duty[4 * k + 1], fslot = duty[4 * k + 3];
+      const int bq = sq / Hkv, kq = sq - bq * Hkv;
+      const int items = G * DIM, chunk = (items + np - 1) / np, mine = cta - f;
+      const int i_end = min(items, (mine + 1) * chunk);
+      for (int item = mine * chunk + tid; item < i_end; item += kThreads) {
+        const int h = item / DIM, d = item - h * DIM;
+        float mv[kMaxAttnCluster], lv[kMaxAttnCluster], ov[kMaxAttnCluster];
 #pragma unroll
-      for (int q = 0; q < kMaxAttnCluster; ++q) {  // all loads in flight together
-        const uint32_t rank = (uint32_t)min(q, cs - 1);
-        mv[q] = ld_cluster_f32(cluster_map(ml_base + 8u * h, rank));
-        lv[q] = ld_cluster_f32(cluster_map(ml_base + 8u * h + 4u, rank));
-        ov[q] = ld_cluster_f32(cluster_map(o_base + 4u * (uint32_t)(h * DIM + d), rank));
-      }
-      float M = kNegInf;
-#pragma unroll
-      for (int q = 0; q < kMaxAttnCluster; ++q)
-        if (q < cs) M = fmaxf(M, mv[q]);
-      float lsum = 0.f, acc = 0.f;
-#pragma unroll
-      for (int q = 0; q < kMaxAttnCluster; ++q)
-        if (q < cs && mv[q] != kNegInf) {
-          const float f = fast_exp2(mv[q] - M);
-          lsum += f * lv[q];
-          acc += f * ov[q];
+        for (int q = 0; q < kMaxAttnCluster; ++q) {  // all loads in flight together
+          const int qq = min(q, np - 1);
+          // the first part is in the slot its CTA chose; the others are their CTAs' first segments
+          const uint32_t slot = qq == 0 ? (uint32_t)fslot : 0u;
+          const uint32_t rank = (uint32_t)((f + qq) % cs);
+          mv[q] = ld_cluster_f32(cluster_map(ml_base + 8u * (slot * HP + h), rank));
+          lv[q] = ld_cluster_f32(cluster_map(ml_base + 8u * (slot * HP + h) + 4u, rank));
+          ov[q] = ld_cluster_f32(cluster_map(o_base + 4u * (uint32_t)((slot * HP + h) * DIM + d), rank));
         }
-      // an empty sequence (no CTA holds a token) gives a zero row
-      p.attn[(long long)bq * p.a_sb + (long long)(kq * G + h) * p.a_sh + d] =
-          __float2bfloat16_rn(lsum > 0.f ? acc / lsum : 0.f);
+        float M = kNegInf;
+#pragma unroll
+        for (int q = 0; q < kMaxAttnCluster; ++q)
+          if (q < np) M = fmaxf(M, mv[q]);  // every part holds a token: finite
+        float lsum = 0.f, acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < kMaxAttnCluster; ++q)
+          if (q < np) {
+            const float w = fast_exp2(mv[q] - M);
+            lsum += w * lv[q];
+            acc += w * ov[q];
+          }
+        p.attn[(long long)bq * p.a_sb + (long long)(kq * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
+      }
     }
     cluster_sync();  // no CTA leaves while another still reads its shared memory
   }
@@ -1185,14 +1213,14 @@ cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(attn_threads(attn_producers(PAGED, NPAD > 0, SCORES)));
-  cfg.dynamicSmemBytes = attn_smem_bytes(p.B, NB, S, DIM);
+  cfg.dynamicSmemBytes = attn_smem_bytes(p.B, NB, S, DIM, kStageBytes, p.cluster > 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   if (NPAD > 0) {
     attr[0].id = cudaLaunchAttributeCooperative;  // the fused step's grid barrier needs every CTA resident
     attr[0].val.cooperative = 1;
   } else {
-    attr[0].id = cudaLaunchAttributeClusterDimension;  // cluster mode: one sequence per cluster
+    attr[0].id = cudaLaunchAttributeClusterDimension;  // cluster mode: on-chip merges
     attr[0].val.clusterDim.x = p.cluster > 1 ? p.cluster : 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;

@@ -67,29 +67,43 @@ struct AttnSmem {
   // paged caches: kIdTiles rows of 16 block ids (one 64-byte TMA box per tile), rows
   // 128 bytes apart (a tensor copy's shared-memory destination is 128-byte aligned)
   __host__ __device__ constexpr size_t off_ids() const { return (off_lens() + (size_t)batch * 4 + 127) & ~(size_t)127; }
-  // cluster mode: this CTA's merged state of its sequence, read by the cluster's other CTAs:
-  // O [heads][dim] then (m, l) [heads][2]
+  // cluster mode: this CTA's merged states of the sequences it shares with other CTAs of its
+  // cluster (slot 0: its first segment, slot 1: its last), read by those CTAs:
+  // O [2][heads][dim], then (m, l) [2][heads][2], then the merge duties int [2][4] and
+  // the equal-lengths flag (int [4] with padding)
   __host__ __device__ constexpr size_t off_cpart() const { return off_ids() + kIdTiles * kIdStride * 4; }
-  __host__ __device__ constexpr size_t total() const { return 1024 + off_cpart() + (size_t)heads() * (dim + 2) * 4; }
+  __host__ __device__ constexpr size_t cpart_bytes() const { return 2 * (size_t)heads() * (dim + 2) * 4 + 48; }
+  // the cluster-mode states only in clusters (at most half as many sequences as SMs)
+  __host__ __device__ constexpr size_t total(bool cluster = false) const {
+    return 1024 + off_cpart() + (cluster ? cpart_bytes() : 0);
+  }
   static constexpr int kIdTiles = 8;
   static constexpr int kIdRow = 16;     // entries a row receives
   static constexpr int kIdStride = 32;  // entries between rows (128 bytes)
 };
 
 constexpr size_t kMaxDynSmem = 232448;  // 227 KB per CTA on sm_100-class GPUs
-constexpr size_t attn_smem_bytes(int batch, int nb, int stages, int dim = kHeadDim, int stage_bytes = kStageBytes) {
-  return AttnSmem(nb, batch, stages, dim, stage_bytes).total();
+constexpr size_t attn_smem_bytes(int batch, int nb, int stages, int dim = kHeadDim, int stage_bytes = kStageBytes,
+                                 bool cluster = false) {
+  return AttnSmem(nb, batch, stages, dim, stage_bytes).total(cluster);
 }
 // fp8 (e4m3) caches: a tile is 128 tokens (128 x 128 dims x 1 byte of K and of V), so a
 // stage holds the same 32 KB and the ring the same 4 stages as for bf16.
 constexpr int kTileFp8 = 128;
 static_assert(AttnSmem(2, kMaxBatch, 4).total() <= kMaxDynSmem, "attention kernel exceeds 227 KB of shared memory");
+// Cluster mode needs room for two parked states: every group width at D = 128, up to
+// eight heads per group at D = 256 (the host checks each launch; wider groups at D = 256
+// merge through L2).
+static_assert(AttnSmem(2, 128, 4).total(true) <= kMaxDynSmem, "cluster mode (D = 128) exceeds 227 KB");
+static_assert(AttnSmem(1, 128, 4, kHeadDimWide).total(true) <= kMaxDynSmem, "cluster mode (D = 256) exceeds 227 KB");
 static_assert(AttnSmem(2, kMaxBatch, 4, kHeadDimWide).total() <= kMaxDynSmem,
               "attention kernel (D = 256) exceeds 227 KB of shared memory");
 // 4 stages by default (measured faster than 6 on the GB300: deeper rings slowed the
 // stream); 6 on request when it fits this batch and group width (D = 128 only).
-constexpr int attn_stages_for(int batch, int nb, int requested) {
-  return requested == kMaxStages && attn_smem_bytes(batch, nb, kMaxStages) <= kMaxDynSmem ? kMaxStages : 4;
+constexpr int attn_stages_for(int batch, int nb, int requested, bool cluster = false) {
+  return requested == kMaxStages && attn_smem_bytes(batch, nb, kMaxStages, kHeadDim, kStageBytes, cluster) <= kMaxDynSmem
+             ? kMaxStages
+             : 4;
 }
 
 struct AttnParams {
@@ -135,9 +149,9 @@ struct AttnParams {
   CUtensorMap tm_table;  // the table as one flat int32 array (one row), box 16 entries
   // fp8 (e4m3) caches only: K = k_cache * k_scale, V = v_cache * v_scale
   float k_scale, v_scale;
-  // Cluster mode (> 1): the grid is B * Hkv clusters of `cluster` CTAs, cluster s = sequence
-  // (b, kvh) = (s / Hkv, s % Hkv); CTA r of it takes tiles [r nt / cluster, (r + 1) nt / cluster)
-  // of the sequence's nt tiles and the partial states merge in distributed shared memory.
+  // Cluster mode (> 1): the grid is launched in clusters of `cluster` consecutive CTAs; the
+  // tiles are split over the CTAs as always, and a sequence whose parts all lie in one
+  // cluster merges them in distributed shared memory (the others through L2).
   int cluster;
   int pdl;  // 1: launched with programmatic dependent launch (waits before any global access)
   // > 0: each CTA lets the next kernel launch when it reaches the tile this many before the
@@ -171,6 +185,9 @@ cudaError_t launch_attention_d256(const AttnParams& p, int grid, int nb, bool sc
 cudaError_t launch_attention_paged(const AttnParams& p, int grid, int nb, int dim, cudaStream_t stream);
 // Attention over an fp8 (e4m3) cache, D = 128 (p.k_scale, p.v_scale set).
 cudaError_t launch_attention_fp8(const AttnParams& p, int grid, int nb, cudaStream_t stream);
+// Clusters of `cluster` attention CTAs (one per SM) that can be resident at once on the
+// current device (the GPCs' SM counts leave some SMs out); 0 if the query fails.
+int attn_max_active_clusters(int cluster);
 
 // ------------------------------------------------------- projection: GEMV path
 constexpr int kGemvThreads = 256;

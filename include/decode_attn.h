@@ -236,12 +236,16 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *   "oproj_path"    0 auto, 1 CUDA-core GEMV, 2 tcgen05 tensor-core GEMM
  *   "oproj_splitk"  split-K factor of the projection (0: auto, two CTAs per SM, at
  *                   most 8)
- *   "attn_cluster"  1 (default): decode_attn_only (and its fp8, paged and
- *                   no-allocation forms) runs small problems (at most about four
- *                   tiles per SM) as one thread-block cluster of up to 8 CTAs per
- *                   (batch, KV head) sequence, merging the CTAs' partial states in
- *                   distributed shared memory; 0: always the flat grid.
- *                   decode_attn_fwd keeps the flat grid (measured faster there)
+ *   "attn_cluster"  1 (default): where there is room for two or more CTAs per
+ *                   (batch, KV head) sequence, the attention kernel is launched in
+ *                   thread-block clusters of up to 8 CTAs (decode_attn_fwd: only
+ *                   above about four tiles per SM). When every sequence has the same
+ *                   length, each gets the CTAs of one cluster and their partial
+ *                   states merge in distributed shared memory; otherwise the tiles
+ *                   are split evenly over the whole grid as in the flat mode, and
+ *                   only the sequences whose parts fall in one cluster merge on
+ *                   chip (the rest through L2). 0: always the flat grid. Results
+ *                   agree within the rounding of the merge order.
  *   "oproj_cluster" 1 (default): the split-K slices of a tcgen05 column tile form a
  *                   thread-block cluster and reduce in distributed shared memory
  *                   (split-K <= 8); 0: through global partials and an atomic counter

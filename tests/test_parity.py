@@ -81,6 +81,13 @@ CLUSTER_CASES = [c for c in CASES if c.name in ("g4_ragged", "zero_len", "all_ze
     W("b1_l2k", 1, 32, 8, 2048, 512, (2048,)),
     W("b2_ragged_short", 2, 32, 8, 700, 256, (700, 5)),
     W("b1_g8_d", 1, 64, 8, 1500, 256, (1333,)),
+    # clusters of two (64 sequences) and four (32): every sequence on chip with equal lengths,
+    # a mix of on-chip and L2 merges with ragged ones (balanced split either way)
+    W("b8_equal_cs2", 8, 32, 8, 1024, 512, (1024,) * 8),
+    W("b8_ragged_cs2", 8, 32, 8, 2048, 512, (2048, 0, 1, 1500, 64, 2000, 777, 129)),
+    W("b4_equal_cs4", 4, 32, 8, 4096, 256, (4096,) * 4),
+    W("b4_ragged_cs4", 4, 32, 8, 4096, 256, (4096, 100, 3000, 65)),
+    W("b2_g16_cs8", 2, 32, 2, 2000, 256, (2000, 999)),
 ]
 
 
@@ -90,7 +97,7 @@ def test_cluster_mode_matches_flat_and_oracle(orc, w):
     distributed shared memory; the flat grid merges through global partials. Both against the
     oracle, and against each other within the bf16 rounding of the merge order."""
     res = {}
-    for mode in (1, 0):
+    for mode in (1, 0):  # clusters where they fit (the default), never
         old = da.decode_attn_get_option("attn_cluster")
         da.decode_attn_set_option("attn_cluster", mode)
         try:
@@ -102,9 +109,11 @@ def test_cluster_mode_matches_flat_and_oracle(orc, w):
     for mode, (_, attn, out) in res.items():
         assert_bf16_close(f64(attn), ref_attn, f"{w.name} attention, cluster mode {mode}")
         assert_bf16_close(f64(out), ref_out, f"{w.name} output, cluster mode {mode}")
-    diff = (res[1][1].float() - res[0][1].float()).abs()
-    tol = 2.0 ** -7 * res[0][1].float().abs() + 1e-3  # the two merges round differently
-    assert torch.all(diff <= tol), f"{w.name}: cluster and flat modes differ by {diff.max().item():.3e}"
+    for mode in (1,):
+        for i, what in ((1, "attention"), (2, "output")):
+            diff = (res[mode][i].float() - res[0][i].float()).abs()
+            tol = 2.0 ** -7 * res[0][i].float().abs() + 1e-3  # the two merges round differently
+            assert torch.all(diff <= tol), f"{w.name}: {what}, cluster mode {mode} and flat differ by {diff.max().item():.3e}"
 
 
 MAX_CASES = [
@@ -343,15 +352,17 @@ class _Path:
         da.decode_attn_set_option("oproj_path", self.old)
 
 
-@pytest.mark.parametrize("B", [1, 2, 3, 8, 9, 16, 17, 32, 33, 64, 65, 128, 130])
-@pytest.mark.parametrize("K,N", [(1088, 384), (256, 264), (4096, 4096)])
+# every batch on the small shapes; the full-size W (4096 x 4096) at a few batch sizes
+GEMM_EXACT = [(B, K, N) for K, N in [(1088, 384), (256, 264)] for B in (1, 2, 3, 8, 9, 16, 17, 32, 33, 64, 65, 128, 130)]
+GEMM_EXACT += [(B, 4096, 4096) for B in (1, 8, 16, 64)]
+
+
+@pytest.mark.parametrize("B,K,N", GEMM_EXACT)
 @pytest.mark.parametrize("path", [1, 2])
 def test_oproj_gemm_integer_exact(path, B, K, N):
     """Both projection paths (1: CUDA-core GEMV, 2: tcgen05): integer operands make every
     fp32 sum exact, so the result is the bf16 rounding of the exact integer matmul
     (batch padding, batch chunks, ragged split-K, partial column tiles)."""
-    if K == 4096 and B not in (1, 8, 16, 64):
-        pytest.skip("full-size W: a few batch sizes")
     g = torch.Generator(device="cpu").manual_seed(300 + B + K)
     xi = torch.randint(-8, 9, (B, K), generator=g)
     wi = torch.randint(-1, 2, (K, N), generator=g)

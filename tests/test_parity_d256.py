@@ -63,6 +63,10 @@ CASES = [
     W("d256_tiny", 1, 2, 1, 1, 8, (1,)),
     W("d256_one_tile", 1, 8, 2, 32, 256, (32,)),
     W("d256_many_batches", 40, 8, 1, 70, 128, tuple(int(x) for x in np.random.default_rng(7).integers(0, 71, 40))),
+    # clusters of two and four CTAs (on-chip merges), and G = 16, which merges through L2
+    W("d256_equal_cs2", 8, 32, 8, 1024, 512, (1024,) * 8),
+    W("d256_ragged_cs4", 4, 32, 8, 2048, 256, (2048, 5, 1500, 33)),
+    W("d256_g16_flat", 2, 32, 2, 1000, 256, (1000, 400)),
 ]
 
 
@@ -84,6 +88,23 @@ def test_decode_d256_matches_oracle(orc, w):
     ref_attn, ref_out = oracle_decode(orc, x)
     assert_bf16_close(f64(attn), ref_attn, f"{w.name} attention")
     assert_bf16_close(f64(out), ref_out, f"{w.name} output")
+
+
+CLUSTER_CASES = [c for c in CASES if c.name in ("d256_equal_cs2", "d256_ragged_cs4", "d256_g16_flat", "d256_g4_ragged",
+                                                 "d256_zero_len", "d256_tiny")]
+
+
+@pytest.mark.parametrize("w", CLUSTER_CASES, ids=[c.name for c in CLUSTER_CASES])
+def test_d256_cluster_and_flat_grids(orc, w):
+    """Clusters of two to eight CTAs with on-chip merges (the default where they fit; G = 16
+    at D = 256 has no room for the parked states and merges through L2) and the flat grid
+    (option attn_cluster = 0), both against the oracle."""
+    for mode in (1, 0):
+        with _Opt(attn_cluster=mode):
+            x, attn, out = _run(w, seed=3)
+        ref_attn, ref_out = oracle_decode(orc, x)
+        assert_bf16_close(f64(attn), ref_attn, f"{w.name} attention, attn_cluster {mode}")
+        assert_bf16_close(f64(out), ref_out, f"{w.name} output, attn_cluster {mode}")
 
 
 @pytest.mark.parametrize("ctas", [1, 2, 7, 300])

@@ -72,6 +72,9 @@ CASES = [
     W("f8_tiny", 1, 2, 1, 1, 8, (1,)),
     W("f8_tile_plus_one", 1, 8, 2, 65, 256, (65,)),
     W("f8_many_batches", 40, 8, 1, 70, 128, tuple(int(x) for x in np.random.default_rng(8).integers(0, 71, 40))),
+    # clusters of two and four CTAs (on-chip merges; a ragged mix partly through L2)
+    W("f8_equal_cs2", 8, 32, 8, 2048, 512, (2048,) * 8),
+    W("f8_ragged_cs4", 4, 32, 8, 4096, 256, (4096, 100, 3000, 129)),
 ]
 
 
@@ -79,6 +82,24 @@ CASES = [
 def test_fp8_matches_oracle(orc, w):
     x = synth.make_inputs(w, seed=31, device=DEV)
     attn, out = run_fp8(w, x)
+    ref_attn, ref_out = oracle_fp8(orc, x)
+    assert_bf16_close(f64(attn), ref_attn, f"{w.name} attention")
+    assert_bf16_close(f64(out), ref_out, f"{w.name} output")
+
+
+CLUSTER_CASES = [c for c in CASES if c.name in ("f8_equal_cs2", "f8_ragged_cs4", "f8_g4_ragged", "f8_zero_len")]
+
+
+@pytest.mark.parametrize("w", CLUSTER_CASES, ids=[c.name for c in CLUSTER_CASES])
+def test_fp8_flat_grid(orc, w):
+    """The flat grid (option attn_cluster = 0) on the cases that take clusters by default."""
+    x = synth.make_inputs(w, seed=33, device=DEV)
+    old = da.decode_attn_get_option("attn_cluster")
+    da.decode_attn_set_option("attn_cluster", 0)
+    try:
+        attn, out = run_fp8(w, x)
+    finally:
+        da.decode_attn_set_option("attn_cluster", old)
     ref_attn, ref_out = oracle_fp8(orc, x)
     assert_bf16_close(f64(attn), ref_attn, f"{w.name} attention")
     assert_bf16_close(f64(out), ref_out, f"{w.name} output")

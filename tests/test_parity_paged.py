@@ -62,6 +62,9 @@ CASES = [  # (workload, block size); Lcap is a multiple of the block size
     (W("p_d256_bs32", 2, 16, 2, 192, 256, (192, 33), D=256), 32),
     (W("p_d256_bs64_g16", 2, 32, 2, 256, 256, (256, 31), D=256), 64),
     (W("p_d256_bs8", 2, 8, 2, 96, 128, (96, 9), D=256), 8),
+    # clusters of two CTAs (on-chip merges; a ragged mix partly through L2)
+    (W("p_equal_cs2_bs16", 8, 32, 8, 1024, 512, (1024,) * 8), 16),
+    (W("p_ragged_cs2_bs64", 8, 32, 8, 2048, 512, (2048, 0, 1, 1500, 64, 2000, 777, 129)), 64),
 ]
 
 
@@ -195,3 +198,30 @@ def test_paged_trigger_point_does_not_change_the_result():
     torch.cuda.synchronize()
     assert da.decode_attn_device_error() == 0
     assert torch.equal(outs[0], outs[1])
+
+
+CLUSTER_CASES = [c for c in CASES if c[0].name in ("p_equal_cs2_bs16", "p_ragged_cs2_bs64", "p_g4_bs16", "p_d256_bs16")]
+
+
+@pytest.mark.parametrize("w,bs", CLUSTER_CASES, ids=[c[0].name for c in CLUSTER_CASES])
+def test_paged_flat_grid(orc, w, bs):
+    """The flat grid (option attn_cluster = 0) on the cases that take clusters by default: the
+    paged path equals the contiguous one under the same plan, and the oracle."""
+    x = synth.make_inputs(w, seed=24, device=DEV)
+    kp, table = scatter(x["k_cache"], bs, seed=3)
+    vp, _ = scatter(x["v_cache"], bs, seed=3)
+    old = da.decode_attn_get_option("attn_cluster")
+    da.decode_attn_set_option("attn_cluster", 0)
+    try:
+        attn, out = _paged(w, x, kp, vp, table)
+        attn0, out0 = _contiguous(w, x)
+        torch.cuda.synchronize()
+    finally:
+        da.decode_attn_set_option("attn_cluster", old)
+    assert da.decode_attn_device_error() == 0
+    assert torch.equal(attn, attn0) and torch.equal(out, out0)
+    lens = x["seq_lens"].cpu().numpy().astype(np.int32)
+    ref_attn, ref_out = orc.decode_paged(synth.to_bits(x["q"]), synth.to_bits(kp), synth.to_bits(vp),
+                                         table.cpu().numpy(), lens, synth.to_bits(x["o_weight"]), x["scale"])
+    assert_bf16_close(f64(attn), ref_attn, f"{w.name} attention")
+    assert_bf16_close(f64(out), ref_out, f"{w.name} output")
