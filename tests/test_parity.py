@@ -93,9 +93,11 @@ CLUSTER_CASES = [c for c in CASES if c.name in ("g4_ragged", "zero_len", "all_ze
 
 @pytest.mark.parametrize("w", CLUSTER_CASES, ids=[c.name for c in CLUSTER_CASES])
 def test_cluster_mode_matches_flat_and_oracle(orc, w):
-    """Small problems run one thread-block cluster per sequence and merge the CTAs' states in
-    distributed shared memory; the flat grid merges through global partials. Both against the
-    oracle, and against each other within the bf16 rounding of the merge order."""
+    """Where there is room, the attention runs in thread-block clusters; with equal lengths each
+    sequence's parts share a cluster and merge in distributed shared memory, with unequal ones
+    the tiles are split over the whole grid and merged through global partials, as on the flat
+    grid (option attn_cluster = 0). Both against the oracle, and against each other within the
+    bf16 rounding of the merge order."""
     res = {}
     for mode in (1, 0):  # clusters where they fit (the default), never
         old = da.decode_attn_get_option("attn_cluster")
