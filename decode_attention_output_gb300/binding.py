@@ -110,8 +110,15 @@ def _ref(t):
     return None if t is None else _pack(t)
 
 
+# The raw handle of the current stream without building a torch.cuda.Stream object
+# (0.3 us against 2.9 us per call); the public route where torch lacks the accessor.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> int | None:
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
@@ -129,7 +136,7 @@ def status_str(code: int) -> str:
 
 def decode_attn_fwd(q, k_cache, v_cache, seq_lens, o_weight, out, scale: float, stream=None) -> torch.Tensor:
     """out[B, N] = (softmax(scale * q K^T) V)_flat . o_weight; returns ``out``."""
-    lib = load()
+    lib = _lib or load()  # the lock only until the library is loaded
     ds = [_ref(x) for x in (q, k_cache, v_cache, seq_lens, o_weight, out)]
     _check("decode_attn_fwd", lib.decode_attn_fwd(*ds, float(scale), _stream(stream)))
     return out
@@ -137,7 +144,7 @@ def decode_attn_fwd(q, k_cache, v_cache, seq_lens, o_weight, out, scale: float, 
 
 def decode_attn_only(q, k_cache, v_cache, seq_lens, attn_out, scale: float, stream=None) -> torch.Tensor:
     """attn_out[B, Hq, D] = softmax(scale * q K^T) V (bf16); returns ``attn_out``."""
-    lib = load()
+    lib = _lib or load()  # the lock only until the library is loaded
     ds = [_ref(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
     _check("decode_attn_only", lib.decode_attn_only(*ds, float(scale), _stream(stream)))
     return attn_out
@@ -149,7 +156,7 @@ def decode_attn_only_noalloc(q, k_cache, v_cache, seq_lens, attn_out, scale: flo
     pool, or no device-wide synchronisation allowed on the request path). Uses a
     fixed 8 MiB scratch array inside the library; calls that overlap on the GPU race
     on it. Raises DecodeAttnError (DA_ERR_SCRATCH) when a call needs more scratch."""
-    lib = load()
+    lib = _lib or load()  # the lock only until the library is loaded
     ds = [_ref(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
     _check("decode_attn_only_noalloc",
            lib.decode_attn_only_noalloc(*ds, float(scale), _stream(stream)))
@@ -160,7 +167,7 @@ def decode_attn_fwd_paged(q, k_pages, v_pages, block_table, seq_lens, o_weight, 
                           stream=None) -> torch.Tensor:
     """decode_attn_fwd over a paged cache: k_pages / v_pages [num_blocks, Hkv, block_size, D],
     block_table [B, max_blocks] int32; returns ``out``."""
-    lib = load()
+    lib = _lib or load()  # the lock only until the library is loaded
     ds = [_ref(x) for x in (q, k_pages, v_pages, block_table, seq_lens, o_weight, out)]
     _check("decode_attn_fwd_paged", lib.decode_attn_fwd_paged(*ds, float(scale), _stream(stream)))
     return out
@@ -169,7 +176,7 @@ def decode_attn_fwd_paged(q, k_pages, v_pages, block_table, seq_lens, o_weight, 
 def decode_attn_only_paged(q, k_pages, v_pages, block_table, seq_lens, attn_out, scale: float,
                            stream=None) -> torch.Tensor:
     """decode_attn_only over a paged cache (see decode_attn_fwd_paged); returns ``attn_out``."""
-    lib = load()
+    lib = _lib or load()  # the lock only until the library is loaded
     ds = [_ref(x) for x in (q, k_pages, v_pages, block_table, seq_lens, attn_out)]
     _check("decode_attn_only_paged",
            lib.decode_attn_only_paged(*ds, float(scale), _stream(stream)))
@@ -180,7 +187,7 @@ def decode_attn_fwd_fp8(q, k_cache, v_cache, seq_lens, o_weight, out, scale: flo
                         stream=None) -> torch.Tensor:
     """decode_attn_fwd over an fp8 cache: k_cache / v_cache torch.float8_e4m3fn, the keys
     and values being k_cache * k_scale and v_cache * v_scale; returns ``out``."""
-    lib = load()
+    lib = _lib or load()  # the lock only until the library is loaded
     ds = [_ref(x) for x in (q, k_cache, v_cache, seq_lens, o_weight, out)]
     _check("decode_attn_fwd_fp8", lib.decode_attn_fwd_fp8(*ds, float(scale), float(k_scale),
                                                           float(v_scale), _stream(stream)))
@@ -190,7 +197,7 @@ def decode_attn_fwd_fp8(q, k_cache, v_cache, seq_lens, o_weight, out, scale: flo
 def decode_attn_only_fp8(q, k_cache, v_cache, seq_lens, attn_out, scale: float, k_scale: float, v_scale: float,
                          stream=None) -> torch.Tensor:
     """decode_attn_only over an fp8 cache (see decode_attn_fwd_fp8); returns ``attn_out``."""
-    lib = load()
+    lib = _lib or load()  # the lock only until the library is loaded
     ds = [_ref(x) for x in (q, k_cache, v_cache, seq_lens, attn_out)]
     _check("decode_attn_only_fp8", lib.decode_attn_only_fp8(*ds, float(scale), float(k_scale),
                                                             float(v_scale), _stream(stream)))
@@ -199,7 +206,7 @@ def decode_attn_only_fp8(q, k_cache, v_cache, seq_lens, attn_out, scale: float, 
 
 def decode_attn_scores(q, k_cache, seq_lens, scores, stream=None) -> torch.Tensor:
     """scores[B, Hq, Lcap] (fp32) = q K^T for t < seq_lens[b]; returns ``scores``."""
-    lib = load()
+    lib = _lib or load()  # the lock only until the library is loaded
     ds = [_ref(x) for x in (q, k_cache, seq_lens, scores)]
     _check("decode_attn_scores", lib.decode_attn_scores(*ds, _stream(stream)))
     return scores
@@ -207,7 +214,7 @@ def decode_attn_scores(q, k_cache, seq_lens, scores, stream=None) -> torch.Tenso
 
 def decode_attn_oproj(attn_flat, o_weight, out, stream=None) -> torch.Tensor:
     """out[B, N] = attn_flat[B, K] . o_weight[K, N] (bf16); returns ``out``."""
-    lib = load()
+    lib = _lib or load()  # the lock only until the library is loaded
     ds = [_ref(x) for x in (attn_flat, o_weight, out)]
     _check("decode_attn_oproj", lib.decode_attn_oproj(*ds, _stream(stream)))
     return out
