@@ -139,6 +139,7 @@ TRIGGER_CASES = [
     W("b1_l2k", 1, 32, 8, 2048, 512, (2048,)),
     W("trig_ragged", 3, 8, 2, 300, 256, (300, 1, 129)),
     W("trig_zero_len", 3, 8, 2, 130, 256, (0, 130, 65)),
+    W("trig_b8_equal_clusters", 8, 32, 8, 1024, 512, (1024,) * 8),  # clusters of two, idle CTAs
 ]
 
 
