@@ -475,11 +475,12 @@ UmmaPlan plan_umma(int B, int K, int N, const Options& o) {
   int ks = (int)o.oproj_splitk;
   // two CTAs per SM, at most eight slices (a cluster): batch 8 step 53.0 -> 51.0 us against one
   // per SM; the long-context workloads within 1 % either way
-  // With K > 4096 (more than 64 k-blocks) four slices measured faster (head dim 256, K = 8192:
-  // step 100.5 -> 97.2 us).
+  // With K > 4096 (more than 64 k-blocks) at most six (head dim 256, K = 8192, batch 8,
+  // interleaved A/B: 8 slices 96.1 us, 6 93.8, 4 94.7, 2 103.4; batch 64 takes 4 from the
+  // grid rule above: 604.7 us against 609.4 at 8 and 614.4 at 6).
   if (ks <= 0) {
     ks = std::min(kMaxClusterSplit, std::max(1, 2 * sms / std::max(1, mtiles * bchunks)));
-    if (nkb > 64) ks = std::min(ks, 4);
+    if (nkb > 64) ks = std::min(ks, 6);
   }
   pl.ksplit = std::max(1, std::min(ks, nkb));
   // up to eight slices reduce in a cluster; more (on request) through global partials

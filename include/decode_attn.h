@@ -235,7 +235,7 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *                   at most 512)
  *   "oproj_path"    0 auto, 1 CUDA-core GEMV, 2 tcgen05 tensor-core GEMM
  *   "oproj_splitk"  split-K factor of the projection (0: auto, two CTAs per SM, at
- *                   most 8)
+ *                   most 8, at most 6 when K > 4096)
  *   "attn_cluster"  1 (default): where there is room for two or more CTAs per
  *                   (batch, KV head) sequence, the attention kernel is launched in
  *                   thread-block clusters of up to 8 CTAs (decode_attn_fwd: only
