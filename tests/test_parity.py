@@ -49,6 +49,10 @@ CASES = [
     W("tile_plus_one", 1, 8, 2, 65, 256, (65,)),
     W("many_batches", 40, 8, 1, 70, 128, tuple(int(x) for x in np.random.default_rng(3).integers(0, 71, 40))),
     W("b9_gemv_chunks", 9, 8, 2, 96, 256, (96, 1, 2, 3, 64, 65, 95, 33, 17)),
+    # batch 1 and 2 with the full hidden size (the projection's full 32 x 8 grid)
+    W("b1_hidden4096", 1, 32, 8, 2048, 4096, (2048,)),
+    W("b1_hidden4096_short", 1, 32, 8, 2048, 4096, (777,)),
+    W("b2_hidden4096", 2, 32, 8, 2048, 4096, (2048, 1000)),
 ]
 
 
