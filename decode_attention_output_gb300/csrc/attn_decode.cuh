@@ -18,11 +18,20 @@
 //    CTA emits one partial (m, l, O) per sequence it touches; the CTA that finishes a
 //    sequence last (an atomic completion counter, no waiting) merges the partials with
 //    the log-sum-exp rule and writes bf16.
-//  * One producer lane streams K and V tiles with one 5-D TMA copy per tile and tensor
-//    (the head dim split into 128-byte rows of 64-dim boxes, 128-byte swizzle) into a
-//    4-stage shared-memory ring guarded by mbarriers; q rows arrive by 1-D bulk copy
-//    with a sequence's first tiles. A paged cache is read in boxes of
-//    min(block size, tile) tokens, the block ids arriving by TMA a few tiles ahead.
+//  * Two producer lanes, one per consumer group (tiles of alternating parity), stream K
+//    and V tiles with one 5-D TMA copy per tile and tensor (the head dim split into
+//    128-byte rows of 64-dim boxes, 128-byte swizzle) into a 4-stage shared-memory ring
+//    guarded by mbarriers; q rows arrive by 1-D bulk copy with a sequence's first tiles.
+//    A paged cache is read in boxes of min(block size, tile) tokens, the block ids
+//    arriving by TMA a few tiles ahead.
+//  * Cluster mode (where there is room for two or more CTAs per sequence): the grid is
+//    launched in thread-block clusters. With equal lengths every sequence gets the CTAs
+//    of one cluster, which merge their partial states through distributed shared memory
+//    after a cluster barrier instead of through L2; with unequal lengths the kernel keeps
+//    the flat split and the L2 merge, and no CTA waits at a cluster barrier.
+//  * Programmatic dependent launch: the kernel waits for the previous kernel in the
+//    stream before its first global access, and lets the next one launch right after its
+//    set-up, or, when the projection follows, a few tiles before the end of its range.
 //  * Two consumer groups of four warps take alternate stages, so two tiles are
 //    in compute at once per SM. Each warp owns 16 tokens of a stage and all G
 //    query heads of the group (every K/V byte is read once). S^T = K . Q^T runs
