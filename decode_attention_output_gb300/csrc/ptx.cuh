@@ -1,6 +1,8 @@
 // ptx.cuh -- thin inline-PTX wrappers used by the sm_103a kernels: mbarrier,
-// TMA (tensor and 1-D bulk copies), ldmatrix / movmatrix / mma.sync, PDL,
-// and bounded waits that record an error code instead of spinning forever.
+// TMA (tensor and 1-D bulk copies, L2 prefetch, cache policies), ldmatrix /
+// movmatrix / mma.sync, tcgen05 (TMEM allocation, MMA, commit, loads), thread-block
+// cluster barriers and distributed shared-memory loads, PDL, and bounded waits that
+// record an error code instead of spinning forever.
 #pragma once
 
 #include <cuda.h>
