@@ -26,8 +26,9 @@ struct Options {
   int64_t gemm_min_batch = 1;  // tcgen05 from batch 1 (with the cluster reduction: batch 1 step
                                // 18.9 -> 16.4 us against the CUDA-core GEMV)
   int64_t pdl = 1;
-  int64_t l2_prefetch = 0;  // fused step: the attention kernel pulls W_o into L2 (measured slower: off)
-  int64_t attn_stages = 4;  // attention pipeline depth, 4 or 6 (6 measured slower)
+  int64_t l2_prefetch = 0;  // decode_attn_fwd: the attention kernel pulls W_o into L2 while it
+                            // streams K/V (measured slower: off)
+  int64_t attn_stages = 4;  // attention pipeline depth, 4 or 6 (6 no faster with two producers)
   int64_t fused = 0;        // decode_attn_fwd as one persistent launch (measured slower so far: off)
   int64_t fused_attn_ctas = 0;  // attention workers of the fused step (0: about 4 tiles each)
   int64_t oproj_cluster = 1;    // tcgen05 projection: split-K slices reduce in a cluster
