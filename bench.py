@@ -4,10 +4,14 @@
 
 A step is one decode_attn_fwd call (the split-KV attention kernel, then the
 projection kernel) over one batch of synthetic inputs resident in HBM. The
-default workload is b8_h32x8_l8k (batch 8, 32 query / 8 KV heads, kv_len
-8192, hidden 4096). Consecutive steps read different copies of the inputs
-(rotated sets, more than twice the L2 between reuses), so no step hits data a
-previous step left in L2. Rank 0 prints one JSON line.
+headline workload is b64_h64x8_l16k (batch 64, 64 query / 8 KV heads, kv_len
+16384, hidden 8192: the largest of the workloads on one GPU). In the same run
+every other workload of the table is timed the same way and reported under
+config.per_workload (step time eager and as CUDA-graph replay, GB/s, fractions
+of the measured copy peak and of 8 TB/s, the attention kernel alone).
+Consecutive steps read different copies of the inputs (rotated sets, more than
+twice the L2 between reuses), so no step hits data a previous step left in L2.
+Rank 0 prints one JSON line.
 
 --impl reference times the fp64 CPU oracle on the host cores instead (a bounded
 sample of the same workload per step); it is the reference arm of this method.
@@ -32,8 +36,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode attn+o_proj µs/step and achieved HBM GB/s (% of GB300 peak), 1 GPU"
-DEFAULT_WORKLOAD = "b8_h32x8_l8k"
+DEFAULT_WORKLOAD = "b64_h64x8_l16k"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # the roofline denominator the workload targets are stated against
 KERNEL_SOURCES = ["attn_decode.cuh", "attn_decode.cu", "ptx.cuh", "kernels.h"]
 
 
@@ -48,6 +53,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true", help="time the chosen workload only")
     return ap.parse_args()
 
 
@@ -304,6 +310,125 @@ def run_reference(args, world, rank):
 
 
 # -------------------------------------------------------------------- our arm
+def make_sets(synth, w, seed, dev, l2):
+    """Input sets of workload ``w`` on ``dev``: enough copies that each is re-read only
+    after more than twice the L2 of other traffic (at least two)."""
+    base = synth.make_inputs(w, seed=seed, device=dev)
+    lens = base["seq_lens"]
+    nb = synth.algorithmic_bytes(w, lens.cpu())
+    set_bytes = sum(base[k].numel() * base[k].element_size() for k in ("q", "k_cache", "v_cache", "o_weight"))
+    n_sets = max(2, math.ceil(2.5 * l2 / max(1, nb["total"])))
+    sets = [base] + [synth.make_inputs(w, seed=seed + i, device=dev) for i in range(1, n_sets)]
+    for s in sets:
+        s["seq_lens"] = lens  # same lengths for every set (a ragged draw is per seed)
+    return sets, nb, set_bytes
+
+
+def time_workload(da, w, sets, nb, steps, warmup, dev, stream):
+    """Times one workload on resident inputs. Returns eager step time (K steps between one
+    event pair), CUDA-graph replay of the same steps, and the attention kernel alone (eager
+    per-launch events, and K launches replayed from a graph between one event pair)."""
+    import torch
+
+    n_sets = len(sets)
+    outs = [torch.empty((w.B, w.N), dtype=torch.bfloat16, device=dev) for _ in range(n_sets)]
+    attn_bufs = [torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev) for _ in range(n_sets)]
+
+    def step(i, st):
+        fwd_call(da, sets[i % n_sets], outs[i % n_sets], stream=st)
+
+    for i in range(max(3, warmup)):
+        step(i, stream)
+    torch.cuda.synchronize(dev)
+    if da.decode_attn_last_device_error(stream) != 0:
+        raise RuntimeError(f"{w.name}: device error during warm-up")
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    ev0.record(stream)
+    for i in range(steps):
+        step(i, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.perf_counter()
+    step_ms = ev0.elapsed_time(ev1) / steps
+
+    # the dominant kernel (split-KV attention) alone, per launch, same inputs and plan
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        evs[i][0].record(stream)
+        only_call(da, sets[i % n_sets], attn_bufs[i % n_sets], stream=stream)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    attn_ms_eager = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    attn_ms = attn_ms_eager
+    try:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        ga = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ga, stream=cap):
+            for i in range(steps):
+                only_call(da, sets[i % n_sets], attn_bufs[i % n_sets], stream=cap)
+        ga.replay()
+        torch.cuda.synchronize(dev)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        ga.replay()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        attn_ms = a0.elapsed_time(a1) / steps
+        del ga
+    except RuntimeError:
+        pass
+
+    # CUDA-graph replay of whole steps (no host launch gaps)
+    graph_us = None
+    try:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(n_sets):
+                step(i, cap)
+        torch.cuda.synchronize(dev)
+        reps = max(1, steps // n_sets)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        g0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        graph_us = g0.elapsed_time(g1) * 1e3 / (reps * n_sets)
+        del graph
+    except RuntimeError as e:  # capture unsupported on this setup: report why
+        graph_us = f"unavailable: {e}"[:200]
+    if da.decode_attn_last_device_error(stream) != 0:
+        raise RuntimeError(f"{w.name}: device error during the timed runs")
+    attn_bytes = nb["kv"] + w.B * w.Hq * w.D * 2 * 2  # K+V of valid tokens + q in + attention out
+    return {"step_ms": step_ms, "graph_us": graph_us, "attn_ms": attn_ms, "attn_ms_eager": attn_ms_eager,
+            "attn_bytes": attn_bytes, "window": (t_wall0, t_wall1), "outs": outs, "step": step}
+
+
+def workload_entry(w, nb, t, peak, clocks, n_sets):
+    """One line of config.per_workload: step time, bandwidth and fractions of the measured
+    copy peak and of 8 TB/s, and the attention kernel alone."""
+    gbs = nb["total"] / (t["step_ms"] * 1e-3) / 1e9
+    attn_gbs = t["attn_bytes"] / (t["attn_ms"] * 1e-3) / 1e9
+    g = t["graph_us"]
+    return {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "kv_len": w.Lcap, "hidden": w.N, "head_dim": w.D,
+            "kv_cache": w.kv, "lens": w.lens, "bytes_per_step": nb["total"],
+            "us_per_step": t["step_ms"] * 1e3, "graph_us_per_step": g, "GBps": gbs,
+            "frac_of_measured_peak": gbs / peak, "frac_of_8TBps": gbs / NOMINAL_HBM_GBS,
+            "graph_GBps": nb["total"] / (g * 1e-6) / 1e9 if isinstance(g, float) else None,
+            "attn_us_per_launch": t["attn_ms"] * 1e3, "attn_us_per_launch_eager": t["attn_ms_eager"] * 1e3,
+            "attn_bytes": t["attn_bytes"], "attn_GBps": attn_gbs, "attn_frac_of_measured_peak": attn_gbs / peak,
+            "input_sets": n_sets, "clocks": clocks}
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -317,26 +442,8 @@ def run_ours(args, world, rank, local):
     w = synth.WORKLOADS[args.workload]
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
-
-    base = synth.make_inputs(w, seed=args.seed + 1000 * rank, device=dev)
-    lens = base["seq_lens"]
-    nb = synth.algorithmic_bytes(w, lens.cpu())
-    set_bytes = sum(base[k].numel() * base[k].element_size() for k in ("q", "k_cache", "v_cache", "o_weight"))
-    n_sets = max(2, math.ceil(2.5 * l2 / max(1, nb["total"])))
-    sets = [base] + [synth.make_inputs(w, seed=args.seed + 1000 * rank + i, device=dev) for i in range(1, n_sets)]
-    for s in sets:
-        s["seq_lens"] = lens  # same lengths for every set (ragged draw is per seed)
-    outs = [torch.empty((w.B, w.N), dtype=torch.bfloat16, device=dev) for _ in range(n_sets)]
     stream = torch.cuda.current_stream(dev)
-
-    def step(i, st=None):
-        s = sets[i % n_sets]
-        fwd_call(da, s, outs[i % n_sets], stream=st if st is not None else stream)
-
-    for i in range(max(3, args.warmup)):
-        step(i)
-    torch.cuda.synchronize(dev)
-    assert da.decode_attn_device_error(stream) == 0
+    peak, peak_src = measured_hbm_peak()
 
     uuid = str(getattr(props, "uuid", "")) or None
     if uuid and not uuid.startswith("GPU-"):
@@ -345,95 +452,33 @@ def run_ours(args, world, rank, local):
     sampler.start()
     time.sleep(0.05)
 
-    # ---- timed region: exactly K steps
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    t_wall0 = time.perf_counter()
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    t_wall1 = time.perf_counter()
-    barrier(world)
-    step_ms = ev0.elapsed_time(ev1) / args.steps
-    sampler_window = (t_wall0, t_wall1)
+    seed = args.seed + 1000 * rank
+    sets, nb, set_bytes = make_sets(synth, w, seed, dev, l2)
+    base = sets[0]
+    lens = base["seq_lens"]
+    n_sets = len(sets)
 
-    # ---- dominant kernel (split-KV attention) timed alone, per launch, same inputs and plan
-    attn_bufs = [torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev) for _ in range(n_sets)]
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        s = sets[i % n_sets]
-        evs[i][0].record(stream)
-        only_call(da, s, attn_bufs[i % n_sets], stream=stream)
-        evs[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    attn_ms_eager = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    # the same launches replayed from a CUDA graph (no host launch gaps), K of them
-    # bracketed by one event pair: average launch duration = elapsed / K
-    attn_ms = attn_ms_eager
-    try:
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        ga = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(ga, stream=cap):
-            for i in range(args.steps):
-                s = sets[i % n_sets]
-                only_call(da, s, attn_bufs[i % n_sets], stream=cap)
-        ga.replay()
-        torch.cuda.synchronize(dev)
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        ga.replay()
-        a1.record(stream)
-        torch.cuda.synchronize(dev)
-        attn_ms = a0.elapsed_time(a1) / args.steps
-        del ga
-    except RuntimeError:
-        pass
-    sampler.stop()
-    assert da.decode_attn_device_error(stream) == 0
+    # ---- timed region: exactly K steps (inside time_workload), barriers on both sides
+    barrier(world)
+    t = time_workload(da, w, sets, nb, args.steps, args.warmup, dev, stream)
+    barrier(world)
+    step_ms = t["step_ms"]
+    clocks = sampler.summary(*t["window"])
 
-    # ---- host cost of one eager call (enqueue only) and CUDA-graph replay of the same steps
+    # ---- host cost of one eager call (enqueue only)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     n_host = min(args.steps, 50)
     for i in range(n_host):
-        step(i)
+        t["step"](i, stream)
     host_us = (time.perf_counter() - t0) / n_host * 1e6
     torch.cuda.synchronize(dev)
-    graph_us = None
-    try:
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=cap):
-            for i in range(n_sets):
-                step(i, cap)
-        torch.cuda.synchronize(dev)
-        reps = max(1, args.steps // n_sets)
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        graph.replay()
-        torch.cuda.synchronize(dev)
-        g0.record(stream)
-        for _ in range(reps):
-            graph.replay()
-        g1.record(stream)
-        torch.cuda.synchronize(dev)
-        graph_us = g0.elapsed_time(g1) * 1e3 / (reps * n_sets)
-        del graph
-    except RuntimeError as e:  # capture unsupported on this setup: report why
-        graph_us = f"unavailable: {e}"[:200]
-    assert da.decode_attn_device_error(stream) == 0
+    assert da.decode_attn_last_device_error(stream) == 0
 
     step_ms_max = max_over_ranks(world, step_ms)
     total_bytes = sum_over_ranks(world, float(nb["total"]))
     value = total_bytes / (step_ms_max * 1e-3) / 1e9
-    peak, peak_src = measured_hbm_peak()
-    attn_bytes = nb["kv"] + w.B * w.Hq * w.D * 2 * 2  # K+V of valid tokens + q in + attention out
-    achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
+    achieved = t["attn_bytes"] / (t["attn_ms"] * 1e-3) / 1e9
     traffic = recorded_traffic(w.name)
 
     # ---- end to end through the C ABI from pinned host buffers
@@ -441,16 +486,17 @@ def run_ours(args, world, rank, local):
     if not args.no_e2e:
         host = {k: base[k].cpu().pin_memory() for k in ("q", "k_cache", "v_cache", "o_weight", "seq_lens")}
         dbuf = {k: torch.empty_like(base[k]) for k in host}
+        out_d = t["outs"][0]
         out_h = torch.empty((w.B, w.N), dtype=torch.bfloat16).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        h2d = sum(x.numel() * x.element_size() for x in host.values())
         d2h = out_h.numel() * out_h.element_size()
         n_e2e = max(3, min(args.steps, 20))
 
         def e2e_step():
             for k in host:
                 dbuf[k].copy_(host[k], non_blocking=True)
-            fwd_call(da, {**base, **dbuf}, outs[0], stream=stream)
-            out_h.copy_(outs[0], non_blocking=True)
+            fwd_call(da, {**base, **dbuf}, out_d, stream=stream)
+            out_h.copy_(out_d, non_blocking=True)
             torch.cuda.current_stream(dev).synchronize()
 
         e2e_step()
@@ -462,29 +508,55 @@ def run_ours(args, world, rank, local):
         e2e = {"value": total_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "us_per_step": e2e_s * 1e6, "steps": n_e2e,
                "note": "all inputs (q, K/V caches, W_o, seq_lens) copied host->device every step"}
+        del host, dbuf
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         x_host = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in base.items()}
         cpu = oracle_baseline(x_host, w, rows=[0], budget_s=args.cpu_seconds)
+        del x_host
+
+    head_entry = workload_entry(w, nb, t, peak, clocks, n_sets)
+    del sets, base, t
+    torch.cuda.empty_cache()
+
+    # ---- every other workload, timed the same way in the same run
+    per_workload = {}
+    names = [] if args.no_per_workload else [n for n in synth.ORDER if n != w.name]
+    for name in synth.ORDER:
+        if name == w.name:
+            per_workload[name] = head_entry
+            continue
+        if name not in names:
+            continue
+        wk = synth.WORKLOADS[name]
+        s2, nb2, _ = make_sets(synth, wk, seed, dev, l2)
+        t2 = time_workload(da, wk, s2, nb2, args.steps, args.warmup, dev, stream)
+        per_workload[name] = workload_entry(wk, nb2, t2, peak, sampler.summary(*t2["window"]), len(s2))
+        del s2, t2
+        torch.cuda.empty_cache()
+    sampler.stop()
 
     if rank == 0:
-        clocks = sampler.summary(*sampler_window)
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms_max, "us_per_step": step_ms_max * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.kv == "bf16" else "e4m3 cache, f16 MMA",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.kv == "bf16" else "e4m3 cache, f16 MMA",
             "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "kv_len": w.Lcap, "hidden": w.N,
                        "head_dim": w.D, "kv_cache": w.kv,
                        "seq_lens_sum": int(lens.sum().item()), "bytes_per_step": nb,
                        "l2": f"{n_sets} rotated input sets of {set_bytes / 1e6:.0f} MB (>2x L2 between reuses)",
-                       "step_hbm_frac": value / world / peak, "parallelism": f"replicas x{world}",
-                       "graph_us_per_step": graph_us, "host_us_per_call": host_us},
+                       "step_hbm_frac": value / world / peak, "step_frac_of_8TBps": value / world / NOMINAL_HBM_GBS,
+                       "parallelism": f"replicas x{world}",
+                       "graph_us_per_step": head_entry["graph_us_per_step"], "host_us_per_call": host_us,
+                       "per_workload": per_workload},
             "roofline": {"bound": "hbm", "kernel": "attn_decode_kernel", "achieved": achieved, "peak": peak,
                          "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": traffic, "algorithmic_bytes_per_launch": attn_bytes,
-                         "us_per_launch": attn_ms * 1e3, "us_per_launch_eager": attn_ms_eager * 1e3,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": head_entry["attn_bytes"],
+                         "us_per_launch": head_entry["attn_us_per_launch"],
+                         "us_per_launch_eager": head_entry["attn_us_per_launch_eager"],
                          "timing": "graph of K launches between two events (eager per-launch events beside it)"},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks,
         }

@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     decode_attn_fwd_fp8,
     decode_attn_fwd_paged,
     decode_attn_get_option,
+    decode_attn_last_device_error,
     decode_attn_only,
     decode_attn_only_fp8,
     decode_attn_only_noalloc,

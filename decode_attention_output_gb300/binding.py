@@ -24,7 +24,7 @@ _DTYPES = {torch.bfloat16: DA_DTYPE_BF16, torch.float32: DA_DTYPE_F32, torch.int
 
 # every symbol declared in include/decode_attn.h
 EXPORTS = ("decode_attn_fwd", "decode_attn_only", "decode_attn_only_noalloc", "decode_attn_fwd_paged",
-           "decode_attn_only_paged", "decode_attn_fwd_fp8", "decode_attn_only_fp8", "decode_attn_scores", "decode_attn_oproj", "decode_attn_set_option", "decode_attn_get_option", "decode_attn_device_error",
+           "decode_attn_only_paged", "decode_attn_fwd_fp8", "decode_attn_only_fp8", "decode_attn_scores", "decode_attn_oproj", "decode_attn_set_option", "decode_attn_get_option", "decode_attn_last_device_error", "decode_attn_device_error",
            "decode_attn_release", "decode_attn_status_str")
 
 
@@ -65,6 +65,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             lib.decode_attn_oproj.argtypes = [P, P, P, vp]
             lib.decode_attn_set_option.argtypes = [ctypes.c_char_p, i64]
             lib.decode_attn_get_option.argtypes = [ctypes.c_char_p, ctypes.POINTER(i64)]
+            lib.decode_attn_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
             lib.decode_attn_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
             lib.decode_attn_release.argtypes = []
             lib.decode_attn_release.restype = None
@@ -230,8 +231,18 @@ def decode_attn_get_option(key: str) -> int:
     return int(v.value)
 
 
+def decode_attn_last_device_error(stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device error word (the
+    workspace's and the no-allocation scratch's, OR-ed); a non-zero word also resets
+    the completion counters beside it."""
+    code = ctypes.c_int32(0)
+    _check("decode_attn_last_device_error",
+           load().decode_attn_last_device_error(_stream(stream), ctypes.byref(code)))
+    return int(code.value)
+
+
 def decode_attn_device_error(stream=None) -> int:
-    """Synchronises the stream; returns (and clears) the device error word."""
+    """decode_attn_last_device_error under its earlier name."""
     code = ctypes.c_int32(0)
     _check("decode_attn_device_error", load().decode_attn_device_error(_stream(stream), ctypes.byref(code)))
     return int(code.value)

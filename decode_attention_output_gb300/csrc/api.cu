@@ -40,6 +40,8 @@ struct Options {
   int64_t attn_trigger = 3;     // decode_attn_fwd: each attention CTA lets the projection launch
                                 // this many tiles before its end (0: at set-up); 3 against 0:
                                 // batch 1 15.9 -> 14.9 us, 131k context 306.2 -> 303.5 us
+  int64_t grid_wait_us = 0;     // test hook: the fused step's grid-barrier wait limit (0: 2 s)
+  int64_t grid_wait_extra = 0;  // test hook: arrivals that barrier waits for beyond the grid
 };
 std::mutex g_mu;
 Options g_opt;
@@ -72,7 +74,10 @@ Workspace g_ws[kMaxDevices];
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Returns the workspace of the current device with at least `scratch` bytes after
-// the header, growing it if needed (growth synchronises the device).
+// the header, growing it if needed. Growth is stream-ordered on `stream` (no device-wide
+// synchronisation): the old block is released with cudaFreeAsync behind the work already
+// queued on `stream`, the new one comes from cudaMallocAsync and its header is zeroed by
+// cudaMemsetAsync, all on `stream`.
 int workspace_get(size_t scratch, cudaStream_t stream, char** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DA_ERR_CUDA;
@@ -81,19 +86,18 @@ int workspace_get(size_t scratch, cudaStream_t stream, char** out) {
   const size_t need = kHeaderBytes + align_up(scratch, 256);
   if (need > ws.bytes) {
     if (ws.base) {
-      if (cudaDeviceSynchronize() != cudaSuccess) return DA_ERR_CUDA;
-      cudaFree(ws.base);
+      if (cudaFreeAsync(ws.base, stream) != cudaSuccess) return DA_ERR_CUDA;
       ws.base = nullptr;
       ws.bytes = 0;
     }
     const size_t bytes = std::max(need, (size_t)32 << 20);
     void* p = nullptr;
-    if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) {
       cudaGetLastError();
       return DA_ERR_NOMEM;
     }
     if (cudaMemsetAsync(p, 0, kHeaderBytes, stream) != cudaSuccess) {
-      cudaFree(p);
+      cudaFreeAsync(p, stream);
       return DA_ERR_CUDA;
     }
     ws.base = static_cast<char*>(p);
@@ -599,6 +603,9 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
     p.proj_part = fused->part;
     p.proj_counters = reinterpret_cast<int*>(ws + kGemvCntOff);
     p.grid_sync = reinterpret_cast<int*>(ws + kGridSyncOff);
+    const Options o = options_snapshot();
+    p.sync_limit_ns = (unsigned long long)o.grid_wait_us * 1000ull;  // 0: the kernels' default
+    p.sync_extra = (int)o.grid_wait_extra;
     p.N = fused->N;
     p.K = fused->K;
     p.kb_per_tile = fused->plan->kb_per_tile;
@@ -770,6 +777,8 @@ int decode_attn_set_option(const char* key, int64_t value) {
   else if (!strcmp(key, "attn_cluster") && (value == 0 || value == 1)) g_opt.attn_cluster = value;
   else if (!strcmp(key, "attn_pdl") && (value == 0 || value == 1)) g_opt.attn_pdl = value;
   else if (!strcmp(key, "attn_trigger") && value >= 0 && value <= (1 << 20)) g_opt.attn_trigger = value;
+  else if (!strcmp(key, "grid_wait_us") && value >= 0 && value <= 2000000) g_opt.grid_wait_us = value;
+  else if (!strcmp(key, "grid_wait_extra") && (value == 0 || value == 1)) g_opt.grid_wait_extra = value;
   else return DA_ERR_OPTION;
   return DA_OK;
 }
@@ -791,6 +800,8 @@ int decode_attn_get_option(const char* key, int64_t* value) {
   else if (!strcmp(key, "attn_cluster")) *value = g_opt.attn_cluster;
   else if (!strcmp(key, "attn_pdl")) *value = g_opt.attn_pdl;
   else if (!strcmp(key, "attn_trigger")) *value = g_opt.attn_trigger;
+  else if (!strcmp(key, "grid_wait_us")) *value = g_opt.grid_wait_us;
+  else if (!strcmp(key, "grid_wait_extra")) *value = g_opt.grid_wait_extra;
   else return DA_ERR_OPTION;
   return DA_OK;
 }
@@ -943,7 +954,7 @@ int decode_attn_fwd_paged(const da_tensor_t* q, const da_tensor_t* k_pages, cons
   return fwd_checked(q, k_pages, v_pages, seq_lens, o_weight, out, scale, stream, s, &ps);
 }
 
-int decode_attn_device_error(void* stream, int32_t* host_code) {
+int decode_attn_last_device_error(void* stream, int32_t* host_code) {
   if (!host_code) return DA_ERR_NULL;
   *host_code = 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -955,12 +966,28 @@ int decode_attn_device_error(void* stream, int32_t* host_code) {
     std::lock_guard<std::mutex> lk(g_mu);
     base = g_ws[dev].base;
   }
-  if (!base) return DA_OK;
+  char* fixed = nullptr;  // the no-allocation scratch, once a call has looked it up here
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    fixed = static_cast<char*>(g_noalloc_addr[dev]);
+  }
   int32_t code = 0;
-  if (cudaMemcpy(&code, base + kErrOff, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) return DA_ERR_CUDA;
-  if (code && cudaMemset(base + kErrOff, 0, sizeof(code)) != cudaSuccess) return DA_ERR_CUDA;
+  for (char* b : {base, fixed}) {
+    if (!b) continue;
+    int32_t c = 0;
+    if (cudaMemcpy(&c, b + kErrOff, sizeof(c), cudaMemcpyDeviceToHost) != cudaSuccess) return DA_ERR_CUDA;
+    // A CTA that gave up waiting left its completion counter (and, in the fused step, the
+    // grid barrier) short of the count that resets it: clear the whole header, or the next
+    // call would see stale counts.
+    if (c && cudaMemset(b, 0, kHeaderBytes) != cudaSuccess) return DA_ERR_CUDA;
+    code |= c;
+  }
   *host_code = code;
   return DA_OK;
+}
+
+int decode_attn_device_error(void* stream, int32_t* host_code) {
+  return decode_attn_last_device_error(stream, host_code);
 }
 
 void decode_attn_release(void) {

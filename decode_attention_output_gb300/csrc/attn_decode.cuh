@@ -128,14 +128,16 @@ __device__ __forceinline__ ProjSplit proj_split(const AttnParams& p, int cta) {
   return r;
 }
 
-// Waits until every CTA of the grid has arrived (bounded), then counts this CTA's
-// departure; the last one to leave resets both counters for the next launch.
-__device__ __forceinline__ bool grid_barrier_wait(int* sync, int n, int* err, volatile int* abort_flag) {
+// Waits until n CTAs have arrived (bounded), then counts this CTA's departure; the
+// last one to leave resets both counters for the next launch. A CTA that gives up
+// records kErrGridSync and carries on without counting its departure (the host's error
+// query then resets the counters): the rest of its pipeline is intact, so every later
+// wait of the kernel still ends, and only the result is invalid.
+__device__ __forceinline__ bool grid_barrier_wait(int* sync, int n, int* err, unsigned long long limit_ns) {
   const unsigned long long t0 = globaltimer_ns();
   while (ld_acquire_gpu(sync) < n) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(err, kErrGridSync);
-      *abort_flag = 1;
       return false;
     }
     __nanosleep(64);
@@ -181,7 +183,8 @@ __device__ void fused_producer(const AttnParams& p, uint32_t ring, uint64_t* bar
     tma_load_2d(dst, &p.tm_w, full_b(j), tile * 128, kb * 64);
     tma_load_2d(dst + 8192, &p.tm_w, full_b(j), tile * 128 + 64, kb * 64);
   }
-  grid_barrier_wait(p.grid_sync, gridDim.x, p.err, flags);
+  grid_barrier_wait(p.grid_sync, (int)gridDim.x + p.sync_extra, p.err,
+                    p.sync_limit_ns ? p.sync_limit_ns : kWaitLimitNs);
   fence_proxy_async_global();  // X was written by other CTAs' generic stores; TMA reads it
   for (int j = 0; j < pre; ++j) {
     const int unit = (int)ps.u0 + j, tile = unit / p.kb_per_tile, kb = unit - tile * p.kb_per_tile;

@@ -137,6 +137,9 @@ struct AttnParams {
   float* proj_part;      // [slots][B][128] fp32 split-K partials
   int* proj_counters;    // [column tiles], zero between calls
   int* grid_sync;        // [2]: arrivals, departures of the grid barrier, zero between calls
+  unsigned long long sync_limit_ns;  // the grid barrier's wait limit (0: two seconds)
+  int sync_extra;        // arrivals the grid barrier waits for beyond the grid (0; a test sets 1
+                         // to make the wait run out)
   int N, K, kb_per_tile, units;  // units = column tiles x k-blocks of 64
   int attn_workers;      // CTAs that take attention tiles (<= grid); the fused step may leave
                          // some CTAs free to start on W_o at once

@@ -34,14 +34,18 @@
  *    A failed launch returns DA_ERR_CUDA.
  *  - The library owns one workspace per device (partial results of the split
  *    KV pass and of the split-K projection, completion counters, the bf16
- *    attention intermediate). It is grown with cudaMalloc when a call needs
- *    more, so the first call with the largest shapes should precede any CUDA
- *    graph capture. Calls that run concurrently on different streams of the
- *    same device share it and must not overlap.
+ *    attention intermediate). When a call needs more, it is grown in stream
+ *    order on that call's stream (cudaFreeAsync of the old block, cudaMallocAsync
+ *    of the new one, cudaMemsetAsync of its header; no device-wide
+ *    synchronisation), so the first call with the largest shapes should precede
+ *    any CUDA graph capture. Calls on different streams of the same device share
+ *    it: the caller must order them (their work must not overlap on the GPU).
  *  - seq_lens lives on the device. Each length is clamped to [0, Lcap] on the
  *    device; a length of 0 gives an all-zero attention row.
  *  - Bounded device waits: every wait inside a kernel gives up after about
- *    two seconds and records a code that decode_attn_device_error() returns.
+ *    two seconds, records a code that decode_attn_last_device_error() returns,
+ *    and the kernel then finishes without waiting further (its output is not
+ *    valid).
  */
 #ifndef DECODE_ATTN_H
 #define DECODE_ATTN_H
@@ -121,11 +125,12 @@ int decode_attn_only(const da_tensor_t* q, const da_tensor_t* k_cache, const da_
 /*
  * decode_attn_only_noalloc -- decode_attn_only for callers that must not allocate
  * device memory at run time: for example a serving process whose GPU memory is
- * reserved up front by its own allocator or memory pool, or a request path that
- * may not take the device-wide synchronisation that growing (freeing and
- * re-allocating) the library workspace implies. The pages have no counterpart;
- * this is a deployment convenience, with the same arguments and the same result
- * as decode_attn_only.
+ * reserved up front by its own allocator or memory pool (an allocation outside
+ * it can fail, or take memory the pool was sized to own), or a request path with
+ * a latency bound, where growing the library workspace (a stream-ordered pool
+ * allocation that may have to map new device memory) is not allowed. The pages
+ * have no counterpart; this is a deployment convenience, with the same arguments
+ * and the same result as decode_attn_only.
  *
  * Scratch: a fixed 8 MiB device array inside the library, held by every GPU that
  * loads it until the process exits. It is never allocated or freed and no
@@ -142,8 +147,9 @@ int decode_attn_only(const da_tensor_t* q, const da_tensor_t* k_cache, const da_
  *   previous call's contents.
  * - All calls share the one array: calls whose work overlaps on the GPU (other
  *   streams, other host threads) race on it and must be serialised by the caller.
- * - Device-side wait timeouts are recorded in the array's own error word;
- *   decode_attn_device_error() does not report them.
+ * - Device-side wait timeouts are recorded in the array's own error word, which
+ *   decode_attn_last_device_error() reads and clears together with the
+ *   workspace's (until the next call of this entry point clears it).
  */
 int decode_attn_only_noalloc(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tensor_t* v_cache,
                              const da_tensor_t* seq_lens, const da_tensor_t* attn_out, float scale,
@@ -173,7 +179,7 @@ int decode_attn_only_noalloc(const da_tensor_t* q, const da_tensor_t* k_cache, c
  * block_size: a power of two from 8 to 2^20; anything else returns DA_ERR_UNSUPPORTED.
  * (Blocks of 32 tokens and more stream at 90-95% of the contiguous rate on GB300; 16
  * at about 75%, 8 at about 55%.) A table entry outside [0, num_blocks) that
- * is read sets bit 64 of the device error word (decode_attn_device_error) and that
+ * is read sets bit 64 of the device error word (decode_attn_last_device_error) and that
  * block reads as zeros. The fused option does not apply: two launches.
  */
 int decode_attn_fwd_paged(const da_tensor_t* q, const da_tensor_t* k_pages, const da_tensor_t* v_pages,
@@ -280,17 +286,32 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *                   pulls the part of its o_weight slice that its ring does not hold
  *                   into L2 before it waits for the attention kernel (measured no
  *                   faster on GB300)
+ *   "grid_wait_us"  test hook: the fused step's grid-barrier wait limit in microseconds
+ *                   (0, the default: two seconds; at most 2000000)
+ *   "grid_wait_extra" test hook, 0 (default) or 1: the fused step's grid barrier waits
+ *                   for this many arrivals beyond the grid, so that with 1 the wait runs
+ *                   out, records error bit 32 and the kernel completes with an invalid
+ *                   result (a failure that touches no bad address and hangs nothing)
  * Returns DA_OK or DA_ERR_OPTION.
  */
 int decode_attn_set_option(const char* key, int64_t value);
 int decode_attn_get_option(const char* key, int64_t* value);
 
 /*
- * decode_attn_device_error -- synchronises `stream`, then reports (in
- * *host_code) and clears the device error word of the current device's
- * workspace: 0 when no kernel recorded an error. Returns DA_OK, or
- * DA_ERR_CUDA when the synchronisation itself failed.
+ * decode_attn_last_device_error -- synchronises `stream`, then reports in
+ * *host_code the device error word of the current device (the bitwise OR of the
+ * workspace's word and the no-allocation scratch's word): 0 when no kernel
+ * recorded an error. Codes (bits): 1 a consumer gave up waiting for a K/V stage,
+ * 2 a producer gave up waiting for a free stage, 4 copies still in flight at
+ * exit, 8 a tensor-core completion never arrived, 32 the fused step's grid
+ * barrier did not complete, 64 a paged cache's block table named a block outside
+ * the pool. A non-zero word is cleared, and with it the completion counters and
+ * grid-barrier words beside it (a CTA that gave up left them short of the count
+ * that resets them), so that the next call starts clean. Returns DA_OK, or
+ * DA_ERR_CUDA when the synchronisation or a copy failed.
  */
+int decode_attn_last_device_error(void* stream, int32_t* host_code);
+/* The same call under its earlier name. */
 int decode_attn_device_error(void* stream, int32_t* host_code);
 
 /* Frees the workspace of every device (synchronises those devices). */

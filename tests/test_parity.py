@@ -27,7 +27,7 @@ def _library():
     da.load()
     torch.cuda.set_device(0)
     yield
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
 
 
 def W(name, B, Hq, Hkv, Lcap, N, lens, k_mult=1.0):
@@ -68,7 +68,7 @@ def _run(w, seed=0, ctas=0):
         torch.cuda.synchronize()
     finally:
         da.decode_attn_set_option("attn_ctas", old)
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
     return x, attn, out
 
 
@@ -378,7 +378,7 @@ def test_oproj_gemm_integer_exact(path, B, K, N):
     with _Path(path):
         da.decode_attn_oproj(xi.to(torch.bfloat16).to(DEV), wi.to(torch.bfloat16).to(DEV), out)
     torch.cuda.synchronize()
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
     assert torch.equal(out.cpu(), ref)
 
 
@@ -441,7 +441,7 @@ def test_fused_step_matches_oracle_and_two_launches(orc, w):
         out2 = torch.full_like(out, float("nan"))
         da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out2, x["scale"])
         torch.cuda.synchronize()
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
     ref_attn, ref_out = oracle_decode(orc, x)
     assert_bf16_close(f64(out), ref_out, f"{w.name} fused output")
     assert_bf16_close(f64(out2), ref_out, f"{w.name} two-launch output")
@@ -463,5 +463,5 @@ def test_fused_step_integer_exact():
         da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], wi.to(torch.bfloat16).to(DEV), out,
                            x["scale"])
     torch.cuda.synchronize()
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
     assert torch.equal(out.cpu(), ref)

@@ -30,7 +30,7 @@ def _library():
     da.load()
     torch.cuda.set_device(0)
     yield
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
 
 
 def W(name, B, Hq, Hkv, Lcap, N, lens, k_mult=1.0):
@@ -78,7 +78,7 @@ def _run(w, seed=0, ctas=0):
         out = torch.full((w.B, w.N), float("nan"), dtype=torch.bfloat16, device=DEV)
         da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out, x["scale"])
         torch.cuda.synchronize()
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
     return x, attn, out
 
 

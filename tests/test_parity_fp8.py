@@ -30,7 +30,7 @@ def _library():
     da.load()
     torch.cuda.set_device(0)
     yield
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
 
 
 def W(name, B, Hq, Hkv, Lcap, N, lens, k_mult=1.0):
@@ -56,7 +56,7 @@ def run_fp8(w, x, ctas=0):
         torch.cuda.synchronize()
     finally:
         da.decode_attn_set_option("attn_ctas", old)
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
     return attn, out
 
 

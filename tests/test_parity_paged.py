@@ -29,7 +29,7 @@ def _library():
     da.load()
     torch.cuda.set_device(0)
     yield
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
 
 
 def scatter(cache: torch.Tensor, bs: int, seed: int, spare: int = 3):
@@ -92,7 +92,7 @@ def test_paged_matches_oracle_and_contiguous(orc, w, bs):
     attn, out = _paged(w, x, kp, vp, table)
     attn0, out0 = _contiguous(w, x)
     torch.cuda.synchronize()
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
     assert torch.equal(attn, attn0), "paged attention differs from the contiguous path"
     assert torch.equal(out, out0), "paged output differs from the contiguous path"
     lens = x["seq_lens"].cpu().numpy().astype(np.int32)
@@ -149,7 +149,7 @@ def test_paged_table_row_stride_and_unused_entries():
     da.decode_attn_only_paged(x["q"], kp, vp, big[:, :10], x["seq_lens"], attn, x["scale"])
     attn0, _ = _contiguous(w, x)
     torch.cuda.synchronize()
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
     assert torch.equal(attn, attn0)
 
 
@@ -163,8 +163,8 @@ def test_paged_out_of_pool_block_is_reported(orc):
     table[1, 2] = kp.shape[0] + 7
     attn = torch.empty((2, 8, 128), dtype=torch.bfloat16, device=DEV)
     da.decode_attn_only_paged(x["q"], kp, vp, table, x["seq_lens"], attn, x["scale"])
-    assert da.decode_attn_device_error() == 64
-    assert da.decode_attn_device_error() == 0  # reading the word cleared it
+    assert da.decode_attn_last_device_error() == 64
+    assert da.decode_attn_last_device_error() == 0  # reading the word cleared it
     lens = x["seq_lens"].cpu().numpy().astype(np.int32)
     ref = orc.attention(synth.to_bits(x["q"]), orc.gather_pages(synth.to_bits(kp), table.cpu().numpy(), lens),
                         orc.gather_pages(synth.to_bits(vp), table.cpu().numpy(), lens), lens, x["scale"])
@@ -196,7 +196,7 @@ def test_paged_trigger_point_does_not_change_the_result():
     finally:
         da.decode_attn_set_option("attn_trigger", old)
     torch.cuda.synchronize()
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
     assert torch.equal(outs[0], outs[1])
 
 
@@ -218,7 +218,7 @@ def test_paged_flat_grid(orc, w, bs):
         torch.cuda.synchronize()
     finally:
         da.decode_attn_set_option("attn_cluster", old)
-    assert da.decode_attn_device_error() == 0
+    assert da.decode_attn_last_device_error() == 0
     assert torch.equal(attn, attn0) and torch.equal(out, out0)
     lens = x["seq_lens"].cpu().numpy().astype(np.int32)
     ref_attn, ref_out = orc.decode_paged(synth.to_bits(x["q"]), synth.to_bits(kp), synth.to_bits(vp),
