@@ -43,39 +43,53 @@ _lib = None
 _lock = threading.Lock()
 
 
+def load_library(path: str) -> ctypes.CDLL:
+    """Loads a build of the library at ``path`` with its argument types declared, without
+    making it the one the entry points below call (see :func:`use_library`)."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: run decode_attention_output_gb300.build.build() first")
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p  # a packed da_tensor_t (see _pack), a pointer to one, or NULL
+    vp, f32, i64 = ctypes.c_void_p, ctypes.c_float, ctypes.c_int64
+    lib.decode_attn_fwd.argtypes = [P, P, P, P, P, P, f32, vp]
+    lib.decode_attn_only.argtypes = [P, P, P, P, P, f32, vp]
+    lib.decode_attn_only_noalloc.argtypes = [P, P, P, P, P, f32, vp]
+    lib.decode_attn_fwd_paged.argtypes = [P, P, P, P, P, P, P, f32, vp]
+    lib.decode_attn_only_paged.argtypes = [P, P, P, P, P, P, f32, vp]
+    lib.decode_attn_fwd_fp8.argtypes = [P, P, P, P, P, P, f32, f32, f32, vp]
+    lib.decode_attn_only_fp8.argtypes = [P, P, P, P, P, f32, f32, f32, vp]
+    lib.decode_attn_scores.argtypes = [P, P, P, P, vp]
+    lib.decode_attn_oproj.argtypes = [P, P, P, vp]
+    lib.decode_attn_set_option.argtypes = [ctypes.c_char_p, i64]
+    lib.decode_attn_get_option.argtypes = [ctypes.c_char_p, ctypes.POINTER(i64)]
+    lib.decode_attn_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.decode_attn_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.decode_attn_release.argtypes = []
+    lib.decode_attn_release.restype = None
+    lib.decode_attn_status_str.argtypes = [ctypes.c_int]
+    lib.decode_attn_status_str.restype = ctypes.c_char_p
+    for name in EXPORTS:
+        if name not in ("decode_attn_release", "decode_attn_status_str"):
+            getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
 def load(path: str | None = None) -> ctypes.CDLL:
     """Loads the library (once). Fails loudly if it has not been built."""
     global _lib
     with _lock:
         if _lib is None:
-            path = path or _build.lib_path()
-            if not os.path.exists(path):
-                raise RuntimeError(f"{path} is missing: run decode_attention_output_gb300.build.build() first")
-            lib = ctypes.CDLL(path)
-            P = ctypes.c_void_p  # a packed da_tensor_t (see _pack), a pointer to one, or NULL
-            vp, f32, i64 = ctypes.c_void_p, ctypes.c_float, ctypes.c_int64
-            lib.decode_attn_fwd.argtypes = [P, P, P, P, P, P, f32, vp]
-            lib.decode_attn_only.argtypes = [P, P, P, P, P, f32, vp]
-            lib.decode_attn_only_noalloc.argtypes = [P, P, P, P, P, f32, vp]
-            lib.decode_attn_fwd_paged.argtypes = [P, P, P, P, P, P, P, f32, vp]
-            lib.decode_attn_only_paged.argtypes = [P, P, P, P, P, P, f32, vp]
-            lib.decode_attn_fwd_fp8.argtypes = [P, P, P, P, P, P, f32, f32, f32, vp]
-            lib.decode_attn_only_fp8.argtypes = [P, P, P, P, P, f32, f32, f32, vp]
-            lib.decode_attn_scores.argtypes = [P, P, P, P, vp]
-            lib.decode_attn_oproj.argtypes = [P, P, P, vp]
-            lib.decode_attn_set_option.argtypes = [ctypes.c_char_p, i64]
-            lib.decode_attn_get_option.argtypes = [ctypes.c_char_p, ctypes.POINTER(i64)]
-            lib.decode_attn_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
-            lib.decode_attn_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
-            lib.decode_attn_release.argtypes = []
-            lib.decode_attn_release.restype = None
-            lib.decode_attn_status_str.argtypes = [ctypes.c_int]
-            lib.decode_attn_status_str.restype = ctypes.c_char_p
-            for name in EXPORTS:
-                if name not in ("decode_attn_release", "decode_attn_status_str"):
-                    getattr(lib, name).restype = ctypes.c_int
-            _lib = lib
+            _lib = load_library(path or _build.lib_path())
     return _lib
+
+
+def use_library(lib: ctypes.CDLL | None) -> ctypes.CDLL | None:
+    """Makes ``lib`` (from :func:`load_library`) the library every entry point below calls
+    and returns the previous one; the tests use it to run the bounds-checked build."""
+    global _lib
+    with _lock:
+        prev, _lib = _lib, lib
+    return prev
 
 
 def describe(t: torch.Tensor | None) -> da_tensor_t | None:

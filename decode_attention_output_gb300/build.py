@@ -3,6 +3,11 @@
 Each .cu file compiles in its own nvcc process (in parallel), then one link
 step produces ``_lib/libdecode_attn.so``. A stamp of the sources, headers and
 flags skips the build when nothing changed.
+
+``build(checked=True)`` makes the bounds-checked copy instead,
+``_lib/checked/libdecode_attn_checked.so`` (compiled with -DDA_BOUNDS_CHECK: every
+guarded index is tested against its buffer and a failure is recorded in the device
+error word); the tests load it beside the regular library.
 """
 from __future__ import annotations
 
@@ -18,8 +23,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
-OBJ_DIR = os.path.join(PKG, "_lib", "obj")
 LIB_NAME = "libdecode_attn.so"
+CHECKED_NAME = "libdecode_attn_checked.so"
+CHECKED_FLAGS = ["-DDA_BOUNDS_CHECK"]
 SOURCES = ["api.cu", "attn_decode.cu", "attn_decode_d256.cu", "attn_decode_paged.cu", "attn_decode_fp8.cu",
            "oproj_gemv.cu", "oproj_umma.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -34,7 +40,9 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def lib_path() -> str:
+def lib_path(checked: bool = False) -> str:
+    if checked:
+        return os.path.join(LIB_DIR, "checked", CHECKED_NAME)
     return os.path.join(LIB_DIR, LIB_NAME)
 
 
@@ -49,12 +57,16 @@ def _stamp(extra=()) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link the library; returns its path."""
-    os.makedirs(OBJ_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checked: bool = False) -> str:
+    """Compile and link the library (or its bounds-checked copy); returns its path."""
+    if checked:
+        extra_flags = [*CHECKED_FLAGS, *extra_flags]
+    out = lib_path(checked)
+    out_dir = os.path.dirname(out)
+    obj_dir = os.path.join(out_dir, "obj")
+    os.makedirs(obj_dir, exist_ok=True)
     stamp = _stamp(extra_flags)
-    stamp_file = os.path.join(LIB_DIR, "stamp.txt")
-    out = lib_path()
+    stamp_file = os.path.join(out_dir, "stamp.txt")
     if not force and os.path.exists(out) and os.path.exists(stamp_file):
         with open(stamp_file) as f:
             if f.read().strip() == stamp:
@@ -62,7 +74,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     exe = nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OBJ_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
         cmd = [exe, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
@@ -87,4 +99,4 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checked="--checked" in sys.argv))

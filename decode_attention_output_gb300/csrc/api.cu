@@ -336,6 +336,7 @@ int check_paged_inputs(const da_tensor_t* q, const da_tensor_t* kp, const da_ten
 // ------------------------------------------------------------------ planning
 struct AttnPlan {
   int grid, nb, gpad;
+  long long slots;  // split-KV partial slots in the scratch
   int cluster;    // > 1: CTAs per sequence in cluster mode
   int flat_grid;  // the grid without cluster mode (the fall-back if a cluster launch is refused)
   size_t part_o_off, part_ml_off, bytes;
@@ -413,6 +414,7 @@ AttnPlan plan_attention(const AttnShape& s, const Options& o, int tile_tok = 0, 
   pl.nb = s.G <= 8 ? 1 : 2;
   pl.gpad = 8 * pl.nb;
   const size_t slots = (size_t)std::max(pl.grid, pl.flat_grid) + (size_t)s.B * s.Hkv;
+  pl.slots = (long long)slots;
   pl.part_ml_off = 0;
   pl.part_o_off = align_up(slots * pl.gpad * 2 * 4, 256);
   pl.bytes = pl.part_o_off + align_up(slots * pl.gpad * s.D * 4, 256);
@@ -456,6 +458,7 @@ int run_gemv(const __nv_bfloat16* x, long long x_sb, const da_tensor_t* w, const
   gp.y_sb = out->stride[0];
   gp.part = reinterpret_cast<float*>(scratch);
   gp.counters = reinterpret_cast<int*>(ws + kGemvCntOff);
+  gp.err = reinterpret_cast<int*>(ws + kErrOff);
   gp.B = B;
   gp.K = K;
   gp.N = N;
@@ -601,6 +604,7 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
     p.y = static_cast<__nv_bfloat16*>(fused->out->data);
     p.y_sb = fused->out->stride[0];
     p.proj_part = fused->part;
+    p.proj_part_floats = (long long)(fused->plan->part_bytes / 4);
     p.proj_counters = reinterpret_cast<int*>(ws + kGemvCntOff);
     p.grid_sync = reinterpret_cast<int*>(ws + kGridSyncOff);
     const Options o = options_snapshot();
@@ -619,6 +623,7 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
   if (paged) {
     p.block_table = paged->table;
     p.bt_stride = paged->table_stride;
+    p.bt_entries = paged->table_entries;
     p.block_size = paged->block_size;
     p.num_blocks = paged->num_blocks;
     p.block_shift = 0;
@@ -637,6 +642,7 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
   p.s_sh = s_sh;
   p.part_ml = reinterpret_cast<float*>(scratch + pl.part_ml_off);
   p.part_o = reinterpret_cast<float*>(scratch + pl.part_o_off);
+  p.part_slots = pl.slots;
   p.counters = reinterpret_cast<int*>(ws + kAttnCntOff);
   p.err = reinterpret_cast<int*>(ws + kErrOff);
   p.B = s.B;

@@ -276,11 +276,14 @@ __device__ void fused_epilogue(const AttnParams& p, uint64_t* bars, uint32_t tme
       continue;
     }
     const long long slot = (long long)blockIdx.x + tile;
+    const bool part_ok = in_bounds((slot * p.B + p.B) * 128 <= p.proj_part_floats, p.err);
 #pragma unroll
     for (int b = 0; b < NPAD; ++b)
-      if (b < p.B) p.proj_part[(slot * p.B + b) * 128 + m] = acc[b];
+      if (b < p.B && part_ok) p.proj_part[(slot * p.B + b) * 128 + m] = acc[b];
     named_bar_sync(2, 128);  // every epilogue thread's partial stores precede the release
-    if (tid == 0) flags[2] = (atomic_add_acq_rel_gpu(p.proj_counters + tile, 1) == np - 1);
+    if (tid == 0)
+      flags[2] = in_bounds(tile * p.kb_per_tile < p.units, p.err) &&
+                 atomic_add_acq_rel_gpu(p.proj_counters + tile, 1) == np - 1;
     named_bar_sync(2, 128);
     if (flags[2]) {  // the last part of this column tile: sum all parts in order
       // batch rows in chunks of up to 32; per pass about 64 loads from clamped (always
@@ -295,7 +298,8 @@ __device__ void fused_epilogue(const AttnParams& p, uint64_t* bars, uint32_t tme
           float v[kParts][kChunk];
 #pragma unroll
           for (int u = 0; u < kParts; ++u) {
-            const int pc = min(p0 + u, np - 1);
+            int pc = min(p0 + u, np - 1);
+            if (!in_bounds(((long long)first + pc + tile + 1) * p.B * 128 <= p.proj_part_floats, p.err)) pc = -first - tile;
 #pragma unroll
             for (int b = 0; b < kChunk; ++b)
               v[u][b] = __ldcg(p.proj_part + (((long long)first + pc + tile) * p.B + min(bc + b, p.B - 1)) * 128 + m);
@@ -355,6 +359,7 @@ __device__ __forceinline__ void paged_producer(const AttnParams& p, uint32_t rin
   // flat table index of a tile's first entry
   auto entry = [&](const Cursor& a) { return (long long)a.b * p.bt_stride + ((a.j << kLogT) >> lbs); };
   auto fetch = [&](const Cursor& a, int slot) {
+    in_bounds(entry(a) >= 0 && entry(a) < p.bt_entries, p.err);  // checked build: record only (TMA fills past the end)
     mbar_arrive_expect_tx(id_bar(slot), kRow * 4);
     tma_load_2d(smem_u32(ids + slot * kStride), &p.tm_table, id_bar(slot), (int)(entry(a) & ~3ll), 0);
   };
@@ -384,6 +389,7 @@ __device__ __forceinline__ void paged_producer(const AttnParams& p, uint32_t rin
       if (x + PF < end) cursor_next(ca, prefix, B, Hkv);
       continue;
     }
+    if (!in_bounds(c.b >= 0 && c.b < B && c.kvh >= 0 && c.kvh < Hkv, p.err)) c.b = c.kvh = 0;  // checked build
     const bool with_q = x - seg0 < kGroups;
     const int stage = it % S;
     const int t0 = c.j << kLogT;
@@ -477,6 +483,12 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
   const uint32_t ring = smem_u32(smem);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
+  // Guards of the bounds-checked build (constant true otherwise): an index against the
+  // extent of its buffer, a shared-memory range against this CTA's dynamic allocation.
+  const uint32_t smem_lo = smem_u32(smem_raw);
+  auto ok = [&](bool c) { return in_bounds(c, p.err); };
+  auto sm_ok = [&](uint32_t addr, uint32_t bytes) { return smem_in_bounds(smem_lo, addr, bytes, p.err); };
+  auto attn_ok = [&](int b, int h, int d) { return ok(b >= 0 && b < B && h >= 0 && h < Hkv * G && d >= 0 && d < DIM); };
 
   if (warp == kGroups * kGroupWarps && lane == 0) {
     // The producer's tensor maps first: their fetch then overlaps the set-up below (the
@@ -626,9 +638,14 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
         const uint32_t fb = full_bar(stage);
         uint32_t bytes = SCORES ? kKB : kSB;
         if (with_q) bytes += G * DIM * 2;
-        mbar_arrive_expect_tx(fb, bytes);
         const uint32_t kdst = ring + stage * kSB;
         const int t0 = c.j * kT;
+        // bounds-checked build: a cursor outside the batch is recorded and clamped, so that
+        // every copy stays inside the tensors and every wait of the kernel still ends
+        if (!(sm_ok(kdst, kSB) && sm_ok(smem_u32(q_slots + stage * kFixed.q_slot()), G * kQRow) &&
+              ok(c.b >= 0 && c.b < B && c.kvh >= 0 && c.kvh < Hkv && t0 >= 0 && t0 < Lcap)))
+          c.b = c.kvh = 0;
+        mbar_arrive_expect_tx(fb, bytes);
         tma_load_5d_hint(kdst, &p.tm_k, fb, 0, t0, 0, c.kvh, c.b, kv_policy);  // all D/64 boxes at once
         if (!SCORES) tma_load_5d_hint(kdst + kKB, &p.tm_v, fb, 0, t0, 0, c.kvh, c.b, kv_policy);
         for (long long todo = min(pf_piece, pf_end - pf_next); todo > 0;) {
@@ -665,7 +682,8 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
         if (lens[b] != 0) continue;
         const int kvh = s - b * Hkv;
         for (int h = tid / DIM; h < G; h += kHStep)
-          p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + (tid % DIM)] = __float2bfloat16_rn(0.f);
+          if (attn_ok(b, kvh * G + h, tid % DIM))
+            p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + (tid % DIM)] = __float2bfloat16_rn(0.f);
       }
     }
     uint32_t qf[NB][kKs][2];
@@ -704,6 +722,7 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
         cursor_next(c, prefix, B, Hkv);
         if (c.j == 0) seg0 = x;
       }
+      if (!ok(c.b >= 0 && c.b < B && c.kvh >= 0 && c.kvh < Hkv)) c.b = c.kvh = 0;  // checked build: record, clamp
       const bool last = (x == end - 1) || (c.j == c.nt - 1);
       if (it % kGroups == grp) {
         const int t0 = c.j * kT;
@@ -882,7 +901,8 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
               for (int i = 0; i < 4; ++i) {
                 const int head = nb * 8 + 2 * t + (i & 1);
                 const int tok = g + 8 * (i >> 1);
-                if (head < G && tok < vw && dh == 0)  // at D = 256 both warps of a pair hold S
+                if (head < G && tok < vw && dh == 0 &&  // at D = 256 both warps of a pair hold S
+                    ok(t0 + tb + tok >= 0 && t0 + tb + tok < Lcap))
                   p.scores[(long long)c.b * p.s_sb + (long long)(c.kvh * G + head) * p.s_sh + t0 + tb + tok] =
                       s[nb][i];
               }
@@ -957,6 +977,7 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
             for (int off = 4; off < 32; off <<= 1) l_run[nb][cc] += __shfl_xor_sync(0xffffffffu, l_run[nb][cc], off);
         float* mo = merge_o + wg * HP * kMergeRow;
         float* ml = merge_ml + wg * HP * 2;
+        if (!(sm_ok(smem_u32(mo), HP * kMergeRow * 4) && sm_ok(smem_u32(ml), HP * 2 * 4))) mo = ml = merge_ml;
         // (1) group 1 hands its state to the partner warp of group 0
         if (grp == 1) {
 #pragma unroll
@@ -1054,14 +1075,17 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
           }
           if constexpr (KV8) acc *= p.v_scale;  // V = v_cache * v_scale (linear through every merge)
           if (on_chip) {
-            cpart_o[(cslot * HP + h) * DIM + d] = acc;
-            if (d == 0) {
-              cpart_ml[(cslot * HP + h) * 2] = M;
-              cpart_ml[(cslot * HP + h) * 2 + 1] = lsum;
+            if (ok(cslot >= 0 && cslot < 2 && h < HP) && sm_ok(smem_u32(cpart_ml + (cslot * HP + h) * 2), 8)) {
+              cpart_o[(cslot * HP + h) * DIM + d] = acc;
+              if (d == 0) {
+                cpart_ml[(cslot * HP + h) * 2] = M;
+                cpart_ml[(cslot * HP + h) * 2 + 1] = lsum;
+              }
             }
           } else if (n_parts == 1) {
-            p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
-          } else {
+            if (attn_ok(b, kvh * G + h, d))
+              p.attn[(long long)b * p.a_sb + (long long)(kvh * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
+          } else if (ok((long long)cta + seq < p.part_slots && h < p.gpad)) {
             // evict-last: a part written early in the launch (a range's first segment) must
             // still be in L2 when the sequence's last CTA merges it, after the K/V stream
             const uint64_t keep = l2_policy_evict_last();
@@ -1075,7 +1099,8 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
         }
         if (!on_chip && n_parts > 1) {
           named_bar_sync(1, kConsumerThreads);  // every thread's partial stores precede the release
-          if (tid == 0) flags[1] = (atomic_add_acq_rel_gpu(p.counters + seq, 1) == n_parts - 1);
+          if (tid == 0)
+            flags[1] = ok(seq >= 0 && seq < B * Hkv) && atomic_add_acq_rel_gpu(p.counters + seq, 1) == n_parts - 1;
           named_bar_sync(1, kConsumerThreads);  // ... and the acquire precedes every thread's loads
           if (flags[1]) {  // every other part has landed: merge them all, in one pass
             // Thread (h, d) loads the parts' (m, l, O[h][d]) for two of its heads together,
@@ -1089,7 +1114,8 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
                 float mv[2][8], lv[2][8], ov[2][8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                  const long long slot = (long long)first_cta + min(p0 + u, n_parts - 1) + seq;
+                  long long slot = (long long)first_cta + min(p0 + u, n_parts - 1) + seq;
+                  if (!ok(slot >= 0 && slot < p.part_slots)) slot = 0;
 #pragma unroll
                   for (int k = 0; k < 2; ++k) {
                     const float* ml = p.part_ml + (slot * p.gpad + hs[k]) * 2;
@@ -1119,7 +1145,7 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
               }
 #pragma unroll
               for (int k = 0; k < 2; ++k)
-                if (k == 0 || hs[1] != h)
+                if ((k == 0 || hs[1] != h) && attn_ok(b, kvh * G + hs[k], d))
                   p.attn[(long long)b * p.a_sb + (long long)(kvh * G + hs[k]) * p.a_sh + d] =
                       __float2bfloat16_rn(acc[k] / lsum[k]);
             }
@@ -1165,6 +1191,7 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
       if (np == 0) continue;
       const int sq = duty[4 * k], f = duty[4 * k + 1], fslot = duty[4 * k + 3];
       const int bq = sq / Hkv, kq = sq - bq * Hkv;
+      if (!ok(np <= cs && cta >= f && cta - f < np && fslot >= 0 && fslot < 2 && sq >= 0 && sq < B * Hkv)) continue;
       const int items = G * DIM, chunk = (items + np - 1) / np, mine = cta - f;
       const int i_end = min(items, (mine + 1) * chunk);
       for (int item = mine * chunk + tid; item < i_end; item += kThreads) {
@@ -1192,7 +1219,8 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
             lsum += w * lv[q];
             acc += w * ov[q];
           }
-        p.attn[(long long)bq * p.a_sb + (long long)(kq * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
+        if (attn_ok(bq, kq * G + h, d))
+          p.attn[(long long)bq * p.a_sb + (long long)(kq * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
       }
     }
     cluster_sync();  // no CTA leaves while another still reads its shared memory

@@ -118,6 +118,7 @@ struct AttnParams {
   long long s_sb, s_sh;
   float* part_o;         // [slots][gpad][D] unnormalised partial outputs
   float* part_ml;        // [slots][gpad][2]   (running max in log2 units, sum)
+  long long part_slots;  // slots of part_o / part_ml (checked in the bounds-checked build)
   int* counters;         // [B*Hkv] completion counters (zero between calls)
   int* err;              // device error word
   int B, Hkv, G, Lcap;
@@ -135,6 +136,7 @@ struct AttnParams {
   __nv_bfloat16* y;      // [B][N]
   long long y_sb;
   float* proj_part;      // [slots][B][128] fp32 split-K partials
+  long long proj_part_floats;  // floats of proj_part (checked in the bounds-checked build)
   int* proj_counters;    // [column tiles], zero between calls
   int* grid_sync;        // [2]: arrivals, departures of the grid barrier, zero between calls
   unsigned long long sync_limit_ns;  // the grid barrier's wait limit (0: two seconds)
@@ -147,6 +149,7 @@ struct AttnParams {
   // is row t % block_size of block block_table[b * bt_stride + t / block_size].
   const int* block_table;
   long long bt_stride;
+  long long bt_entries;  // flat extent of the table, (B - 1) * bt_stride + max_blocks
   int block_size, num_blocks;
   int block_shift;       // log2(block_size)
   CUtensorMap tm_table;  // the table as one flat int32 array (one row), box 16 entries
@@ -206,6 +209,7 @@ struct GemvParams {
   long long y_sb;
   float* part;             // [ksplit][B][N] fp32 split-K partials
   int* counters;           // [batch chunks][column blocks]
+  int* err;                // device error word (bounds-checked build)
   int B, K, N, kc, ksplit;
 };
 
@@ -224,7 +228,7 @@ struct UmmaParams {
   CUtensorMap tm_x;  // X [B][K] bf16: box 64 k x npad batch rows, 128B swizzle
   __nv_bfloat16* y;  // [B][N]
   long long y_sb;
-  float* part;       // [ksplit][B][N] fp32 split-K partials
+  float* part;       // [ksplit][B][N] fp32 split-K partials (null: the cluster reduction)
   int* counters;     // [batch chunks][column tiles]
   int* err;
   int B, K, N, ksplit;

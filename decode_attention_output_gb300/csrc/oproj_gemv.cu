@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) oproj_gemv_kernel(const __gri
     const int c = col0 + tid;
     if (b0 + b < p.B && c < p.N) {
       if (p.ksplit == 1) p.y[(long long)(b0 + b) * p.y_sb + c] = __float2bfloat16_rn(sum);
-      else p.part[((long long)ks * p.B + b0 + b) * p.N + c] = sum;
+      else if (in_bounds(ks < p.ksplit && b0 + b < p.B && c < p.N, p.err)) p.part[((long long)ks * p.B + b0 + b) * p.N + c] = sum;
     }
   }
   if (p.ksplit == 1) return;

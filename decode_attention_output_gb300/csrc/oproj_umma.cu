@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 2) oproj_umma_kernel(const __gri
     // so every stage was consumed). CTA r of the cluster sums its share of the outputs
     // over the slices in slice order (deterministic) and writes bf16.
     float* red = reinterpret_cast<float*>(smem);
+    static_assert(NPAD * kUmmaBM * 4 <= C::kStages * C::kStage, "the fp32 tile fits the ring");
 #pragma unroll
     for (int b = 0; b < NPAD; ++b) red[b * kUmmaBM + warp * 32 + lane] = acc[b];
     cluster_sync();  // every slice's tile is in its CTA's shared memory
@@ -174,7 +175,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 2) oproj_umma_kernel(const __gri
     const int total = nb_valid * kUmmaBM, chunk = (total + p.ksplit - 1) / p.ksplit;
     const int o_end = min(total, (rank + 1) * chunk);
     const uint32_t red_u32 = smem_u32(red);
-    for (int o = rank * chunk + tid; o < o_end; o += kUmmaThreads) {
+    const bool red_ok = in_bounds(p.ksplit <= kMaxClusterSplit && rank < p.ksplit && o_end <= NPAD * kUmmaBM, p.err);
+    for (int o = rank * chunk + tid; red_ok && o < o_end; o += kUmmaThreads) {
       float v[kMaxClusterSplit];
 #pragma unroll
       for (int q = 0; q < kMaxClusterSplit; ++q)
@@ -183,13 +185,14 @@ __global__ void __launch_bounds__(kUmmaThreads, 2) oproj_umma_kernel(const __gri
 #pragma unroll
       for (int q = 0; q < kMaxClusterSplit; ++q) sum += q < p.ksplit ? v[q] : 0.f;
       const int b = o / kUmmaBM, nn = n0 + o % kUmmaBM;
-      if (nn < p.N) p.y[(long long)(b0 + b) * p.y_sb + nn] = __float2bfloat16_rn(sum);
+      if (nn < p.N && in_bounds(b0 + b < p.B, p.err)) p.y[(long long)(b0 + b) * p.y_sb + nn] = __float2bfloat16_rn(sum);
     }
     cluster_sync();  // no CTA leaves while another still reads its shared memory
   } else {
 #pragma unroll
     for (int b = 0; b < NPAD; ++b)
-      if (n_ok && b0 + b < p.B) p.part[((long long)ks * p.B + b0 + b) * p.N + n] = acc[b];
+      if (n_ok && b0 + b < p.B && in_bounds(ks < p.ksplit && p.part != nullptr, p.err))
+        p.part[((long long)ks * p.B + b0 + b) * p.N + n] = acc[b];
     __syncthreads();  // every thread's partial stores precede the release below
     int* counter = p.counters + blockIdx.z * gridDim.x + mt;
     if (tid == 0) *flag = (atomic_add_acq_rel_gpu(counter, 1) == p.ksplit - 1);

@@ -21,6 +21,7 @@ enum : int {
   kErrTmem = 16,         // TMEM allocation failed
   kErrGridSync = 32,     // the fused step's grid barrier did not complete
   kErrBlockTable = 64,   // a paged cache's block table named a block outside the pool
+  kErrBounds = 256,      // bounds-checked build: an index fell outside its buffer (access skipped)
 };
 
 // Two seconds: a kernel of this library runs for milliseconds at most.
@@ -34,6 +35,41 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// ---------------------------------------------------------- bounds-checked build
+// Compiled with -DDA_BOUNDS_CHECK, the kernels test every guarded index before the
+// access it feeds: an index outside its buffer ORs kErrBounds into the error word and the
+// access is skipped (no trap, no assert: the kernel carries on and the host reads the
+// word). Without the macro every guard is the constant true and compiles away.
+#ifdef DA_BOUNDS_CHECK
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+
+__device__ __forceinline__ bool in_bounds(bool ok, int* err) {
+  if constexpr (kBoundsCheck) {
+    if (!ok) atomicOr(err, kErrBounds);
+    return ok;
+  } else {
+    return true;
+  }
+}
+
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+  uint32_t r;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+  return r;
+}
+
+// [addr, addr + bytes) lies in this CTA's dynamic shared memory, whose first byte is `lo`.
+__device__ __forceinline__ bool smem_in_bounds(uint32_t lo, uint32_t addr, uint32_t bytes, int* err) {
+  if constexpr (kBoundsCheck) {
+    return in_bounds(addr >= lo && addr + bytes <= lo + dynamic_smem_bytes(), err);
+  } else {
+    return true;
+  }
 }
 
 // ---------------------------------------------------------------- mbarrier

@@ -465,3 +465,35 @@ def test_fused_step_integer_exact():
     torch.cuda.synchronize()
     assert da.decode_attn_last_device_error() == 0
     assert torch.equal(out.cpu(), ref)
+
+
+def test_graph_replays_and_eager_calls_agree_with_the_oracle(orc):
+    """decode_attn_fwd captured in a CUDA graph and replayed, interleaved with eager calls,
+    on inputs refilled in place between calls: every result matches the oracle (the
+    workspace's completion counters return to zero after every call, whichever way it
+    was launched)."""
+    w = W("graph", 2, 32, 8, 1000, 512, (1000, 517))
+    x = synth.make_inputs(w, seed=31, device=DEV)
+    out = torch.full((w.B, w.N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    st = torch.cuda.Stream(DEV)
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out, x["scale"])
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out, x["scale"])
+        for i in range(6):
+            y = synth.make_inputs(w, seed=40 + i, device=DEV)
+            for k in ("q", "k_cache", "v_cache"):
+                x[k].copy_(y[k])
+            out.fill_(float("nan"))
+            if i % 2:
+                da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out, x["scale"])
+            else:
+                g.replay()
+            st.synchronize()
+            assert da.decode_attn_last_device_error(st) == 0
+            _, ref_out = oracle_decode(orc, x)
+            assert_bf16_close(f64(out), ref_out, f"call {i} ({'eager' if i % 2 else 'graph'})")
+    del g
