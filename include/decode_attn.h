@@ -274,7 +274,8 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *                   projection reads o_weight from L2 (measured slower on GB300:
  *                   the prefetch competes with the K/V stream)
  *   "attn_stages"   4 (default) or 6: depth of the attention kernel's K/V ring
- *                   (6 only at D = 128 and when it fits in shared memory for the batch)
+ *                   (6 only at D = 128, bf16 or fp8 cache, and when it fits in shared
+ *                   memory for the batch)
  *   "fused"         0 (default): decode_attn_fwd runs two launches (attention,
  *                   projection); 1: one persistent cooperative launch (attention,
  *                   a bounded grid barrier, tcgen05 projection) when batch <= 128

@@ -192,3 +192,24 @@ def test_fp8_trigger_point_does_not_change_the_result():
     finally:
         da.decode_attn_set_option("attn_trigger", old)
     assert torch.equal(outs[0], outs[1])
+
+
+SIX_STAGE_CASES = [c for c in CASES if c.name in ("f8_g4_ragged", "f8_g16", "f8_zero_len", "f8_equal_cs2",
+                                                   "f8_many_batches", "f8_tile_plus_one")]
+
+
+@pytest.mark.parametrize("w", SIX_STAGE_CASES, ids=[c.name for c in SIX_STAGE_CASES])
+def test_fp8_six_stage_ring(orc, w):
+    """The 6-stage ring (option attn_stages = 6) gives bit for bit the 4-stage result: the
+    ring depth changes when tiles arrive, not which CTA reads which tile or the merge order."""
+    x = synth.make_inputs(w, seed=34, device=DEV)
+    attn4, out4 = run_fp8(w, x)
+    old = da.decode_attn_get_option("attn_stages")
+    da.decode_attn_set_option("attn_stages", 6)
+    try:
+        attn6, out6 = run_fp8(w, x)
+    finally:
+        da.decode_attn_set_option("attn_stages", old)
+    assert torch.equal(attn4, attn6) and torch.equal(out4, out6)
+    ref_attn, ref_out = oracle_fp8(orc, x)
+    assert_bf16_close(f64(attn6), ref_attn, f"{w.name} attention, 6 stages")
