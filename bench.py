@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true", help="time the chosen workload only")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the workload's shape at this batch instead (profiler captures of a smaller case)")
     return ap.parse_args()
 
 
@@ -199,9 +201,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the attention kernel from the committed ncu summary,
-    valid only while the kernel sources are unchanged since the capture."""
+def recorded_traffic(workload: str, batch: int):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary, valid
+    only while the kernel sources are unchanged since the capture. A capture made on the
+    workload's shape at a smaller batch is scaled by the batch (the attention's bytes are
+    per batch row: K, V, q and its output)."""
     path = os.path.join(ROOT, "profiles", "attn_decode_traffic.json")
     try:
         with open(path) as f:
@@ -211,7 +215,7 @@ def recorded_traffic(workload: str):
     ent = rec.get(workload)
     if not ent or ent.get("kernel_hash") != kernel_source_hash():
         return None
-    return ent.get("dram_bytes_per_launch")
+    return ent.get("dram_bytes_per_launch") * batch / ent.get("captured_batch", batch)
 
 
 def fwd_call(da, x, out, stream=None):
@@ -440,6 +444,8 @@ def run_ours(args, world, rank, local):
     build.build()
     da.load()
     w = synth.WORKLOADS[args.workload]
+    if args.batch > 0:
+        w = dataclasses.replace(w, B=args.batch)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
     stream = torch.cuda.current_stream(dev)
@@ -479,7 +485,7 @@ def run_ours(args, world, rank, local):
     total_bytes = sum_over_ranks(world, float(nb["total"]))
     value = total_bytes / (step_ms_max * 1e-3) / 1e9
     achieved = t["attn_bytes"] / (t["attn_ms"] * 1e-3) / 1e9
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic(w.name, w.B)
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
@@ -545,7 +551,7 @@ def run_ours(args, world, rank, local):
             "dtype": "bf16" if w.kv == "bf16" else "e4m3 cache, f16 MMA",
             "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "kv_len": w.Lcap, "hidden": w.N,
-                       "head_dim": w.D, "kv_cache": w.kv,
+                       "head_dim": w.D, "kv_cache": w.kv, "batch_override": args.batch or None,
                        "seq_lens_sum": int(lens.sum().item()), "bytes_per_step": nb,
                        "l2": f"{n_sets} rotated input sets of {set_bytes / 1e6:.0f} MB (>2x L2 between reuses)",
                        "step_hbm_frac": value / world / peak, "step_frac_of_8TBps": value / world / NOMINAL_HBM_GBS,
