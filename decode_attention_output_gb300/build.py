@@ -27,7 +27,7 @@ LIB_NAME = "libdecode_attn.so"
 CHECKED_NAME = "libdecode_attn_checked.so"
 CHECKED_FLAGS = ["-DDA_BOUNDS_CHECK"]
 SOURCES = ["api.cu", "attn_decode.cu", "attn_decode_d256.cu", "attn_decode_paged.cu", "attn_decode_fp8.cu",
-           "oproj_gemv.cu", "oproj_umma.cu"]
+           "oproj_gemv.cu", "oproj_umma.cu", "oproj_onchip.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -21,7 +21,7 @@ using namespace da;
 // ------------------------------------------------------------------ options
 struct Options {
   int64_t attn_ctas = 0;
-  int64_t oproj_path = 0;  // 0 auto, 1 gemv, 2 tcgen05
+  int64_t oproj_path = 0;  // 0 auto, 1 gemv, 2 tcgen05, 3 on-chip staged (batch 1 behind the attention)
   int64_t oproj_splitk = 0;
   int64_t gemm_min_batch = 1;  // tcgen05 from batch 1 (with the cluster reduction: batch 1 step
                                // 18.9 -> 16.4 us against the CUDA-core GEMV)
@@ -520,18 +520,78 @@ int run_umma(const void* x, long long x_sb, const da_tensor_t* w, const da_tenso
   return launch_umma(up, pl.npad, pdl, stream) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
-// The projection step: picks the tcgen05 GEMM or the CUDA-core GEMV by batch size (or
-// the "oproj_path" option) and says how much scratch it needs.
+// The batch-1 projection with W staged on chip while the attention runs (oproj_onchip.cu):
+// one CTA per SM the attention leaves free, a grid of 512-column groups by k-ranges, each
+// CTA holding its rectangle of W in shared memory and registers. Feasible when the free SMs
+// can hold all of W that way.
+struct OnchipPlan {
+  bool ok = false;
+  int kgroups = 0, smem_kblocks = 0;
+  size_t bytes = 0;  // k-range parts
+};
+
+OnchipPlan plan_onchip(int B, int K, int N, int free_sms) {
+  OnchipPlan pl;
+  if (B != 1 || K % 64 || N % kOnchipCols || K <= 0 || N <= 0 || N / kOnchipCols > (int)kMaxCounters) return pl;
+  const int kb = K / 64, groups = N / kOnchipCols;
+  pl.smem_kblocks = onchip_max_smem_kblocks(K);
+  const int per_cta = pl.smem_kblocks + kOnchipRegKblocks;  // k-blocks one CTA can hold
+  if (pl.smem_kblocks <= 0 || free_sms < groups) return pl;
+  pl.kgroups = std::min(free_sms / groups, kb);
+  if ((kb + pl.kgroups - 1) / pl.kgroups > per_cta) return pl;  // the free SMs cannot hold all of W
+  pl.bytes = align_up((size_t)groups * pl.kgroups * kOnchipCols * 4, 256);
+  pl.ok = true;
+  return pl;
+}
+
+int run_onchip(const void* x, const da_tensor_t* w, const da_tensor_t* out, int K, int N, char* ws, char* scratch,
+               const OnchipPlan& pl, bool pdl, cudaStream_t stream) {
+  OnchipParams op;
+  memset(&op, 0, sizeof(op));
+  DA_TRY(encode_2d_map(&op.tm_w, w->data, K, N, w->stride[0], 64));
+  op.x = static_cast<const __nv_bfloat16*>(x);
+  op.w = static_cast<const __nv_bfloat16*>(w->data);
+  op.w_sk = w->stride[0];
+  op.y = static_cast<__nv_bfloat16*>(out->data);
+  op.part = reinterpret_cast<float*>(scratch);
+  op.counters = reinterpret_cast<int*>(ws + kGemvCntOff);
+  op.err = reinterpret_cast<int*>(ws + kErrOff);
+  op.K = K;
+  op.N = N;
+  op.kb = K / 64;
+  op.smem_kblocks = pl.smem_kblocks;
+  return launch_onchip(op, pl.kgroups, pdl, stream) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+// The projection step: picks the tcgen05 GEMM, the CUDA-core GEMV or (batch 1 behind the
+// attention) the on-chip-staged projection by batch size (or the "oproj_path" option) and
+// says how much scratch it needs.
 struct ProjPlan {
   bool gemm;
+  bool onchip = false;
   GemvPlan gv;
   UmmaPlan um;
+  OnchipPlan oc;
   size_t bytes;
 };
 
-ProjPlan plan_projection(int B, int K, int N, const Options& o) {
+// free_sms: SMs the attention kernel leaves free when the projection follows it (0: none).
+ProjPlan plan_projection(int B, int K, int N, const Options& o, int free_sms = 0) {
   ProjPlan pl;
-  pl.gemm = o.oproj_path == 2 || (o.oproj_path == 0 && B >= o.gemm_min_batch);
+  // On request only (option 3): measured slower than the tcgen05 path at batch 1 (21.8 against
+  // 15.6 us per step): the attention slows by ~2 us under W's concurrent stream, the register
+  // part of the staging issues at ~36 GB/s per SM, and the CUDA-core arithmetic after the
+  // wait takes ~2.4 us.
+  if (o.oproj_path == 3) {
+    pl.oc = plan_onchip(B, K, N, free_sms);
+    if (pl.oc.ok) {
+      pl.onchip = true;
+      pl.gemm = false;
+      pl.bytes = pl.oc.bytes;
+      return pl;
+    }
+  }
+  pl.gemm = o.oproj_path == 2 || ((o.oproj_path == 0 || o.oproj_path == 3) && B >= o.gemm_min_batch);  // 3 where infeasible: auto
   if (pl.gemm) {
     pl.um = plan_umma(B, K, N, o);
     pl.bytes = pl.um.bytes;
@@ -544,6 +604,7 @@ ProjPlan plan_projection(int B, int K, int N, const Options& o) {
 
 int run_projection(const __nv_bfloat16* x, long long x_sb, const da_tensor_t* w, const da_tensor_t* out, int B,
                    int K, int N, char* ws, char* scratch, const ProjPlan& pl, bool pdl, cudaStream_t stream) {
+  if (pl.onchip) return run_onchip(x, w, out, K, N, ws, scratch, pl.oc, pdl, stream);
   if (pl.gemm) return run_umma(x, x_sb, w, out, B, K, N, ws, scratch, pl.um, pdl, stream);
   return run_gemv(x, x_sb, w, out, B, K, N, ws, scratch, pl.gv, pdl, stream);
 }
@@ -729,16 +790,20 @@ int fwd_checked(const da_tensor_t* q, const da_tensor_t* k_cache, const da_tenso
                                  scale, st, o.l2_prefetch ? o_weight->data : nullptr, w_span, &fa);
     if (rc != DA_ERR_UNSUPPORTED) return rc;  // else: not co-resident here, take two launches
   }
-  const ProjPlan gp = plan_projection(s.B, (int)K, (int)N, o);
+  // Batch 1: the on-chip-staged projection takes the SMs the attention leaves free (it runs
+  // beside the attention, so it needs the programmatic dependent launch of both kernels).
+  const int free_sms = (o.pdl && o.attn_pdl && !ap.cluster) ? std::max(0, sm_count() - ap.grid) : 0;
+  const ProjPlan gp = plan_projection(s.B, (int)K, (int)N, o, free_sms);
   char* ws = nullptr;
   DA_TRY(workspace_get(ap.bytes + attn_bytes + gp.bytes, st, &ws));
   char* scratch = ws + kHeaderBytes;
   __nv_bfloat16* attn = reinterpret_cast<__nv_bfloat16*>(scratch + ap.bytes);
   // W_o span: rows 0..K-1 of stride w_sk, the last row N wide
   const long long w_span = ((long long)(K - 1) * o_weight->stride[0] + N) * 2;
+  // The on-chip projection stages W while the attention runs: launched right after its set-up.
   DA_TRY(run_attention(q, k_cache, v_cache, seq_lens, s, ap, ws, scratch, attn, K, s.D, nullptr, 0, 0, scale,
                        st, o.l2_prefetch ? o_weight->data : nullptr, w_span, nullptr, paged, kv8,
-                       (int)o.attn_trigger));
+                       gp.onchip ? 0 : (int)o.attn_trigger));
   return run_projection(attn, K, o_weight, out, s.B, (int)K, (int)N, ws, scratch + ap.bytes + attn_bytes, gp,
                         o.pdl != 0, st);
 }
@@ -770,7 +835,7 @@ int decode_attn_set_option(const char* key, int64_t value) {
   if (!key) return DA_ERR_OPTION;
   std::lock_guard<std::mutex> lk(g_mu);
   if (!strcmp(key, "attn_ctas") && value >= 0 && value <= kMaxAttnCtas) g_opt.attn_ctas = value;
-  else if (!strcmp(key, "oproj_path") && value >= 0 && value <= 2) g_opt.oproj_path = value;
+  else if (!strcmp(key, "oproj_path") && value >= 0 && value <= 3) g_opt.oproj_path = value;
   else if (!strcmp(key, "oproj_splitk") && value >= 0 && value <= 4096) g_opt.oproj_splitk = value;
   else if (!strcmp(key, "gemm_min_batch") && value >= 1) g_opt.gemm_min_batch = value;
   else if (!strcmp(key, "pdl") && (value == 0 || value == 1)) g_opt.pdl = value;

@@ -237,6 +237,30 @@ struct UmmaParams {
 };
 constexpr int kMaxClusterSplit = 8;  // portable cluster size
 
+// ---------------------------- projection of a single-row batch with W staged on chip
+constexpr int kOnchipThreads = 512;   // thread t: 8 columns (piece t % 8 of column tile t / 64), rows (t / 8) % 8 + 8 i
+constexpr int kOnchipCols = 512;      // columns of a CTA's group (1 KB of every row of W)
+constexpr int kOnchipRegKblocks = 3;  // k-blocks (64 rows) a CTA holds in registers (8 x 16 bytes each per thread)
+
+struct OnchipParams {
+  CUtensorMap tm_w;          // W [K][N] bf16 row-major: box 64 columns x 64 rows, 128B swizzle
+  const __nv_bfloat16* x;    // [K] the attention output of the one batch row (16-byte aligned)
+  const __nv_bfloat16* w;    // W, for the register-held k-blocks
+  long long w_sk;            // row stride of W in elements
+  __nv_bfloat16* y;          // [N]
+  float* part;               // [N / 512 groups][k-ranges][512] fp32 parts
+  int* counters;             // [N / 512] completion counters, zero between calls
+  int* err;
+  int K, N;                  // K a multiple of 64, N of 512
+  int kb;                    // K / 64
+  int smem_kblocks;          // k-blocks a CTA stages in shared memory (the rest of its range in registers)
+};
+size_t onchip_smem_bytes(int smem_kblocks, int K);
+int onchip_max_smem_kblocks(int K);
+// grid = (N / 512 column groups, kgroups k-ranges): one CTA per SM that the attention leaves
+// free; each CTA's k-range is at most smem_kblocks + kOnchipRegKblocks k-blocks.
+cudaError_t launch_onchip(const OnchipParams& p, int kgroups, bool pdl, cudaStream_t stream);
+
 size_t umma_smem_bytes(int npad);
 // grid = (ceil(N / 128), ksplit, ceil(B / npad)); npad in {16, 32, 64, 128}.
 cudaError_t launch_umma(const UmmaParams& p, int npad, bool pdl, cudaStream_t stream);

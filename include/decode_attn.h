@@ -239,7 +239,10 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *   "attn_ctas"     CTAs of the persistent attention kernel (0: one per SM, fewer for
  *                   small problems: about four tiles each by the cache capacity;
  *                   at most 512)
- *   "oproj_path"    0 auto, 1 CUDA-core GEMV, 2 tcgen05 tensor-core GEMM
+ *   "oproj_path"    0 auto, 1 CUDA-core GEMV, 2 tcgen05 tensor-core GEMM, 3 (decode_attn_fwd
+ *                   at batch 1) o_weight staged in the shared memory and registers of the
+ *                   SMs the attention leaves free while the attention runs, then a CUDA-core
+ *                   product (correct, measured slower on GB300; auto where it does not fit)
  *   "oproj_splitk"  split-K factor of the projection (0: auto, two CTAs per SM, at
  *                   most 8, at most 6 when K > 4096)
  *   "attn_cluster"  1 (default): where there is room for two or more CTAs per

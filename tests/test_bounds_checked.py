@@ -112,6 +112,7 @@ STEP_CASES = [
     (W("gemv", 5, 8, 2, 130, 264, (130, 7, 0, 64, 129)), {"oproj_path": 1}),
     (W("splitk_partials", 4, 32, 8, 256, 512, (256, 100, 1, 255)), {"oproj_cluster": 0, "oproj_splitk": 16}),
     (W("batch130", 130, 8, 2, 40, 256, tuple(int(v) for v in np.random.default_rng(2).integers(0, 41, 130))), {}),
+    (W("onchip_b1", 1, 32, 8, 1024, 2048, (1000,)), {"oproj_path": 3}),
 ]
 
 

@@ -497,3 +497,54 @@ def test_graph_replays_and_eager_calls_agree_with_the_oracle(orc):
             _, ref_out = oracle_decode(orc, x)
             assert_bf16_close(f64(out), ref_out, f"call {i} ({'eager' if i % 2 else 'graph'})")
     del g
+
+
+# ------------------------------------------- batch-1 projection staged on chip (option 3)
+ONCHIP_CASES = [
+    W("oc_b1_h4096", 1, 32, 8, 2048, 4096, (2048,)),
+    W("oc_b1_short", 1, 32, 8, 2048, 4096, (301,)),
+    W("oc_b1_n2048", 1, 32, 8, 1024, 2048, (1000,)),
+    W("oc_b1_g8", 1, 64, 8, 512, 4096, (512,)),
+    W("oc_b1_empty", 1, 32, 8, 256, 4096, (0,)),
+]
+
+
+@pytest.mark.parametrize("w", ONCHIP_CASES, ids=[c.name for c in ONCHIP_CASES])
+def test_onchip_projection_matches_oracle(orc, w):
+    """Batch 1 with the projection staged on chip behind the attention (option oproj_path = 3,
+    where the free SMs can hold W) against the oracle, and
+    against the tcgen05 projection within the bf16 tolerance (their sums run in other orders).
+    Called three times in a row: the strip counters return to zero after every call."""
+    x = synth.make_inputs(w, seed=19, device=DEV)
+    outs = {}
+    for path in (3, 2):
+        with _Opt(oproj_path=path):
+            out = torch.full((w.B, w.N), float("nan"), dtype=torch.bfloat16, device=DEV)
+            for _ in range(3):
+                da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out, x["scale"])
+            torch.cuda.synchronize()
+            assert da.decode_attn_last_device_error() == 0
+            outs[path] = out
+    _, ref_out = oracle_decode(orc, x)
+    assert_bf16_close(f64(outs[3]), ref_out, f"{w.name} on-chip projection")
+    assert_bf16_close(f64(outs[3]), f64(outs[2]), f"{w.name} on-chip vs tcgen05 projection")
+
+
+def test_onchip_projection_integer_exact():
+    """Integer attention outputs (V rows constant per KV head) and W in {-1, 0, 1}: the
+    on-chip projection's fp32 sums are exact, so the result is the exact integer product."""
+    B, Hq, Hkv, L, N = 1, 32, 8, 777, 4096
+    w = W("oc_int", B, Hq, Hkv, L, N, (L,))
+    x = synth.make_inputs(w, seed=3, device=DEV)
+    vals = torch.randint(-3, 4, (B, Hkv, 1, 128), generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    x["v_cache"][:] = vals.to(DEV)
+    wi = torch.randint(-1, 2, (Hq * 128, N), generator=torch.Generator().manual_seed(5))
+    attn_ref = vals[:, :, 0].repeat_interleave(Hq // Hkv, dim=1).reshape(B, Hq * 128).long()
+    ref = (attn_ref @ wi.long()).double().to(torch.bfloat16)
+    out = torch.full((B, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    with _Opt(oproj_path=3):
+        da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], wi.to(torch.bfloat16).to(DEV), out,
+                           x["scale"])
+    torch.cuda.synchronize()
+    assert da.decode_attn_last_device_error() == 0
+    assert torch.equal(out.cpu(), ref)
