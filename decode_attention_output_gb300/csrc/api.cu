@@ -651,6 +651,18 @@ struct FusedArgs {
   int K, N;
 };
 
+// Multiplier and shift that make floor(n / d) = (n * m) >> sh exact for 0 <= n < 2^31 (d >= 1):
+// sh = 31 + ceil(log2 d), m = ceil(2^sh / d) < 2^32 + 1, so n * m < 2^64 and n * m / 2^sh
+// exceeds n / d by less than n / 2^sh < 1 / d.
+void set_split_divisor(AttnParams& p, int k, int d) {
+  d = std::max(d, 1);
+  int l = 0;
+  while ((1ll << l) < d) ++l;
+  p.split_div[k] = d;
+  p.split_shift[k] = 31 + l;
+  p.split_mul[k] = ((1ull << (31 + l)) + (unsigned long long)d - 1) / (unsigned long long)d;
+}
+
 int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t* v, const da_tensor_t* lens,
                   const AttnShape& s, const AttnPlan& pl, char* ws, char* scratch, __nv_bfloat16* attn,
                   long long a_sb, long long a_sh, float* scores, long long s_sb, long long s_sh, float scale,
@@ -723,6 +735,10 @@ int run_attention(const da_tensor_t* q, const da_tensor_t* k, const da_tensor_t*
   p.pdl = options_snapshot().attn_pdl ? 1 : 0;
   p.trigger_at = fused ? 0 : trigger_at;
   auto launch = [&](int grid) {
+    // the worker counts the kernel divides the tiles by: the flat grid's and cluster mode's
+    const int flat = std::min(grid, p.attn_workers);
+    set_split_divisor(p, 0, flat);
+    set_split_divisor(p, 1, p.cluster > 1 ? (int)std::min<long long>(flat, (long long)s.B * s.Hkv * p.cluster) : flat);
     return kv8     ? launch_attention_fp8(p, grid, pl.nb, stream)
            : paged ? launch_attention_paged(p, grid, pl.nb, s.D, stream)
                    : launch_attention(p, grid, pl.nb, s.D, scores != nullptr, stream, fused ? fused->plan->npad : 0);

@@ -64,24 +64,8 @@ struct Cursor {
   int b, kvh, j, nt;  // batch row, KV head, tile index in the sequence, tiles in the sequence
 };
 
-// prefix[b] = KV heads x tiles of all batch rows before b; prefix[B] = total tiles.
-__device__ __forceinline__ Cursor cursor_at(long long x, const int* prefix, int B, int Hkv) {
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= x) lo = mid;
-    else hi = mid - 1;
-  }
-  Cursor c;
-  c.b = lo;
-  c.nt = (prefix[lo + 1] - prefix[lo]) / Hkv;
-  const int r = (int)(x - prefix[lo]);
-  c.kvh = r / c.nt;
-  c.j = r - c.kvh * c.nt;
-  return c;
-}
-
-// Advances to the next tile (only called while one exists).
+// Advances to the next tile (only called while one exists); prefix[b] = KV heads x tiles of
+// all batch rows before b, prefix[B] = total tiles.
 __device__ __forceinline__ void cursor_next(Cursor& c, const int* prefix, int B, int Hkv) {
   if (++c.j < c.nt) return;
   c.j = 0;
@@ -91,6 +75,29 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const int* prefix, int B,
     ++c.b;
   } while (c.b < B - 1 && prefix[c.b + 1] == prefix[c.b]);
   c.nt = (prefix[c.b + 1] - prefix[c.b]) / Hkv;
+}
+
+// floor(n / d) for 0 <= n < 2^31 from the host's m = ceil(2^s / d), s = 31 + ceil(log2 d):
+// n m / 2^s exceeds n / d by less than n / 2^s < 1 / d, too little to reach the next integer.
+__device__ __forceinline__ unsigned div_mul(unsigned n, unsigned long long m, int s) {
+  return (unsigned)(((unsigned long long)n * m) >> s);
+}
+
+// floor(a / b) for 0 <= a < 2^31, b > 0 and a quotient below 2^16: the float quotient's
+// relative error (two roundings to float and a 2-ulp division) stays below 2^-21, so it lies
+// within 0.05 of a / b and one step either way corrects its truncation.
+__device__ __forceinline__ int div_small(int a, int b) {
+  int q = (int)__fdividef((float)a, (float)b);
+  const long long r = (long long)a - (long long)q * b;
+  if (r < 0) --q;
+  else if (r >= b) ++q;
+  return q;
+}
+
+// Tiles of a range [start, end) copied by the set-up warp (contiguous caches): the first, and
+// the second when it lies in the same sequence (its first tile at j, of nt).
+__device__ __forceinline__ int early_tiles(long long start, long long end, int j, int nt) {
+  return end - start >= 2 && j + 1 < nt ? 2 : (end > start ? 1 : 0);
 }
 
 // CTA whose range [i*T/P, (i+1)*T/P) holds tile x.
@@ -334,7 +341,8 @@ __device__ void fused_epilogue(const AttnParams& p, uint64_t* bars, uint32_t tme
 template <int S, int DIM>
 __device__ __forceinline__ void paged_producer(const AttnParams& p, uint32_t ring, uint8_t* q_slots, size_t q_slot,
                                                uint64_t* bars, int* flags, const int* prefix, const int* lens,
-                                               int* ids, long long start, long long end, int role) {
+                                               int* ids, long long start, long long end, const Cursor& c_start,
+                                               int role) {
   // This lane shares its SM sub-partition with two busy consumer warps, so every
   // instruction per tile costs: block sizes are powers of two (shifts, no divisions),
   // and all but the copies is done before waiting for the stage.
@@ -372,12 +380,12 @@ __device__ __forceinline__ void paged_producer(const AttnParams& p, uint32_t rin
   // ring rows of the same parity (S and PF are even), and walks the same cursor to skip the
   // others.
   static_assert(S % 2 == 0 && PF % 2 == 0, "stages and id rows split by parity");
-  Cursor ca = cursor_at(start, prefix, B, Hkv);  // the tile whose ids were fetched last
+  Cursor ca = c_start;  // the tile whose ids were fetched last
   for (int k = 0; k < PF && start + k < end; ++k) {
     if (k > 0) cursor_next(ca, prefix, B, Hkv);
     if ((k & 1) == role) fetch(ca, k);
   }
-  Cursor c = cursor_at(start, prefix, B, Hkv);
+  Cursor c = c_start;
   long long seg0 = start;
   int it = 0;
   for (long long x = start; x < end; ++x, ++it) {
@@ -390,7 +398,7 @@ __device__ __forceinline__ void paged_producer(const AttnParams& p, uint32_t rin
       continue;
     }
     if (!in_bounds(c.b >= 0 && c.b < B && c.kvh >= 0 && c.kvh < Hkv, p.err)) c.b = c.kvh = 0;  // checked build
-    const bool with_q = x - seg0 < kGroups;
+    const bool with_q = seg0 != start && x - seg0 < kGroups;  // (the range's first q: the consumers)
     const int stage = it % S;
     const int t0 = c.j << kLogT;
     // boxes holding tokens of the sequence (>= 1: t0 < L); the first row in the block:
@@ -479,7 +487,7 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
   int* lens = reinterpret_cast<int*>(smem + lay.off_lens());                 // [B], clamped
   float* cpart_o = reinterpret_cast<float*>(smem + lay.off_cpart());         // [2][HP][DIM] (cluster mode)
   float* cpart_ml = cpart_o + 2 * HP * DIM;                                   // [2][HP][2]
-  int* duty = reinterpret_cast<int*>(cpart_ml + 2 * HP * 2);  // [2][4] merges to share, [8] equal lengths
+  int* duty = reinterpret_cast<int*>(cpart_ml + 2 * HP * 2);  // [2][4] merges to share
   const uint32_t ring = smem_u32(smem);
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + S + s); };
@@ -490,8 +498,11 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
   auto sm_ok = [&](uint32_t addr, uint32_t bytes) { return smem_in_bounds(smem_lo, addr, bytes, p.err); };
   auto attn_ok = [&](int b, int h, int d) { return ok(b >= 0 && b < B && h >= 0 && h < Hkv * G && d >= 0 && d < DIM); };
 
-  if (warp == kGroups * kGroupWarps && lane == 0) {
-    // The producer's tensor maps first: their fetch then overlaps the set-up below (the
+  // L2 policy of the producers' K/V copies (read exactly once); no memory access, so it is
+  // made before the wait below, off the path to the first copy
+  const uint64_t kv_policy = l2_policy_evict_first();
+  if (warp >= kGroups * kGroupWarps && lane == 0) {
+    // The producers' tensor maps first: their fetch then overlaps the set-up below (the
     // sequence lengths' load) instead of delaying the first copy.
     prefetch_tensormap(&p.tm_k);
     if (!SCORES) prefetch_tensormap(&p.tm_v);
@@ -501,7 +512,7 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
       prefetch_tensormap(&p.tm_x);
     }
   }
-  if (tid == 0) {
+  if (tid == 32) {  // (the set-up warp's first lane: it copies the first tiles, below)
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), kGroupWarps);
@@ -558,9 +569,84 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
       if (b < B) prefix[b + 1] = carry + v;
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
+    if (lane == 0) prefix[0] = 0;
+    // This CTA's range [start, end) of the T tiles and the cursor at its first tile, for every
+    // warp after the barrier. Worker c of P takes [c T / P, (c + 1) T / P), computed as
+    // c (T / P) + c (T % P) / P in 32-bit arithmetic (T < 2^31, c <= P <= 512), each division
+    // by P a multiply and a shift from the host when P is the worker count it expected.
+    __syncwarp();  // prefix[] and lens[] complete
+    const int T = carry;
+    // Cluster mode with unequal lengths: the cluster CTAs work as the flat grid does
+    const bool chip = p.cluster > 1 && !unequal;
+    int workers = min((int)gridDim.x, p.attn_workers);
+    if (chip) workers = min(workers, B * Hkv * p.cluster);
+    const int P = T > 0 ? min(workers, T) : 1;
+    const int cta = blockIdx.x;
+    int start = 0, end = 0;
+    if (T > 0 && cta < P) {
+      if (P == T) {  // one tile each
+        start = cta;
+        end = cta + 1;
+      } else {
+        unsigned tq, tr, f0, f1;
+        if (P == (chip ? p.split_div[1] : p.split_div[0])) {
+          const unsigned long long m = chip ? p.split_mul[1] : p.split_mul[0];
+          const int sh = chip ? p.split_shift[1] : p.split_shift[0];
+          tq = div_mul((unsigned)T, m, sh);
+          tr = (unsigned)T - tq * (unsigned)P;
+          f0 = div_mul((unsigned)cta * tr, m, sh);
+          f1 = div_mul((unsigned)(cta + 1) * tr, m, sh);
+        } else {
+          tq = (unsigned)T / (unsigned)P;
+          tr = (unsigned)T % (unsigned)P;
+          f0 = (unsigned)cta * tr / (unsigned)P;
+          f1 = (unsigned)(cta + 1) * tr / (unsigned)P;
+        }
+        start = (int)((unsigned)cta * tq + f0);
+        end = (int)((unsigned)(cta + 1) * tq + f1);
+      }
+    }
+    // The cursor at `start`: the last batch row whose first tile is at or before it (prefix
+    // is non-decreasing: count the rows at or before it, 32 at a time), then the KV head and
+    // the tile within the row's share.
+    int cb = 0, ckvh = 0, cj = 0, cnt = 1;
+    if (start < end) {
+      int rows = 0;
+      for (int base = 0; base < B; base += 32) {
+        const unsigned at = __ballot_sync(0xffffffffu, base + lane < B && prefix[base + lane] <= start);
+        rows += __popc(at);
+        if (at != 0xffffffffu) break;
+      }
+      cb = rows - 1;  // >= 0: prefix[0] = 0
+      cnt = (lens[cb] + kT - 1) / kT;
+      const int r = start - prefix[cb];
+      ckvh = div_small(r, cnt);
+      cj = r - ckvh * cnt;
+    }
+    // The first tile of each consumer group (lane g: group g's, stage g), copied now so that
+    // they are in flight while the other warps pass the set-up barrier; the second only if
+    // it lies in the same sequence (it then needs no q: the consumers read the range's first
+    // q themselves). The barriers are fresh, initialised by lane 0 of this warp.
+    if (!PAGED && lane < kGroups && lane < early_tiles(start, end, cj, cnt)) {
+      Cursor ce = {cb, ckvh, cj, cnt};
+      if (lane == 1) cursor_next(ce, prefix, B, Hkv);
+      const uint32_t fb = full_bar(lane), dst = ring + lane * kSB;
+      if (!(sm_ok(dst, kSB) && ok(ce.b >= 0 && ce.b < B && ce.kvh >= 0 && ce.kvh < Hkv && ce.j * kT < Lcap)))
+        ce.b = ce.kvh = ce.j = 0;  // checked build: record, clamp
+      mbar_arrive_expect_tx(fb, SCORES ? kKB : kSB);
+      tma_load_5d_hint(dst, &p.tm_k, fb, 0, ce.j * kT, 0, ce.kvh, ce.b, kv_policy);
+      if (!SCORES) tma_load_5d_hint(dst + kKB, &p.tm_v, fb, 0, ce.j * kT, 0, ce.kvh, ce.b, kv_policy);
+    }
     if (lane == 0) {
-      prefix[0] = 0;
-      if (p.cluster > 1) duty[8] = unequal ? 0 : 1;
+      int* rng = flags + 8;
+      rng[0] = start;
+      rng[1] = end;
+      rng[2] = P;
+      rng[3] = cb;
+      rng[4] = ckvh;
+      rng[5] = cj;
+      rng[6] = cnt;
+      rng[7] = chip ? 1 : 0;
     }
   }
   if (kFused) tc_fence_before_sync();
@@ -575,6 +661,7 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
 
   const long long T = prefix[B];
   const int cta = blockIdx.x;
+  const int* rng = flags + 8;  // range and first cursor (set-up warp)
   // > 1: cluster mode: the grid comes in clusters of `cs` consecutive CTAs. With equal
   // lengths the tiles go to B * Hkv * cs workers, cs per sequence, so that the parts of
   // every sequence lie in one cluster and merge on chip (the grid's other CTAs leave at
@@ -583,33 +670,28 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
   // With unequal lengths the cluster CTAs work as the flat grid does, without on-chip
   // merges and without the cluster barriers at the end, which would hold every CTA of a
   // cluster until its slowest one is done (the same flag in every CTA).
-  const bool chip = cs > 1 && duty[8];
-  int workers = min((int)gridDim.x, p.attn_workers);
-  if (chip) workers = min(workers, B * Hkv * cs);
+  const bool chip = rng[7] != 0;
   // P workers share the T tiles; with P <= T every range is non-empty, so the CTAs
   // cta_of(first tile) .. cta_of(last tile) of a sequence all hold a part of it.
-  const int P = T > 0 ? (int)min((long long)workers, T) : 1;
-  // floor(c * T / P) = c * (T / P) + floor(c * (T % P) / P) in 32-bit arithmetic (T < 2^31,
-  // c <= P <= 512): no 64-bit division on the way to the first copy
-  const unsigned Tq = (unsigned)T / (unsigned)P, Tr = (unsigned)T % (unsigned)P;
-  auto split = [&](int c) { return (long long)c * Tq + (long long)(((unsigned)c * Tr) / (unsigned)P); };
-  long long start = (T > 0 && cta < P) ? split(cta) : 0;
-  long long end = (T > 0 && cta < P) ? split(cta + 1) : 0;
+  const int P = rng[2];
+  // first tile of worker c, floor(c * T / P) (off the path to the first copy)
+  auto split = [&](int c) {
+    return (long long)c * ((unsigned)T / (unsigned)P) + (long long)(((unsigned)c * ((unsigned)T % (unsigned)P)) / (unsigned)P);
+  };
+  const long long start = rng[0], end = rng[1];
+  const Cursor c_start = {rng[3], rng[4], rng[5], rng[6]};
 
   if (warp >= kGroups * kGroupWarps) {
     // ------------------------------------------------------------ producer(s)
     if constexpr (PAGED) {
       if (lane == 0)
         paged_producer<S, DIM>(p, ring, q_slots, kFixed.q_slot(), bars, flags, prefix, lens,
-                               reinterpret_cast<int*>(smem + lay.off_ids()), start, end,
+                               reinterpret_cast<int*>(smem + lay.off_ids()), start, end, c_start,
                                warp - kGroups * kGroupWarps);
     } else if (lane == 0) {
      const int role = warp - kGroups * kGroupWarps;  // with two producers: tiles of parity `role`
      int it = 0;
      if (start < end) {
-      prefetch_tensormap(&p.tm_k);
-      if (!SCORES) prefetch_tensormap(&p.tm_v);
-      const uint64_t kv_policy = l2_policy_evict_first();  // K/V are read exactly once
       // This CTA's share of the prefetch region, in 4 KB-aligned pieces, one per tile.
       const uint64_t pf_policy = l2_policy_evict_last();
       long long pf_next = 0, pf_end = 0, pf_piece = 0;
@@ -623,7 +705,8 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
           else pf_piece *= 2;
         }
       }
-      Cursor c = cursor_at(start, prefix, B, Hkv);
+      const int n_early = early_tiles(start, end, c_start.j, c_start.nt);
+      Cursor c = c_start;
       long long seg0 = start;
       for (long long x = start; x < end; ++x, ++it) {
         if (x != start) {
@@ -631,23 +714,27 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
           if (c.j == 0) seg0 = x;
         }
         if (kProducers == 2 && (it & 1) != role) continue;  // the other producer's tile
-        const bool with_q = x - seg0 < kGroups;  // each group's first tile of the segment
+        // each group's first tile of a segment that starts inside the range (the consumers
+        // read the range's first q themselves)
+        const bool with_q = seg0 != start && x - seg0 < kGroups;
         const int stage = it % S;
         const uint32_t ph = (it / S) & 1;
-        mbar_wait_bounded(empty_bar(stage), ph ^ 1, p.err, kErrWaitEmpty, flags);
         const uint32_t fb = full_bar(stage);
-        uint32_t bytes = SCORES ? kKB : kSB;
-        if (with_q) bytes += G * DIM * 2;
-        const uint32_t kdst = ring + stage * kSB;
-        const int t0 = c.j * kT;
-        // bounds-checked build: a cursor outside the batch is recorded and clamped, so that
-        // every copy stays inside the tensors and every wait of the kernel still ends
-        if (!(sm_ok(kdst, kSB) && sm_ok(smem_u32(q_slots + stage * kFixed.q_slot()), G * kQRow) &&
-              ok(c.b >= 0 && c.b < B && c.kvh >= 0 && c.kvh < Hkv && t0 >= 0 && t0 < Lcap)))
-          c.b = c.kvh = 0;
-        mbar_arrive_expect_tx(fb, bytes);
-        tma_load_5d_hint(kdst, &p.tm_k, fb, 0, t0, 0, c.kvh, c.b, kv_policy);  // all D/64 boxes at once
-        if (!SCORES) tma_load_5d_hint(kdst + kKB, &p.tm_v, fb, 0, t0, 0, c.kvh, c.b, kv_policy);
+        if (it >= n_early) {  // (the first ones: copied by the set-up warp)
+          if (it >= S) mbar_wait_bounded(empty_bar(stage), ph ^ 1, p.err, kErrWaitEmpty, flags);  // (fresh before)
+          uint32_t bytes = SCORES ? kKB : kSB;
+          if (with_q) bytes += G * DIM * 2;
+          const uint32_t kdst = ring + stage * kSB;
+          const int t0 = c.j * kT;
+          // bounds-checked build: a cursor outside the batch is recorded and clamped, so that
+          // every copy stays inside the tensors and every wait of the kernel still ends
+          if (!(sm_ok(kdst, kSB) && sm_ok(smem_u32(q_slots + stage * kFixed.q_slot()), G * kQRow) &&
+                ok(c.b >= 0 && c.b < B && c.kvh >= 0 && c.kvh < Hkv && t0 >= 0 && t0 < Lcap)))
+            c.b = c.kvh = 0;
+          mbar_arrive_expect_tx(fb, bytes);
+          tma_load_5d_hint(kdst, &p.tm_k, fb, 0, t0, 0, c.kvh, c.b, kv_policy);  // all D/64 boxes at once
+          if (!SCORES) tma_load_5d_hint(kdst + kKB, &p.tm_v, fb, 0, t0, 0, c.kvh, c.b, kv_policy);
+        }
         for (long long todo = min(pf_piece, pf_end - pf_next); todo > 0;) {
           const long long n = min(todo, 32768ll);
           bulk_prefetch_l2(p.prefetch + pf_next, (uint32_t)n, pf_policy);
@@ -713,8 +800,45 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
     const uint32_t qk_row = row_off(tb + (lane & 7) + ((lane >> 3) & 1) * 8);  // ldmatrix rows of S^T
     const uint32_t pv_row = row_off(tb + (lane & 7) + ((lane >> 4) & 1) * 8);  // ldmatrix.trans rows of V
     const float sl2 = p.scale_log2;
+    // q fragments of a segment's (batch row, KV head): head h's row at rows + h * stride bytes
+    // (in shared memory for the segments that start inside the range, whose first tiles carry
+    // q; from global memory for the range's first segment, loaded while its first stages are
+    // in flight). Head rows at or past `heads` read as zero.
+    auto load_q = [&](const uint8_t* rows, long long stride, int heads, bool global) {
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const int h = nb * 8 + g;
+#pragma unroll
+        for (int ks = 0; ks < kKs; ++ks) {
+          uint32_t w0 = 0, w1 = 0;
+          if constexpr (KV8) {
+            // k-slots 2t, 2t+1, 2t+8, 2t+9 of step ks hold dims 16ks + 4t .. 4t+3 (the
+            // order in which an fp8 K row reaches this lane); q in f16, same order
+            const uint8_t* row = rows + h * stride + (ks * 16 + 4 * t) * 2;
+            if (h < heads) {
+              const uint2 w = global ? __ldg(reinterpret_cast<const uint2*>(row)) : *reinterpret_cast<const uint2*>(row);
+              w0 = bf16x2_to_f16x2_clamped(w.x);
+              w1 = bf16x2_to_f16x2_clamped(w.y);
+            }
+          } else {
+            const uint8_t* row = rows + h * stride + (ks * 16 + 2 * t) * 2;
+            if (h < heads) {
+              w0 = global ? __ldg(reinterpret_cast<const uint32_t*>(row)) : *reinterpret_cast<const uint32_t*>(row);
+              w1 = global ? __ldg(reinterpret_cast<const uint32_t*>(row + 16)) : *reinterpret_cast<const uint32_t*>(row + 16);
+            }
+          }
+          qf[nb][ks][0] = w0;
+          qf[nb][ks][1] = w1;
+        }
+      }
+    };
     Cursor c;
-    if (start < end) c = cursor_at(start, prefix, B, Hkv);
+    if (start < end) {
+      c = c_start;
+      if (ok(c.b >= 0 && c.b < B && c.kvh >= 0 && c.kvh < Hkv))
+        load_q(reinterpret_cast<const uint8_t*>(p.q + (long long)c.b * p.q_sb + (long long)(c.kvh * G) * p.q_sh),
+               p.q_sh * 2, G, true);
+    }
     long long seg0 = start;
     int it = 0;
     for (long long x = start; x < end; ++x, ++it) {
@@ -730,27 +854,8 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
         const int stage = it % S;
         const uint32_t ph = (it / S) & 1;
         mbar_wait_bounded(full_bar(stage), ph, p.err, kErrWaitFull, flags);
-        if (x - seg0 < kGroups) {  // this group's first tile of the segment carries q
-          const uint8_t* qs = q_slots + stage * kFixed.q_slot();
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-#pragma unroll
-            for (int ks = 0; ks < kKs; ++ks) {
-              if constexpr (KV8) {
-                // k-slots 2t, 2t+1, 2t+8, 2t+9 of step ks hold dims 16ks + 4t .. 4t+3 (the
-                // order in which an fp8 K row reaches this lane); q in f16, same order
-                const uint8_t* row = qs + (nb * 8 + g) * kQRow + (ks * 16 + 4 * t) * 2;
-                const uint2 w = *reinterpret_cast<const uint2*>(row);
-                qf[nb][ks][0] = bf16x2_to_f16x2_clamped(w.x);
-                qf[nb][ks][1] = bf16x2_to_f16x2_clamped(w.y);
-              } else {
-                const uint8_t* row = qs + (nb * 8 + g) * kQRow + (ks * 16 + 2 * t) * 2;
-                qf[nb][ks][0] = *reinterpret_cast<const uint32_t*>(row);
-                qf[nb][ks][1] = *reinterpret_cast<const uint32_t*>(row + 16);
-              }
-            }
-          }
-        }
+        if (seg0 != start && x - seg0 < kGroups)  // this group's first tile of the segment carries q
+          load_q(q_slots + stage * kFixed.q_slot(), kQRow, HP, false);
         if constexpr (KV8) {
           // fp8 cache: this warp owns 32 tokens (rows tb .. tb+31 of a 128-token tile), two
           // 16-row halves that share one softmax update. K and V rows are 128 bytes.

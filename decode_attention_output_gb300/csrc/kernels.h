@@ -62,15 +62,17 @@ struct AttnSmem {
   __host__ __device__ constexpr size_t off_bars() const { return off_merge_ml() + (size_t)kGroupWarps * heads() * 2 * 4; }
   // barriers: full[S], empty[S] (attention); full[8], empty[8], accum[2] (fused projection)
   __host__ __device__ constexpr size_t off_flags() const { return off_bars() + (2 * stages + 18) * 8; }
-  __host__ __device__ constexpr size_t off_prefix() const { return off_flags() + 16; }
+  // flags: int [16]: [0] abort, [1] last CTA of a sequence, [2] last CTA of a column tile (fused
+  // step), [3] TMEM address, [8..15] this CTA's range of tiles and the cursor at its first tile
+  __host__ __device__ constexpr size_t off_prefix() const { return off_flags() + 64; }
   __host__ __device__ constexpr size_t off_lens() const { return off_prefix() + (size_t)(batch + 1) * 4; }
   // paged caches: kIdTiles rows of 16 block ids (one 64-byte TMA box per tile), rows
   // 128 bytes apart (a tensor copy's shared-memory destination is 128-byte aligned)
   __host__ __device__ constexpr size_t off_ids() const { return (off_lens() + (size_t)batch * 4 + 127) & ~(size_t)127; }
   // cluster mode: this CTA's merged states of the sequences it shares with other CTAs of its
   // cluster (slot 0: its first segment, slot 1: its last), read by those CTAs:
-  // O [2][heads][dim], then (m, l) [2][heads][2], then the merge duties int [2][4] and
-  // the equal-lengths flag (int [4] with padding)
+  // O [2][heads][dim], then (m, l) [2][heads][2], then the merge duties int [2][4] (and 16
+  // bytes of padding)
   __host__ __device__ constexpr size_t off_cpart() const { return off_ids() + kIdTiles * kIdStride * 4; }
   __host__ __device__ constexpr size_t cpart_bytes() const { return 2 * (size_t)heads() * (dim + 2) * 4 + 48; }
   // the cluster-mode states only in clusters (at most half as many sequences as SMs)
@@ -163,6 +165,11 @@ struct AttnParams {
   // > 0: each CTA lets the next kernel launch when it reaches the tile this many before the
   // end of its range; 0: right after set-up
   int trigger_at;
+  // floor(n / d) = (n * split_mul) >> split_shift, exact for 0 <= n < 2^31, for the two worker
+  // counts d that split the tiles over the CTAs: [0] min(grid, attn_workers), [1] (cluster
+  // mode) min(that, B * Hkv * cluster). A worker count that differs is divided the plain way.
+  unsigned long long split_mul[2];
+  int split_div[2], split_shift[2];
 };
 constexpr int kMaxAttnCluster = 8;  // portable cluster size
 
