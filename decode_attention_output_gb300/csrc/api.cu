@@ -359,7 +359,10 @@ ClusterUse cluster_use_only(const Options& o) {  // the attention-only entry poi
   return o.attn_cluster ? ClusterUse::kAny : ClusterUse::kNever;
 }
 // decode_attn_fwd: at batch 1 the flat grid gave the faster step (15.0 vs 15.7 us)
-ClusterUse cluster_use_fwd(const Options& o) { return o.attn_cluster ? ClusterUse::kLarge : ClusterUse::kNever; }
+// (2: at every size there too)
+ClusterUse cluster_use_fwd(const Options& o) {
+  return o.attn_cluster == 2 ? ClusterUse::kAny : (o.attn_cluster ? ClusterUse::kLarge : ClusterUse::kNever);
+}
 
 // Clusters of cs attention CTAs resident at once on the current device (cached).
 int max_active_clusters(int cs) {
@@ -861,7 +864,7 @@ int decode_attn_set_option(const char* key, int64_t value) {
   else if (!strcmp(key, "fused_attn_ctas") && value >= 0 && value <= kMaxAttnCtas) g_opt.fused_attn_ctas = value;
   else if (!strcmp(key, "oproj_prefetch") && (value == 0 || value == 1)) g_opt.oproj_prefetch = value;
   else if (!strcmp(key, "oproj_cluster") && (value == 0 || value == 1)) g_opt.oproj_cluster = value;
-  else if (!strcmp(key, "attn_cluster") && (value == 0 || value == 1)) g_opt.attn_cluster = value;
+  else if (!strcmp(key, "attn_cluster") && value >= 0 && value <= 2) g_opt.attn_cluster = value;
   else if (!strcmp(key, "attn_pdl") && (value == 0 || value == 1)) g_opt.attn_pdl = value;
   else if (!strcmp(key, "attn_trigger") && value >= 0 && value <= (1 << 20)) g_opt.attn_trigger = value;
   else if (!strcmp(key, "grid_wait_us") && value >= 0 && value <= 2000000) g_opt.grid_wait_us = value;

@@ -253,8 +253,9 @@ int decode_attn_oproj(const da_tensor_t* attn_flat, const da_tensor_t* o_weight,
  *                   states merge in distributed shared memory; otherwise the tiles
  *                   are split evenly over the whole grid as in the flat mode, and
  *                   only the sequences whose parts fall in one cluster merge on
- *                   chip (the rest through L2). 0: always the flat grid. Results
- *                   agree within the rounding of the merge order.
+ *                   chip (the rest through L2). 2: as 1, and decode_attn_fwd
+ *                   takes clusters at every size too. 0: always the flat grid.
+ *                   Results agree within the rounding of the merge order.
  *   "oproj_cluster" 1 (default): the split-K slices of a tcgen05 column tile form a
  *                   thread-block cluster and reduce in distributed shared memory
  *                   (split-K <= 8); 0: through global partials and an atomic counter

@@ -64,7 +64,7 @@ OPTION_DEFAULTS = {"attn_ctas": 0, "oproj_path": 0, "oproj_splitk": 0, "gemm_min
                    "oproj_cluster": 1, "attn_cluster": 1, "attn_pdl": 1, "attn_trigger": 3, "grid_wait_us": 0,
                    "grid_wait_extra": 0}
 OPTION_BAD = {"attn_ctas": 513, "oproj_path": 4, "pdl": 2, "l2_prefetch": -1, "attn_stages": 5, "fused": 2,
-              "oproj_prefetch": 2, "oproj_cluster": 2, "attn_cluster": 2, "gemm_min_batch": 0, "attn_pdl": 2,
+              "oproj_prefetch": 2, "oproj_cluster": 2, "attn_cluster": 3, "gemm_min_batch": 0, "attn_pdl": 2,
               "attn_trigger": -1, "grid_wait_us": 2000001, "grid_wait_extra": 2}
 
 
