@@ -51,6 +51,8 @@
 //  * fp8 (e4m3) cache: a warp owns 32 tokens (two 16-row halves, one softmax update);
 //    codes are widened to f16 in registers (exact) for f16 MMAs, q and P in f16.
 #pragma once
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -1299,34 +1301,41 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
       if (!ok(np <= cs && cta >= f && cta - f < np && fslot >= 0 && fslot < 2 && sq >= 0 && sq < B * Hkv)) continue;
       const int items = G * DIM, chunk = (items + np - 1) / np, mine = cta - f;
       const int i_end = min(items, (mine + 1) * chunk);
-      for (int item = mine * chunk + tid; item < i_end; item += kThreads) {
-        const int h = item / DIM, d = item - h * DIM;
-        float mv[kMaxAttnCluster], lv[kMaxAttnCluster], ov[kMaxAttnCluster];
+      // NP >= np parts, all loads of an item in flight together (as many as the parts need)
+      auto merge = [&](auto np_max) {
+        constexpr int NP = decltype(np_max)::value;
+        for (int item = mine * chunk + tid; item < i_end; item += kThreads) {
+          const int h = item / DIM, d = item - h * DIM;
+          float mv[NP], lv[NP], ov[NP];
 #pragma unroll
-        for (int q = 0; q < kMaxAttnCluster; ++q) {  // all loads in flight together
-          const int qq = min(q, np - 1);
-          // the first part is in the slot its CTA chose; the others are their CTAs' first segments
-          const uint32_t slot = qq == 0 ? (uint32_t)fslot : 0u;
-          const uint32_t rank = (uint32_t)((f + qq) % cs);
-          mv[q] = ld_cluster_f32(cluster_map(ml_base + 8u * (slot * HP + h), rank));
-          lv[q] = ld_cluster_f32(cluster_map(ml_base + 8u * (slot * HP + h) + 4u, rank));
-          ov[q] = ld_cluster_f32(cluster_map(o_base + 4u * (uint32_t)((slot * HP + h) * DIM + d), rank));
-        }
-        float M = kNegInf;
-#pragma unroll
-        for (int q = 0; q < kMaxAttnCluster; ++q)
-          if (q < np) M = fmaxf(M, mv[q]);  // every part holds a token: finite
-        float lsum = 0.f, acc = 0.f;
-#pragma unroll
-        for (int q = 0; q < kMaxAttnCluster; ++q)
-          if (q < np) {
-            const float w = fast_exp2(mv[q] - M);
-            lsum += w * lv[q];
-            acc += w * ov[q];
+          for (int q = 0; q < NP; ++q) {
+            const int qq = min(q, np - 1);
+            // the first part is in the slot its CTA chose; the others are their CTAs' first segments
+            const uint32_t slot = qq == 0 ? (uint32_t)fslot : 0u;
+            const uint32_t rank = (uint32_t)((f + qq) % cs);
+            mv[q] = ld_cluster_f32(cluster_map(ml_base + 8u * (slot * HP + h), rank));
+            lv[q] = ld_cluster_f32(cluster_map(ml_base + 8u * (slot * HP + h) + 4u, rank));
+            ov[q] = ld_cluster_f32(cluster_map(o_base + 4u * (uint32_t)((slot * HP + h) * DIM + d), rank));
           }
-        if (attn_ok(bq, kq * G + h, d))
-          p.attn[(long long)bq * p.a_sb + (long long)(kq * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
-      }
+          float M = kNegInf;
+#pragma unroll
+          for (int q = 0; q < NP; ++q)
+            if (q < np) M = fmaxf(M, mv[q]);  // every part holds a token: finite
+          float lsum = 0.f, acc = 0.f;
+#pragma unroll
+          for (int q = 0; q < NP; ++q)
+            if (q < np) {
+              const float w = fast_exp2(mv[q] - M);
+              lsum += w * lv[q];
+              acc += w * ov[q];
+            }
+          if (attn_ok(bq, kq * G + h, d))
+            p.attn[(long long)bq * p.a_sb + (long long)(kq * G + h) * p.a_sh + d] = __float2bfloat16_rn(acc / lsum);
+        }
+      };
+      if (np <= 2) merge(std::integral_constant<int, 2>());
+      else if (np <= 4) merge(std::integral_constant<int, 4>());
+      else merge(std::integral_constant<int, kMaxAttnCluster>());
     }
     cluster_sync();  // no CTA leaves while another still reads its shared memory
   }
