@@ -189,6 +189,50 @@ def test_cta_count_does_not_change_the_result(orc, ctas):
     assert np.sqrt(np.sum((a - b) ** 2) / np.sum(b * b)) <= 2e-3
 
 
+def test_range_starts_at_every_kind_of_tile(orc):
+    """The set-up warp computes each CTA's range and the cursor at its first tile, copies the
+    first tile of each consumer group (the second only inside the same sequence), and the
+    consumers read the first segment's q themselves. Sweeping the CTA count moves the range
+    boundaries over every position: a range of one tile, a range that starts on a sequence's
+    last tile (its second tile opens the next sequence and carries q), ranges that start
+    mid-sequence, empty rows between (equal prefix entries), one tile per CTA (more CTAs
+    than tiles). Every split must equal the oracle."""
+    # tiles of 64 tokens per row: 0, 1, 1, 5, 2, 2, 0, 3; two KV heads: 28 tiles
+    w = W("firsttiles", 8, 8, 2, 300, 256, (0, 64, 1, 300, 65, 128, 0, 150))
+    x = synth.make_inputs(w, seed=23, device=DEV)
+    ref_attn, _ = oracle_decode(orc, x)
+    old_ctas, old_cl = da.decode_attn_get_option("attn_ctas"), da.decode_attn_get_option("attn_cluster")
+    try:
+        da.decode_attn_set_option("attn_cluster", 0)
+        for ctas in list(range(1, 31)) + [57]:
+            da.decode_attn_set_option("attn_ctas", ctas)
+            attn = torch.full((w.B, w.Hq, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+            da.decode_attn_only(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], attn, x["scale"])
+            torch.cuda.synchronize()
+            assert da.decode_attn_last_device_error() == 0
+            assert_bf16_close(f64(attn), ref_attn, f"ctas={ctas} attention")
+    finally:
+        da.decode_attn_set_option("attn_ctas", old_ctas)
+        da.decode_attn_set_option("attn_cluster", old_cl)
+
+
+def test_step_with_clusters_at_every_size(orc):
+    """attn_cluster = 2: decode_attn_fwd takes the cluster mode for small problems too."""
+    w = W("fwd_clusters", 1, 32, 8, 2048, 1024, (2048,))
+    x = synth.make_inputs(w, seed=29, device=DEV)
+    _, ref_out = oracle_decode(orc, x)
+    old = da.decode_attn_get_option("attn_cluster")
+    try:
+        da.decode_attn_set_option("attn_cluster", 2)
+        out = torch.full((w.B, w.N), float("nan"), dtype=torch.bfloat16, device=DEV)
+        da.decode_attn_fwd(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], x["o_weight"], out, x["scale"])
+        torch.cuda.synchronize()
+    finally:
+        da.decode_attn_set_option("attn_cluster", old)
+    assert da.decode_attn_last_device_error() == 0
+    assert_bf16_close(f64(out), ref_out, "clusters at batch 1: output")
+
+
 def test_lengths_are_clamped_to_the_cache(orc):
     w = W("clamp", 3, 8, 2, 100, 256, (150, -5, 100))
     x, attn, out = _run(w)

@@ -115,6 +115,24 @@ def test_fp8_cta_counts(orc, ctas):
     assert_bf16_close(f64(out), ref_out, f"ctas={ctas} output")
 
 
+def test_fp8_range_starts_at_every_kind_of_tile(orc):
+    """As for bf16, over 128-token tiles: every CTA count from 1 past the number of tiles
+    (ranges of one tile, ranges starting on a sequence's last tile or mid-sequence, empty
+    rows) equals the oracle."""
+    # tiles of 128 tokens per row: 0, 1, 1, 3, 2; two KV heads: 14 tiles
+    w = W("f8_firsttiles", 5, 8, 2, 300, 256, (0, 128, 1, 300, 129))
+    x = synth.make_inputs(w, seed=41, device=DEV)
+    ref_attn, _ = oracle_fp8(orc, x)
+    old = da.decode_attn_get_option("attn_cluster")
+    try:
+        da.decode_attn_set_option("attn_cluster", 0)
+        for ctas in range(1, 17):
+            attn, _ = run_fp8(w, x, ctas=ctas)
+            assert_bf16_close(f64(attn), ref_attn, f"ctas={ctas} attention")
+    finally:
+        da.decode_attn_set_option("attn_cluster", old)
+
+
 def test_fp8_ones_give_v_scale():
     """V codes = 1.0 and v_scale = 2^-6: every attention output is exactly 2^-6."""
     w = W("f8_ones", 2, 16, 2, 333, 256, (333, 70))
