@@ -16,6 +16,8 @@
 // The split-K slices of a column tile form a thread-block cluster and sum their fp32
 // tiles through distributed shared memory in a fixed order (more than eight slices, on
 // request only: through global partials and the CTA that completes the tile last).
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -172,21 +174,40 @@ __global__ void __launch_bounds__(kUmmaThreads, 2) oproj_umma_kernel(const __gri
     cluster_sync();  // every slice's tile is in its CTA's shared memory
     const int rank = (int)cluster_ctarank();
     const int nb_valid = p.B - b0 < NPAD ? p.B - b0 : NPAD;
-    const int total = nb_valid * kUmmaBM, chunk = (total + p.ksplit - 1) / p.ksplit;
+    // shares of four consecutive outputs (one row of the tile: 128 is a multiple of 4), read
+    // as 16-byte vectors from the slices that exist (2, 4 or at most 8 of them)
+    const int total = nb_valid * kUmmaBM, chunk = ((total + p.ksplit - 1) / p.ksplit + 3) & ~3;
     const int o_end = min(total, (rank + 1) * chunk);
     const uint32_t red_u32 = smem_u32(red);
     const bool red_ok = in_bounds(p.ksplit <= kMaxClusterSplit && rank < p.ksplit && o_end <= NPAD * kUmmaBM, p.err);
-    for (int o = rank * chunk + tid; red_ok && o < o_end; o += kUmmaThreads) {
-      float v[kMaxClusterSplit];
+    auto reduce = [&](auto ks_max) {
+      constexpr int KS = decltype(ks_max)::value;
+      for (int o = rank * chunk + 4 * tid; red_ok && o < o_end; o += 4 * kUmmaThreads) {
+        float4 v[KS];
 #pragma unroll
-      for (int q = 0; q < kMaxClusterSplit; ++q)
-        v[q] = ld_cluster_f32(cluster_map(red_u32 + 4u * o, (uint32_t)min(q, p.ksplit - 1)));
-      float sum = 0.f;
+        for (int q = 0; q < KS; ++q) v[q] = ld_cluster_f32x4(cluster_map(red_u32 + 4u * o, (uint32_t)min(q, p.ksplit - 1)));
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;  // slices added in order
 #pragma unroll
-      for (int q = 0; q < kMaxClusterSplit; ++q) sum += q < p.ksplit ? v[q] : 0.f;
-      const int b = o / kUmmaBM, nn = n0 + o % kUmmaBM;
-      if (nn < p.N && in_bounds(b0 + b < p.B, p.err)) p.y[(long long)(b0 + b) * p.y_sb + nn] = __float2bfloat16_rn(sum);
-    }
+        for (int q = 0; q < KS; ++q)
+          if (q < p.ksplit) {
+            s0 += v[q].x;
+            s1 += v[q].y;
+            s2 += v[q].z;
+            s3 += v[q].w;
+          }
+        const int b = o / kUmmaBM, nn = n0 + o % kUmmaBM;  // nn, N multiples of 4: all four or none
+        if (nn < p.N && in_bounds(b0 + b < p.B, p.err)) {
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(s0, s1), hi = __floats2bfloat162_rn(s2, s3);
+          uint2 pk;
+          pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(p.y + (long long)(b0 + b) * p.y_sb + nn) = pk;
+        }
+      }
+    };
+    if (p.ksplit <= 2) reduce(std::integral_constant<int, 2>());
+    else if (p.ksplit <= 4) reduce(std::integral_constant<int, 4>());
+    else reduce(std::integral_constant<int, kMaxClusterSplit>());
     cluster_sync();  // no CTA leaves while another still reads its shared memory
   } else {
 #pragma unroll
