@@ -18,10 +18,15 @@
 //    CTA emits one partial (m, l, O) per sequence it touches; the CTA that finishes a
 //    sequence last (an atomic completion counter, no waiting) merges the partials with
 //    the log-sum-exp rule and writes bf16.
+//  * Start-up: the set-up warp scans the lengths, computes this CTA's range and the cursor
+//    at its first tile (division by the worker count as a host-computed multiply and shift,
+//    a warp ballot for the batch row) and copies the first tile of each consumer group
+//    itself; the consumers read the range's first q straight from global memory.
 //  * Two producer lanes, one per consumer group (tiles of alternating parity), stream K
 //    and V tiles with one 5-D TMA copy per tile and tensor (the head dim split into
 //    128-byte rows of 64-dim boxes, 128-byte swizzle) into a 4-stage shared-memory ring
-//    guarded by mbarriers; q rows arrive by 1-D bulk copy with a sequence's first tiles.
+//    guarded by mbarriers; q rows arrive by 1-D bulk copy with the first tiles of a
+//    sequence that starts inside the range.
 //    A paged cache is read in boxes of min(block size, tile) tokens, the block ids
 //    arriving by TMA a few tiles ahead.
 //  * Cluster mode (where there is room for two or more CTAs per sequence): the grid is

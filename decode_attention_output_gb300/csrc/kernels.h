@@ -21,7 +21,6 @@ constexpr int kTile = 64;                      // tokens per pipeline stage at D
 constexpr int kGroupWarps = 4;                 // consumer warps per group; each owns 16 tokens of a stage
 constexpr int kGroups = 2;                     // consumer groups take alternate stages
 constexpr int kConsumerThreads = kGroups * kGroupWarps * 32;
-constexpr int kAttnThreads = kConsumerThreads + 32;  // + one TMA producer warp
 // Producer warps of the attention kernel: one per consumer group (each issues the tiles of
 // its group's stages) for a paged cache, where small blocks mean several copies per tile and
 // one lane's issue rate set the pace; for a contiguous cache when kContigTwoProducers.
