@@ -358,6 +358,17 @@ def time_workload(da, w, sets, nb, steps, warmup, dev, stream):
     t_wall1 = time.perf_counter()
     step_ms = ev0.elapsed_time(ev1) / steps
 
+    # the spread of single steps (an event pair around each step, after the timed run): p10,
+    # median and p90
+    sevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        sevs[i][0].record(stream)
+        step(i, stream)
+        sevs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    per_step = sorted(a.elapsed_time(b) * 1e3 for a, b in sevs)
+    step_pct = [per_step[(len(per_step) - 1) * q // 100] for q in (10, 50, 90)]
+
     # the dominant kernel (split-KV attention) alone, per launch, same inputs and plan
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     torch.cuda.synchronize(dev)
@@ -414,7 +425,8 @@ def time_workload(da, w, sets, nb, steps, warmup, dev, stream):
         raise RuntimeError(f"{w.name}: device error during the timed runs")
     attn_bytes = nb["kv"] + w.B * w.Hq * w.D * 2 * 2  # K+V of valid tokens + q in + attention out
     return {"step_ms": step_ms, "graph_us": graph_us, "attn_ms": attn_ms, "attn_ms_eager": attn_ms_eager,
-            "attn_bytes": attn_bytes, "window": (t_wall0, t_wall1), "outs": outs, "step": step}
+            "attn_bytes": attn_bytes, "window": (t_wall0, t_wall1), "outs": outs, "step": step,
+            "step_pct": step_pct}
 
 
 def workload_entry(w, nb, t, peak, clocks, n_sets):
@@ -426,6 +438,7 @@ def workload_entry(w, nb, t, peak, clocks, n_sets):
     return {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "kv_len": w.Lcap, "hidden": w.N, "head_dim": w.D,
             "kv_cache": w.kv, "lens": w.lens, "bytes_per_step": nb["total"],
             "us_per_step": t["step_ms"] * 1e3, "graph_us_per_step": g, "GBps": gbs,
+            "us_per_step_p10_p50_p90": [round(x, 3) for x in t["step_pct"]],
             "frac_of_measured_peak": gbs / peak, "frac_of_8TBps": gbs / NOMINAL_HBM_GBS,
             "graph_GBps": nb["total"] / (g * 1e-6) / 1e9 if isinstance(g, float) else None,
             "attn_us_per_launch": t["attn_ms"] * 1e3, "attn_us_per_launch_eager": t["attn_ms_eager"] * 1e3,
