@@ -518,6 +518,24 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
       prefetch_tensormap(&p.tm_w);
       prefetch_tensormap(&p.tm_x);
     }
+    // The lengths are not known before the wait below, but when every sequence is full (the
+    // cache's capacity) this CTA's first two tiles are those of the split of B * Hkv full
+    // sequences: pull them into L2 now, so that the set-up warp's copies of them come from L2.
+    // (An L2 prefetch only warms the cache, which stays coherent with whatever the previous
+    // kernel writes; a wrong guess costs two tiles of bandwidth.)
+    if constexpr (!PAGED && !kFused) {
+      const int role = warp - kGroups * kGroupWarps;
+      const long long nt = (p.Lcap + kT - 1) / kT, per_b = (long long)p.Hkv * nt, Tg = (long long)p.B * per_b;
+      int workers = min((int)gridDim.x, p.attn_workers);
+      if (p.cluster > 1) workers = min(workers, p.B * p.Hkv * p.cluster);
+      const long long Pg = min((long long)workers, Tg);
+      const long long x = Pg > 0 ? (long long)blockIdx.x * Tg / Pg + role : 0;
+      if (Pg > 0 && blockIdx.x < Pg && x < ((long long)blockIdx.x + 1) * Tg / Pg) {
+        const int b = (int)(x / per_b), r = (int)(x - (long long)b * per_b), kvh = r / (int)nt, j = r - kvh * (int)nt;
+        tma_prefetch_5d(&p.tm_k, 0, j * kT, 0, kvh, b);
+        if (!SCORES) tma_prefetch_5d(&p.tm_v, 0, j * kT, 0, kvh, b);
+      }
+    }
   }
   if (tid == 32) {  // (the set-up warp's first lane: it copies the first tiles, below)
     for (int s = 0; s < S; ++s) {
