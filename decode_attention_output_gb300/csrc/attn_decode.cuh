@@ -519,8 +519,9 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
       prefetch_tensormap(&p.tm_x);
     }
     // The lengths are not known before the wait below, but when every sequence is full (the
-    // cache's capacity) this CTA's first two tiles are those of the split of B * Hkv full
-    // sequences: pull them into L2 now, so that the set-up warp's copies of them come from L2.
+    // cache's capacity) this CTA's first tiles are those of the split of B * Hkv full
+    // sequences: pull the first ring's worth into L2 now (and the first q), so that the first
+    // copies come from L2.
     // (An L2 prefetch only warms the cache, which stays coherent with whatever the previous
     // kernel writes; a wrong guess costs two tiles of bandwidth.)
     if constexpr (!PAGED && !kFused) {
@@ -529,11 +530,15 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
       int workers = min((int)gridDim.x, p.attn_workers);
       if (p.cluster > 1) workers = min(workers, p.B * p.Hkv * p.cluster);
       const long long Pg = min((long long)workers, Tg);
-      const long long x = Pg > 0 ? (long long)blockIdx.x * Tg / Pg + role : 0;
-      if (Pg > 0 && blockIdx.x < Pg && x < ((long long)blockIdx.x + 1) * Tg / Pg) {
+      const long long x0 = Pg > 0 ? (long long)blockIdx.x * Tg / Pg : 0;
+      const long long x1 = Pg > 0 ? ((long long)blockIdx.x + 1) * Tg / Pg : 0;
+      for (long long x = x0 + role; Pg > 0 && blockIdx.x < Pg && x < x1 && x < x0 + S; x += kProducers) {
         const int b = (int)(x / per_b), r = (int)(x - (long long)b * per_b), kvh = r / (int)nt, j = r - kvh * (int)nt;
         tma_prefetch_5d(&p.tm_k, 0, j * kT, 0, kvh, b);
         if (!SCORES) tma_prefetch_5d(&p.tm_v, 0, j * kT, 0, kvh, b);
+        if (x == x0)  // and the q rows of that sequence, which the consumers read first
+          bulk_prefetch_l2(p.q + (long long)b * p.q_sb + (long long)(kvh * p.G) * p.q_sh,
+                           (uint32_t)((((long long)(p.G - 1) * p.q_sh + DIM) * 2 + 15) & ~15ll), l2_policy_evict_last());
       }
     }
   }
