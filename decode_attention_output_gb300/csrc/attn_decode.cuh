@@ -65,6 +65,12 @@ namespace da {
 namespace {
 
 constexpr float kNegInf = -__builtin_huge_valf();
+// Online softmax with a lagging reference: a warp takes its weights 2^(x - m) against a
+// running reference m that moves to the running maximum (rescaling l and O) only when a
+// score of the tile exceeds it by more than kSlack (log2 units). Weights then stay at or
+// below 2^kSlack, and most tiles skip the maximum's shuffle reduction and the rescale.
+// Every merge takes a part's reference as its m: the result does not depend on it.
+constexpr float kSlack = 8.f;
 
 // Position of the current tile in the flattened tile order.
 struct Cursor {
@@ -926,49 +932,61 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
             }
             // ---- online softmax over the 32 tokens (element i of half hh: token
             // 16hh + g + 8(i>>1), head 8nb + 2t + (i&1)); P rounded to f16 for P.V
-            uint32_t pb[2][NB][2];
+            float xv[NB][2][4];
+            bool grow = false;
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-              float xv[2][4];
-              float mx0 = kNegInf, mx1 = kNegInf;
+            for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
                 const bool v0 = 16 * hh + g < vw, v1 = 16 * hh + g + 8 < vw;
-                xv[hh][0] = v0 ? sa[hh][nb][0] * sl2 : kNegInf;
-                xv[hh][1] = v0 ? sa[hh][nb][1] * sl2 : kNegInf;
-                xv[hh][2] = v1 ? sa[hh][nb][2] * sl2 : kNegInf;
-                xv[hh][3] = v1 ? sa[hh][nb][3] * sl2 : kNegInf;
-                mx0 = fmaxf(mx0, fmaxf(xv[hh][0], xv[hh][2]));
-                mx1 = fmaxf(mx1, fmaxf(xv[hh][1], xv[hh][3]));
+                xv[nb][hh][0] = v0 ? sa[hh][nb][0] * sl2 : kNegInf;
+                xv[nb][hh][1] = v0 ? sa[hh][nb][1] * sl2 : kNegInf;
+                xv[nb][hh][2] = v1 ? sa[hh][nb][2] * sl2 : kNegInf;
+                xv[nb][hh][3] = v1 ? sa[hh][nb][3] * sl2 : kNegInf;
+                grow |= fmaxf(xv[nb][hh][0], xv[nb][hh][2]) > m_run[nb][0] + kSlack;
+                grow |= fmaxf(xv[nb][hh][1], xv[nb][hh][3]) > m_run[nb][1] + kSlack;
               }
+            if (__any_sync(0xffffffffu, grow)) {  // the reference moves to the running maximum
 #pragma unroll
-              for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+              for (int nb = 0; nb < NB; ++nb) {
+                float mx0 = fmaxf(fmaxf(xv[nb][0][0], xv[nb][0][2]), fmaxf(xv[nb][1][0], xv[nb][1][2]));
+                float mx1 = fmaxf(fmaxf(xv[nb][0][1], xv[nb][0][3]), fmaxf(xv[nb][1][1], xv[nb][1][3]));
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m_run[nb][0], mx0), mn1 = fmaxf(m_run[nb][1], mx1);
+                const float al0 = fast_exp2(m_run[nb][0] - mn0), al1 = fast_exp2(m_run[nb][1] - mn1);
+                m_run[nb][0] = mn0;
+                m_run[nb][1] = mn1;
+                l_run[nb][0] *= al0;
+                l_run[nb][1] *= al1;
+#pragma unroll
+                for (int mb = 0; mb < 8; ++mb) {
+                  o[mb][nb][0] *= al0;
+                  o[mb][nb][1] *= al1;
+                  o[mb][nb][2] *= al0;
+                  o[mb][nb][3] *= al1;
+                }
               }
-              const float mn0 = fmaxf(m_run[nb][0], mx0), mn1 = fmaxf(m_run[nb][1], mx1);
-              const float al0 = fast_exp2(m_run[nb][0] - mn0), al1 = fast_exp2(m_run[nb][1] - mn1);
-              m_run[nb][0] = mn0;
-              m_run[nb][1] = mn1;
+            }
+            uint32_t pb[2][NB][2];
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              const float m0 = m_run[nb][0], m1 = m_run[nb][1];
               float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
-                const uint32_t r0 = pack_f16x2(fast_exp2(xv[hh][0] - mn0), fast_exp2(xv[hh][1] - mn1));
-                const uint32_t r1 = pack_f16x2(fast_exp2(xv[hh][2] - mn0), fast_exp2(xv[hh][3] - mn1));
+                const uint32_t r0 = pack_f16x2(fast_exp2(xv[nb][hh][0] - m0), fast_exp2(xv[nb][hh][1] - m1));
+                const uint32_t r1 = pack_f16x2(fast_exp2(xv[nb][hh][2] - m0), fast_exp2(xv[nb][hh][3] - m1));
                 ls0 += f16lo_to_f32(r0) + f16lo_to_f32(r1);  // the weights that enter P.V
                 ls1 += f16hi_to_f32(r0) + f16hi_to_f32(r1);
                 pb[hh][nb][0] = movmatrix_trans(r0);  // P[head g][tokens 16hh + 2t, +1]
                 pb[hh][nb][1] = movmatrix_trans(r1);  // P[head g][tokens 16hh + 2t + 8, +9]
               }
-              l_run[nb][0] = l_run[nb][0] * al0 + ls0;
-              l_run[nb][1] = l_run[nb][1] * al1 + ls1;
-#pragma unroll
-              for (int mb = 0; mb < 8; ++mb) {
-                o[mb][nb][0] *= al0;
-                o[mb][nb][1] *= al1;
-                o[mb][nb][2] *= al0;
-                o[mb][nb][3] *= al1;
-              }
+              l_run[nb][0] += ls0;
+              l_run[nb][1] += ls1;
             }
             // ---- O^T += V^T . P^T, one k-step per half. ldmatrix.trans of 16-bit pairs hands
             // a lane tokens 2t, 2t+1 of dims 2g, 2g+1 (a byte each); a byte permute makes
@@ -1043,35 +1061,50 @@ __global__ void __launch_bounds__(attn_threads(attn_producers(PAGED, NPAD > 0, S
               }
           } else {
             const bool v0 = g < vw, v1 = g + 8 < vw;
+            float xs[NB][4];
+            bool grow = false;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              xs[nb][0] = v0 ? s[nb][0] * sl2 : kNegInf;
+              xs[nb][1] = v0 ? s[nb][1] * sl2 : kNegInf;
+              xs[nb][2] = v1 ? s[nb][2] * sl2 : kNegInf;
+              xs[nb][3] = v1 ? s[nb][3] * sl2 : kNegInf;
+              grow |= fmaxf(xs[nb][0], xs[nb][2]) > m_run[nb][0] + kSlack;
+              grow |= fmaxf(xs[nb][1], xs[nb][3]) > m_run[nb][1] + kSlack;
+            }
+            if (__any_sync(0xffffffffu, grow)) {  // the reference moves to the running maximum
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb) {
+                float mx0 = fmaxf(xs[nb][0], xs[nb][2]), mx1 = fmaxf(xs[nb][1], xs[nb][3]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m_run[nb][0], mx0), mn1 = fmaxf(m_run[nb][1], mx1);
+                const float al0 = fast_exp2(m_run[nb][0] - mn0), al1 = fast_exp2(m_run[nb][1] - mn1);
+                m_run[nb][0] = mn0;
+                m_run[nb][1] = mn1;
+                l_run[nb][0] *= al0;
+                l_run[nb][1] *= al1;
+#pragma unroll
+                for (int mb = 0; mb < 8; ++mb) {
+                  o[mb][nb][0] *= al0;
+                  o[mb][nb][1] *= al1;
+                  o[mb][nb][2] *= al0;
+                  o[mb][nb][3] *= al1;
+                }
+              }
+            }
             uint32_t pb[NB][2];
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
-              const float x0 = v0 ? s[nb][0] * sl2 : kNegInf;
-              const float x1 = v0 ? s[nb][1] * sl2 : kNegInf;
-              const float x2 = v1 ? s[nb][2] * sl2 : kNegInf;
-              const float x3 = v1 ? s[nb][3] * sl2 : kNegInf;
-              float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-              for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-              }
-              const float mn0 = fmaxf(m_run[nb][0], mx0), mn1 = fmaxf(m_run[nb][1], mx1);
-              const float al0 = fast_exp2(m_run[nb][0] - mn0), al1 = fast_exp2(m_run[nb][1] - mn1);
-              m_run[nb][0] = mn0;
-              m_run[nb][1] = mn1;
+              const float m0 = m_run[nb][0], m1 = m_run[nb][1];
               // the sum uses the bf16-rounded weights that enter P.V
-              const uint32_t r0 = pack_bf16x2(fast_exp2(x0 - mn0), fast_exp2(x1 - mn1));  // token g
-              const uint32_t r1 = pack_bf16x2(fast_exp2(x2 - mn0), fast_exp2(x3 - mn1));  // token g+8
-              l_run[nb][0] = l_run[nb][0] * al0 + (bf16lo_to_f32(r0) + bf16lo_to_f32(r1));
-              l_run[nb][1] = l_run[nb][1] * al1 + (bf16hi_to_f32(r0) + bf16hi_to_f32(r1));
-#pragma unroll
-              for (int mb = 0; mb < 8; ++mb) {
-                o[mb][nb][0] *= al0;
-                o[mb][nb][1] *= al1;
-                o[mb][nb][2] *= al0;
-                o[mb][nb][3] *= al1;
-              }
+              const uint32_t r0 = pack_bf16x2(fast_exp2(xs[nb][0] - m0), fast_exp2(xs[nb][1] - m1));  // token g
+              const uint32_t r1 = pack_bf16x2(fast_exp2(xs[nb][2] - m0), fast_exp2(xs[nb][3] - m1));  // token g+8
+              l_run[nb][0] += bf16lo_to_f32(r0) + bf16lo_to_f32(r1);
+              l_run[nb][1] += bf16hi_to_f32(r0) + bf16hi_to_f32(r1);
               pb[nb][0] = movmatrix_trans(r0);  // P[head g][tokens 2t, 2t+1]
               pb[nb][1] = movmatrix_trans(r1);  // P[head g][tokens 2t+8, 2t+9]
             }

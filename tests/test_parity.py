@@ -294,6 +294,32 @@ def test_dominant_key_copies_its_value_row():
     assert torch.equal(attn, ref)
 
 
+@pytest.mark.parametrize("rise", [3.0, 30.0, 600.0, -60.0])
+@pytest.mark.parametrize("D", [128, 256])
+def test_running_maximum_moving_along_the_sequence(orc, rise, D):
+    """Scores that rise (or fall) along the sequence by about `rise` log2 units in all (a ramp
+    in dim 0 of K, q[0] = 4): the running reference of the online softmax then moves every
+    few tiles (30), on every tile (600: ~8.7 per 16 tokens), never after the first tile (-60)
+    or hardly at all (3). Every case equals the oracle, on one CTA and on many."""
+    w = synth.Workload("ramp", B=2, Hq=8, Hkv=2, Lcap=1100, N=256, fixed_lens=(1100, 777), D=D)
+    x = synth.make_inputs(w, seed=9, device=DEV)
+    x["q"][..., 0] = 4.0
+    per_unit = 4.0 * x["scale"] * math.log2(math.e)  # log2 units per unit of k[0]
+    ramp = torch.arange(w.Lcap, device=DEV, dtype=torch.float32) * (rise / per_unit / w.Lcap)
+    x["k_cache"][:, :, :, 0] = ramp.to(torch.bfloat16)
+    ref_attn, _ = oracle_decode(orc, x)
+    old = da.decode_attn_get_option("attn_ctas")
+    try:
+        for ctas in (1, 0):
+            da.decode_attn_set_option("attn_ctas", ctas)
+            attn = torch.full((w.B, w.Hq, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+            da.decode_attn_only(x["q"], x["k_cache"], x["v_cache"], x["seq_lens"], attn, x["scale"])
+            torch.cuda.synchronize()
+            assert_bf16_close(f64(attn), ref_attn, f"rise {rise}, D {D}, ctas {ctas}")
+    finally:
+        da.decode_attn_set_option("attn_ctas", old)
+
+
 # ------------------------------------------------------------- fp32 scores
 @pytest.mark.parametrize("G,Hkv", [(4, 2), (8, 1), (16, 1), (3, 2)])
 def test_scores_match_oracle(orc, G, Hkv):

@@ -133,6 +133,26 @@ def test_fp8_range_starts_at_every_kind_of_tile(orc):
         da.decode_attn_set_option("attn_cluster", old)
 
 
+@pytest.mark.parametrize("rise", [3.0, 30.0, 600.0, -60.0])
+def test_fp8_running_maximum_moving_along_the_sequence(orc, rise):
+    """As for bf16: a ramp in dim 0 of the K codes (k_scale 1, q[0] = 16) makes the scores rise
+    or fall along the sequence by about `rise` log2 units, so that the running reference of the
+    online softmax moves every few tiles, on every tile (600: ~17 per warp's 32 tokens), never
+    after the first or hardly at all; each equals the oracle on one CTA and on many."""
+    w = W("f8_ramp", 2, 8, 2, 1100, 256, (1100, 777))
+    x = synth.make_inputs(w, seed=9, device=DEV)
+    x["q"][..., 0] = 16.0
+    x["k_scale"] = 1.0
+    per_unit = 16.0 * x["scale"] * np.log2(np.e)
+    kc = x["k_cache"].float()
+    kc[:, :, :, 0] = torch.arange(w.Lcap, device=DEV, dtype=torch.float32) * (rise / per_unit / w.Lcap)
+    x["k_cache"] = kc.to(torch.float8_e4m3fn)
+    ref_attn, _ = oracle_fp8(orc, x)
+    for ctas in (1, 0):
+        attn, _ = run_fp8(w, x, ctas=ctas)
+        assert_bf16_close(f64(attn), ref_attn, f"rise {rise}, ctas {ctas}")
+
+
 def test_fp8_ones_give_v_scale():
     """V codes = 1.0 and v_scale = 2^-6: every attention output is exactly 2^-6."""
     w = W("f8_ones", 2, 16, 2, 333, 256, (333, 70))
