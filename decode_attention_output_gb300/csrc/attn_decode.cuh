@@ -41,9 +41,10 @@
 //    in compute at once per SM. Each warp owns 16 tokens of a stage and all G
 //    query heads of the group (every K/V byte is read once). S^T = K . Q^T runs
 //    on mma.sync m16n8k16 with tokens as M and heads as N (G <= 8 fills one
-//    8-wide N block); the online softmax runs in registers (running max / sum,
-//    shuffle reductions, exp2 with scale*log2e folded); P is rounded to bf16 and
-//    moved into the B-operand layout with movmatrix; O^T = V^T . P^T accumulates
+//    8-wide N block); the online softmax runs in registers (a lagging reference
+//    maximum, see kSlack, a running sum, exp2 with scale*log2e folded); P is
+//    rounded to bf16 and moved into the B-operand layout with movmatrix;
+//    O^T = V^T . P^T accumulates
 //    in fp32 registers. At the end of a sequence segment the eight warps' states
 //    are merged (pairwise in registers, then across four warps in shared memory).
 //  * D = 256 (a GQA decode whose QK^T contracts D in two 128-wide halves and whose
