@@ -68,6 +68,7 @@ CASES = [
     W("f8_g1_mha", 2, 4, 4, 100, 128, (100, 16)),
     W("f8_g3", 2, 6, 2, 257, 264, (257, 130)),
     W("f8_g5_sharp", 2, 10, 2, 190, 640, (190, 33), k_mult=2.0),
+    W("f8_g4_very_sharp", 2, 8, 2, 700, 256, (700, 77), k_mult=60.0),
     W("f8_zero_len", 3, 8, 2, 130, 256, (0, 130, 65)),
     W("f8_tiny", 1, 2, 1, 1, 8, (1,)),
     W("f8_tile_plus_one", 1, 8, 2, 65, 256, (65,)),
